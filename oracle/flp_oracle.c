@@ -1,0 +1,307 @@
+/*
+ * flp_oracle.c - plain, slow, fp64 CPU reference for the fused linear
+ * log-prob / cross-entropy LM head.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the tests, the smoke check and the bench's
+ * CPU-baseline leg may load this library.  It shares no code, header, table or
+ * helper with the CUDA path, and the CUDA path never calls it.
+ *
+ * What it computes is the plain definition of the method, with every logit
+ * materialised in fp64:
+ *
+ *   z_ij       = s * sum_k X_ik W_jk                      (scaled classifier GEMM)
+ *   LSE_i      = log sum_j exp(z_ij)
+ *   p_ij       = exp(z_ij - LSE_i)
+ *   logprob_i  = z_{i,y_i} - LSE_i
+ *   entropy_i  = LSE_i - sum_j p_ij z_ij
+ *   dZ_ij      = s * [ g_lp_i (1[j = y_i] - p_ij) + g_ent_i p_ij (sum_k p_ik z_ik - z_ij) ]
+ *   dX         = dZ W,     dW = dZ^T X
+ *
+ * Sources (the pages are web text; each function below names the passage it
+ * follows):
+ *  - "Triton MoE improvements and chunked GRPO improvements" (Liger-Kernel
+ *    pull request 1294), section "Chunked Triton GRPO loss": the lm_head
+ *    projection fused into the loss with an online logsumexp, so the logits
+ *    are never stored; "Kernel design notes": the backward recomputes the
+ *    logits tiles into grad_logits, then grad_hidden = grad_logits . W and
+ *    grad_weight += grad_logits^T . hidden.
+ *  - Liger-Kernel v0.8.3 test/transformers page (the native SM100 fused scaled
+ *    linear cross-entropy commit), section "Summary": classifier GEMM fused
+ *    with NLL/LSE and optional entropy; "Correctness": ignored targets.
+ *  - "perf(megatron): autotune fused LM-head Triton kernels" (SkyRL pull
+ *    request 2141), sections "Summary" and "Overview": optional entropy,
+ *    log-sum-exp started from the true row maximum (-inf initialisation).
+ *
+ * Readings taken where the pages are silent (each is also listed in the
+ * design notes of the repository):
+ *  - the scale s multiplies the fp32/fp64 accumulator, so every output is over
+ *    the scaled logits and the gradients carry the factor s;
+ *  - a row whose target equals ignore_index has logprob = 0, entropy = 0 and a
+ *    zero dZ row; its LSE is still reported;
+ *  - a target outside [0, V) that is not ignore_index is a contract violation:
+ *    logprob is NaN for that row and the call returns FLPO_BAD_TARGET;
+ *  - grad_logprob is the upstream gradient of logprob (not of the NLL), so
+ *    dZ carries g_lp * (onehot - p);
+ *  - with compute_entropy = 0 no entropy is produced and g_ent is ignored.
+ *
+ * No blocking, fusion or reordering beyond the definitions: each row's logits
+ * are formed in full, the max shift is the textbook one, and the GEMMs are
+ * plain triple loops.  OpenMP only splits independent rows (or, for dW,
+ * independent vocabulary rows).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define FLPO_OK 0
+#define FLPO_BAD_TARGET 5
+#define FLPO_INVALID_ARG 1
+#define FLPO_NO_MEMORY 7
+
+/* Element type of an input matrix. */
+#define FLPO_BF16 1
+#define FLPO_F64 2
+
+/* bf16 is the upper half of an IEEE binary32; widening is exact. */
+static double bf16_to_double(uint16_t h) {
+    uint32_t bits = ((uint32_t)h) << 16;
+    float f;
+    memcpy(&f, &bits, sizeof f);
+    return (double)f;
+}
+
+/* Round a binary32 to bf16, round-to-nearest-even (NaN kept quiet). */
+static uint16_t float_to_bf16_rne(float f) {
+    uint32_t bits;
+    memcpy(&bits, &f, sizeof bits);
+    if ((bits & 0x7f800000u) == 0x7f800000u && (bits & 0x007fffffu) != 0)
+        return (uint16_t)((bits >> 16) | 0x0040u);
+    uint32_t lsb = (bits >> 16) & 1u;
+    bits += 0x7fffu + lsb;
+    return (uint16_t)(bits >> 16);
+}
+
+static double get_elem(const void* base, int type, int64_t idx) {
+    if (type == FLPO_BF16) return bf16_to_double(((const uint16_t*)base)[idx]);
+    return ((const double*)base)[idx];
+}
+
+/* z_j = s * <X_i, W_j> for every j in [0, V): the full, materialised logit row. */
+static void logits_row(const void* X, const void* W, int type, int64_t i, int64_t H,
+                       int64_t V, double s, double* xrow, double* z) {
+    for (int64_t k = 0; k < H; ++k) xrow[k] = get_elem(X, type, i * H + k);
+    for (int64_t j = 0; j < V; ++j) {
+        double acc = 0.0;
+        for (int64_t k = 0; k < H; ++k) acc += xrow[k] * get_elem(W, type, j * H + k);
+        z[j] = s * acc;
+    }
+}
+
+/* Per-row statistics from the materialised row, by definition.
+ * The max shift starts from the true row maximum, as the SkyRL page's
+ * "Correctness" section prescribes for strongly negative rows. */
+typedef struct {
+    double lse;
+    double sum_pz; /* sum_j p_j z_j */
+} row_stats;
+
+static row_stats stats_from_logits(const double* z, int64_t V) {
+    double m = -INFINITY;
+    for (int64_t j = 0; j < V; ++j)
+        if (z[j] > m) m = z[j];
+    double se = 0.0;
+    for (int64_t j = 0; j < V; ++j) se += exp(z[j] - m);
+    row_stats r;
+    r.lse = m + log(se);
+    double spz = 0.0;
+    for (int64_t j = 0; j < V; ++j) spz += exp(z[j] - r.lse) * z[j];
+    r.sum_pz = spz;
+    return r;
+}
+
+static int target_ok(int64_t y, int64_t V) { return y >= 0 && y < V; }
+
+/*
+ * Forward outputs for the rows listed in `rows` (all rows when rows == NULL).
+ * Output k belongs to row rows[k].  entropy may be NULL when compute_entropy
+ * is 0.  Follows the Liger-Kernel native commit's "Summary" (NLL/LSE and
+ * optional entropy) and the SkyRL page's "Overview" (entropy optional).
+ */
+static int forward_impl(const void* X, const void* W, int type, const int64_t* y, int64_t M,
+                        int64_t H, int64_t V, int64_t ignore_index, double s,
+                        int compute_entropy, const int64_t* rows, int64_t nrows,
+                        double* logprob, double* lse, double* entropy) {
+    if (M < 0 || H < 1 || V < 1 || nrows < 0) return FLPO_INVALID_ARG;
+    if (rows == NULL && nrows != M) return FLPO_INVALID_ARG;
+    int status = FLPO_OK;
+#pragma omp parallel
+    {
+        double* xrow = (double*)malloc(sizeof(double) * (size_t)H);
+        double* z = (double*)malloc(sizeof(double) * (size_t)V);
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t k = 0; k < nrows; ++k) {
+            int64_t i = rows ? rows[k] : k;
+            if (i < 0 || i >= M) {
+#pragma omp atomic write
+                status = FLPO_INVALID_ARG;
+                continue;
+            }
+            logits_row(X, W, type, i, H, V, s, xrow, z);
+            row_stats st = stats_from_logits(z, V);
+            if (lse) lse[k] = st.lse;
+            double lp, ent = st.lse - st.sum_pz;
+            if (y[i] == ignore_index) {
+                lp = 0.0;
+                ent = 0.0;
+            } else if (!target_ok(y[i], V)) {
+                lp = NAN;
+#pragma omp atomic write
+                status = FLPO_BAD_TARGET;
+            } else {
+                lp = z[y[i]] - st.lse;
+            }
+            if (logprob) logprob[k] = lp;
+            if (compute_entropy && entropy) entropy[k] = ent;
+        }
+        free(xrow);
+        free(z);
+    }
+    return status;
+}
+
+/*
+ * Backward for the rows listed in `rows` (all rows when rows == NULL): every
+ * listed row's logits are recomputed (the "Kernel design notes" of the chunked
+ * GRPO page), its dZ row is formed from the definition above, and
+ *   dX_rows[k, :] = sum_j dZ[rows[k], j] W[j, :]        (when dX_rows != NULL)
+ *   dW[j, :]      = sum_k dZ[rows[k], j] X[rows[k], :]  (when dW != NULL)
+ * Rows that are not listed contribute nothing to dW, which equals a backward
+ * whose upstream gradients are zero on those rows.
+ *
+ * round_dz_bf16 = 1 rounds each dZ value to fp32 and then to bf16 (RNE) before
+ * the two contractions, mirroring the rounding point of the bf16 GEMM operands
+ * that the chunked PPO backward of the same page adopts; 0 keeps fp64.
+ */
+static int backward_impl(const void* X, const void* W, int type, const int64_t* y, int64_t M,
+                         int64_t H, int64_t V, int64_t ignore_index, double s,
+                         int compute_entropy, const double* g_lp, const double* g_ent,
+                         const int64_t* rows, int64_t nrows, int round_dz_bf16,
+                         double* dX_rows, double* dW) {
+    if (M < 0 || H < 1 || V < 1 || nrows < 0) return FLPO_INVALID_ARG;
+    if (rows == NULL && nrows != M) return FLPO_INVALID_ARG;
+    for (int64_t k = 0; k < nrows; ++k) {
+        int64_t i = rows ? rows[k] : k;
+        if (i < 0 || i >= M) return FLPO_INVALID_ARG;
+    }
+    double* dZ = (double*)malloc(sizeof(double) * (size_t)(nrows > 0 ? nrows : 1) * (size_t)V);
+    if (!dZ) return FLPO_NO_MEMORY;
+    int status = FLPO_OK;
+#pragma omp parallel
+    {
+        double* xrow = (double*)malloc(sizeof(double) * (size_t)H);
+        double* z = (double*)malloc(sizeof(double) * (size_t)V);
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t k = 0; k < nrows; ++k) {
+            int64_t i = rows ? rows[k] : k;
+            double* dz = dZ + k * V;
+            double glp = g_lp ? g_lp[i] : 0.0;
+            double gent = (compute_entropy && g_ent) ? g_ent[i] : 0.0;
+            if (y[i] == ignore_index) {
+                for (int64_t j = 0; j < V; ++j) dz[j] = 0.0;
+                continue;
+            }
+            if (!target_ok(y[i], V)) {
+#pragma omp atomic write
+                status = FLPO_BAD_TARGET;
+            }
+            logits_row(X, W, type, i, H, V, s, xrow, z);
+            row_stats st = stats_from_logits(z, V);
+            for (int64_t j = 0; j < V; ++j) {
+                double p = exp(z[j] - st.lse);
+                double onehot = (j == y[i]) ? 1.0 : 0.0;
+                dz[j] = s * (glp * (onehot - p) + gent * p * (st.sum_pz - z[j]));
+            }
+            if (round_dz_bf16)
+                for (int64_t j = 0; j < V; ++j)
+                    dz[j] = bf16_to_double(float_to_bf16_rne((float)dz[j]));
+        }
+        free(xrow);
+        free(z);
+    }
+    if (dX_rows) {
+#pragma omp parallel for schedule(dynamic, 1)
+        for (int64_t k = 0; k < nrows; ++k) {
+            const double* dz = dZ + k * V;
+            double* out = dX_rows + k * H;
+            for (int64_t h = 0; h < H; ++h) out[h] = 0.0;
+            for (int64_t j = 0; j < V; ++j) {
+                if (dz[j] == 0.0) continue;
+                for (int64_t h = 0; h < H; ++h) out[h] += dz[j] * get_elem(W, type, j * H + h);
+            }
+        }
+    }
+    if (dW) {
+#pragma omp parallel for schedule(dynamic, 16)
+        for (int64_t j = 0; j < V; ++j) {
+            double* out = dW + j * H;
+            for (int64_t h = 0; h < H; ++h) out[h] = 0.0;
+            for (int64_t k = 0; k < nrows; ++k) {
+                int64_t i = rows ? rows[k] : k;
+                double d = dZ[k * V + j];
+                if (d == 0.0) continue;
+                for (int64_t h = 0; h < H; ++h) out[h] += d * get_elem(X, type, i * H + h);
+            }
+        }
+    }
+    free(dZ);
+    return status;
+}
+
+/* ---- exported entry points (ctypes) ---- */
+
+int flpo_forward_bf16(const uint16_t* X, const uint16_t* W, const int64_t* y, int64_t M,
+                      int64_t H, int64_t V, int64_t ignore_index, double s,
+                      int compute_entropy, const int64_t* rows, int64_t nrows,
+                      double* logprob, double* lse, double* entropy) {
+    return forward_impl(X, W, FLPO_BF16, y, M, H, V, ignore_index, s, compute_entropy, rows,
+                        nrows, logprob, lse, entropy);
+}
+
+int flpo_forward_f64(const double* X, const double* W, const int64_t* y, int64_t M, int64_t H,
+                     int64_t V, int64_t ignore_index, double s, int compute_entropy,
+                     const int64_t* rows, int64_t nrows, double* logprob, double* lse,
+                     double* entropy) {
+    return forward_impl(X, W, FLPO_F64, y, M, H, V, ignore_index, s, compute_entropy, rows,
+                        nrows, logprob, lse, entropy);
+}
+
+int flpo_backward_bf16(const uint16_t* X, const uint16_t* W, const int64_t* y, int64_t M,
+                       int64_t H, int64_t V, int64_t ignore_index, double s,
+                       int compute_entropy, const double* g_lp, const double* g_ent,
+                       const int64_t* rows, int64_t nrows, int round_dz_bf16, double* dX_rows,
+                       double* dW) {
+    return backward_impl(X, W, FLPO_BF16, y, M, H, V, ignore_index, s, compute_entropy, g_lp,
+                         g_ent, rows, nrows, round_dz_bf16, dX_rows, dW);
+}
+
+int flpo_backward_f64(const double* X, const double* W, const int64_t* y, int64_t M,
+                      int64_t H, int64_t V, int64_t ignore_index, double s,
+                      int compute_entropy, const double* g_lp, const double* g_ent,
+                      const int64_t* rows, int64_t nrows, int round_dz_bf16, double* dX_rows,
+                      double* dW) {
+    return backward_impl(X, W, FLPO_F64, y, M, H, V, ignore_index, s, compute_entropy, g_lp,
+                         g_ent, rows, nrows, round_dz_bf16, dX_rows, dW);
+}
+
+/* Threads OpenMP will use for the parallel regions above. */
+int flpo_num_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
