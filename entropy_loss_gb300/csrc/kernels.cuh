@@ -1,0 +1,648 @@
+// kernels.cuh - sm_103a kernels of the fused linear log-prob / cross-entropy head.
+//
+// One warp-specialised, persistent tile kernel serves the four contractions of
+// the path; a mode template parameter selects the operand layouts and the
+// epilogue:
+//
+//   kFwd : z = s X W^T tiles -> online max / sum-exp / (entropy) / target
+//          pick per row, raw per-split partials (forward, fused epilogue)
+//   kDz  : z tiles recomputed -> dZ = s[g_lp(onehot - p) + g_ent p(sum pz - z)]
+//          rounded to bf16, TMA-stored into the wave's dZ buffer
+//   kDx  : dX[wave] = dZ W          (A = dZ K-major, B = W MN-major)
+//   kDw  : dW (+)= dZ^T X[wave]     (A = dZ MN-major, B = X MN-major)
+//
+// Roles (192 threads, one CTA per SM):
+//   warp 0      TMA producer (one elected lane)
+//   warp 1      TMEM allocator and tcgen05.mma issuer (one elected lane)
+//   warps 2..5  epilogue: thread == accumulator row (TMEM lane), 4 x 32 lanes
+// Accumulators: two 128 x 256 fp32 buffers in TMEM (512 columns), so the
+// epilogue of one tile overlaps the MMAs of the next.
+// Operand tiles: 128 rows (A) and 256 rows (B) by 64 bf16 (one 128-byte
+// swizzle atom) per pipeline stage, moved by TMA into 1024-byte aligned shared
+// memory in the canonical 128B-swizzled layouts that the smem descriptors name.
+//
+// Every mbarrier wait is bounded (globaltimer); on expiry the kernel raises the
+// timeout bit in the error word, stops issuing work, waits (bounded) for its own
+// copies and MMAs in flight, frees its TMEM and returns.
+#pragma once
+#include <cstdint>
+#include <cuda.h>
+#include "ptx.cuh"
+
+namespace flp {
+
+constexpr int BM = 128;           // rows per tile (UMMA M)
+constexpr int BN = 256;           // columns per tile (UMMA N)
+constexpr int BK = 64;            // K per pipeline stage
+constexpr int UMMA_K = 16;        // K per tcgen05.mma (bf16)
+constexpr int STAGES = 4;
+constexpr int NUM_THREADS = 192;
+constexpr int EPI_THREADS = 128;
+constexpr uint32_t TMEM_COLS = 512;
+
+constexpr uint32_t A_STAGE_BYTES = BM * BK * 2;    // 16 KiB
+constexpr uint32_t B_STAGE_BYTES = BN * BK * 2;    // 32 KiB
+constexpr uint32_t STAGE_TX = A_STAGE_BYTES + B_STAGE_BYTES;
+constexpr uint32_t STG_BYTES = 128 * 128;          // one 128-row x 128-byte store box
+constexpr uint32_t NUM_STG = 2;
+
+constexpr int ERR_BAD_TARGET = 1;
+constexpr int ERR_TIMEOUT = 2;
+
+constexpr float LOG2E = 1.4426950408889634f;
+constexpr float LN2 = 0.6931471805599453f;
+
+enum Mode : int { kFwd = 0, kDz = 1, kDx = 2, kDw = 3 };
+
+// Offsets inside the (1024-byte aligned) dynamic shared memory block.
+constexpr uint32_t SMEM_A = 0;
+constexpr uint32_t SMEM_B = SMEM_A + STAGES * A_STAGE_BYTES;
+constexpr uint32_t SMEM_STG = SMEM_B + STAGES * B_STAGE_BYTES;
+constexpr uint32_t SMEM_BAR = SMEM_STG + NUM_STG * STG_BYTES;
+constexpr uint32_t NUM_BARS = 2 * STAGES + 4 + 1;
+constexpr uint32_t SMEM_MISC = SMEM_BAR + NUM_BARS * 8;
+constexpr uint32_t SMEM_TOTAL = SMEM_MISC + 16;
+constexpr uint32_t SMEM_ALLOC = SMEM_TOTAL + 1024;  // slack for 1024-byte alignment
+
+struct TileParams {
+    // schedule: units are runs [n0, n1) of N-tiles that share one M-tile
+    int units, Mt, Nt, S, tps, GM;
+    int KB;  // K blocks of 64
+    // problem
+    int M;     // valid rows of this launch (all rows for kFwd, the wave's rows otherwise)
+    int V;     // vocabulary size (kFwd / kDz column mask)
+    int row0;  // first global row of the wave (kDz)
+    long long ignore_index;
+    float scale;   // s
+    float scale2;  // s * log2(e)
+    int compute_entropy;
+    int dw_add;  // kDw: 0 = TMA store, 1 = TMA reduce-add into dW
+    const long long* y;
+    const float* lse;
+    const float* ent;
+    const float* g_lp;
+    const float* g_ent;
+    float* part_m;
+    float* part_s;
+    float* part_t;
+    float* zy;
+    int* err;
+    unsigned long long wait_limit_ns;
+    int debug_stall_after;  // < 0: off; else the producer stops after this many stages
+};
+
+struct Unit {
+    int mt, n0, n1, split;
+};
+
+__device__ __forceinline__ Unit decode_unit(const TileParams& p, int u) {
+    const int per_group = p.GM * p.S;
+    const int g = u / per_group;
+    const int first_m = g * p.GM;
+    const int gm = min(p.GM, p.Mt - first_m);
+    const int r = u - g * per_group;
+    Unit t;
+    t.split = r / gm;
+    t.mt = first_m + (r - t.split * gm);
+    t.n0 = t.split * p.tps;
+    t.n1 = min(p.Nt, t.n0 + p.tps);
+    return t;
+}
+
+template <int kMode>
+struct ModeCfg {
+    static constexpr int a_mn = (kMode == kDw) ? 1 : 0;
+    static constexpr int b_mn = (kMode == kDx || kMode == kDw) ? 1 : 0;
+    static constexpr uint32_t idesc = idesc_bf16_f32(BM, BN, a_mn, b_mn);
+};
+
+// ----------------------------------------------------------------- producer
+
+template <int kMode>
+__device__ __forceinline__ void issue_stage_loads(const CUtensorMap* tmA, const CUtensorMap* tmB,
+                                                  uint8_t* a_dst, uint8_t* b_dst, uint64_t* bar,
+                                                  int mt, int nt, int kb) {
+    if constexpr (ModeCfg<kMode>::a_mn == 0) {
+        tma_load_2d(a_dst, tmA, kb * BK, mt * BM, bar);  // box: 64 k x 128 rows
+    } else {
+#pragma unroll
+        for (int j = 0; j < BM / 64; ++j)  // box: 64 m x 64 k rows, one per 64-wide MN atom
+            tma_load_2d(a_dst + j * 8192, tmA, mt * BM + j * 64, kb * BK, bar);
+    }
+    if constexpr (ModeCfg<kMode>::b_mn == 0) {
+        tma_load_2d(b_dst, tmB, kb * BK, nt * BN, bar);  // box: 64 k x 256 rows
+    } else {
+#pragma unroll
+        for (int j = 0; j < BN / 64; ++j)
+            tma_load_2d(b_dst + j * 8192, tmB, nt * BN + j * 64, kb * BK, bar);
+    }
+}
+
+// Operand descriptors for UMMA step k (0..3) inside a 64-deep stage.
+template <int kMN>
+__device__ __forceinline__ uint64_t operand_desc(uint32_t base, int k) {
+    if constexpr (kMN == 0)
+        return sdesc_sw128(base + k * (UMMA_K * 2), 16, 1024);  // K-major: advance 32 B in the atom
+    else
+        return sdesc_sw128(base + k * (UMMA_K * 128), 8192, 1024);  // MN-major: advance 16 rows
+}
+
+// ------------------------------------------------------------ epilogue pieces
+
+// v[idx] for a thread-dependent idx in [0, 32) through a 5-level select tree,
+// so the 32 values stay in registers (no dynamically indexed local array).
+__device__ __forceinline__ float select32(const uint32_t (&v)[32], int idx) {
+    uint32_t a[16], b[8], c[4], d[2];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) a[j] = (idx & 16) ? v[j + 16] : v[j];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) b[j] = (idx & 8) ? a[j + 8] : a[j];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) c[j] = (idx & 4) ? b[j + 4] : b[j];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) d[j] = (idx & 2) ? c[j + 2] : c[j];
+    return __uint_as_float((idx & 1) ? d[1] : d[0]);
+}
+
+// Write 8 x 16-byte chunks of one row into a 128B-swizzled 128-row box.
+__device__ __forceinline__ void stage_row(uint32_t box_base, int r, const uint32_t (&w)[32]) {
+    const uint32_t row_addr = box_base + r * 128;
+#pragma unroll
+    for (int c = 0; c < 8; ++c)
+        st_shared_v4(row_addr + ((c ^ (r & 7)) << 4), w[4 * c], w[4 * c + 1], w[4 * c + 2],
+                     w[4 * c + 3]);
+}
+
+// Bookkeeping of the two store boxes: before reusing a box wait until the
+// bulk store that last read it has finished reading.
+struct StoreRing {
+    uint32_t n = 0;
+};
+
+__device__ __forceinline__ uint32_t store_box_acquire(StoreRing& ring, uint8_t* smem, int et) {
+    const uint32_t buf = ring.n & 1u;
+    if (ring.n >= NUM_STG) {
+        if (et == 0) bulk_wait_group_read<NUM_STG - 1>();
+        named_bar_sync(1, EPI_THREADS);
+    }
+    return smem_addr(smem + SMEM_STG + buf * STG_BYTES);
+}
+
+template <int kMode>
+__device__ __forceinline__ void store_box_release(StoreRing& ring, uint8_t* smem, int et,
+                                                  const CUtensorMap* tmOut, int x, int y,
+                                                  bool add) {
+    const uint32_t buf = ring.n & 1u;
+    fence_proxy_async_smem();
+    named_bar_sync(1, EPI_THREADS);
+    if (et == 0) {
+        const void* src = smem + SMEM_STG + buf * STG_BYTES;
+        if (add)
+            tma_reduce_add_2d(tmOut, src, x, y);
+        else
+            tma_store_2d(tmOut, src, x, y);
+        bulk_commit_group();
+    }
+    ring.n++;
+}
+
+// ------------------------------------------------------------------- kernel
+
+template <int kMode, bool kEnt, bool kOutF32>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    flp_tile_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                    const __grid_constant__ CUtensorMap tmOut, const TileParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + SMEM_BAR);
+    uint64_t* full = bars;
+    uint64_t* empty = bars + STAGES;
+    uint64_t* tfull = bars + 2 * STAGES;
+    uint64_t* tempty = bars + 2 * STAGES + 2;
+    uint64_t* drain = bars + 2 * STAGES + 4;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + SMEM_MISC);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + SMEM_MISC + 4);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(&tfull[a], 1);
+            mbar_init(&tempty[a], EPI_THREADS);
+        }
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        fence_mbarrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+        if constexpr (kMode != kFwd) tma_prefetch_desc(&tmOut);
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    const uint64_t limit = p.wait_limit_ns;
+
+    if (warp == 0) {
+        // ------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t issued_mask = 0, issued_parity = 0;
+            long long issued = 0;
+            bool ok = true;
+            for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
+                const Unit t = decode_unit(p, u);
+                for (int nt = t.n0; nt < t.n1 && ok; ++nt) {
+                    for (int kb = 0; kb < p.KB; ++kb) {
+                        if (p.debug_stall_after >= 0 && issued >= p.debug_stall_after) {
+                            ok = false;  // injected stall: stop feeding the MMA warp
+                            break;
+                        }
+                        if (!mbar_wait(&empty[stage], phase ^ 1u, limit, abort_flag)) {
+                            ok = false;
+                            break;
+                        }
+                        mbar_arrive_expect_tx(&full[stage], STAGE_TX);
+                        issue_stage_loads<kMode>(&tmA, &tmB, smem + SMEM_A + stage * A_STAGE_BYTES,
+                                                 smem + SMEM_B + stage * B_STAGE_BYTES,
+                                                 &full[stage], t.mt, nt, kb);
+                        issued_mask |= 1u << stage;
+                        issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+                        ++issued;
+                        if (++stage == STAGES) {
+                            stage = 0;
+                            phase ^= 1u;
+                        }
+                    }
+                }
+            }
+            if (!ok && p.debug_stall_after < 0) {
+                atomicOr(p.err, ERR_TIMEOUT);
+                *abort_flag = 1;
+            }
+            // Wait (bounded) for every load this thread issued to land before
+            // the CTA can exit and its shared memory be reused.
+            for (int s = 0; s < STAGES; ++s)
+                if (issued_mask & (1u << s)) {
+                    volatile int no_abort = 0;
+                    mbar_wait(&full[s], (issued_parity >> s) & 1u, limit, &no_abort);
+                }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            int acc = 0;
+            uint32_t acc_phase = 0;
+            bool ok = true;
+            constexpr uint32_t idesc = ModeCfg<kMode>::idesc;
+            for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
+                const Unit t = decode_unit(p, u);
+                for (int nt = t.n0; nt < t.n1 && ok; ++nt) {
+                    if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, limit, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+                    for (int kb = 0; kb < p.KB; ++kb) {
+                        if (!mbar_wait(&full[stage], phase, limit, abort_flag)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t a_base = smem_addr(smem + SMEM_A + stage * A_STAGE_BYTES);
+                        const uint32_t b_base = smem_addr(smem + SMEM_B + stage * B_STAGE_BYTES);
+#pragma unroll
+                        for (int k = 0; k < BK / UMMA_K; ++k) {
+                            umma_bf16(d_tmem, operand_desc<ModeCfg<kMode>::a_mn>(a_base, k),
+                                      operand_desc<ModeCfg<kMode>::b_mn>(b_base, k), idesc,
+                                      (kb > 0 || k > 0) ? 1u : 0u);
+                        }
+                        umma_commit(&empty[stage]);  // frees the smem stage once read
+                        if (++stage == STAGES) {
+                            stage = 0;
+                            phase ^= 1u;
+                        }
+                    }
+                    if (!ok) break;
+                    umma_commit(&tfull[acc]);  // accumulator ready for the epilogue
+                    acc ^= 1;
+                    if (acc == 0) acc_phase ^= 1u;
+                }
+            }
+            if (!ok) {
+                atomicOr(p.err, ERR_TIMEOUT);
+                *abort_flag = 1;
+            }
+            // Every MMA this thread issued completes before TMEM is freed.
+            umma_commit(drain);
+            volatile int no_abort = 0;
+            mbar_wait(drain, 0, limit, &no_abort);
+        }
+    } else {
+        // --------------------------------------------------------- epilogue
+        const int et = threadIdx.x - 64;         // 0..127
+        const int q = warp & 3;                  // TMEM lane quadrant of this warp
+        const int r = q * 32 + lane;             // accumulator row == TMEM lane
+        const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        bool ok = true;
+        StoreRing ring;
+
+        for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
+            const Unit t = decode_unit(p, u);
+            const int row = t.mt * BM + r;  // row inside this launch
+            const bool row_ok = row < p.M;
+
+            // ---- per-unit row state
+            long long yv = -1;
+            float run_m = -INFINITY, run_s = 0.f, run_t = 0.f, zyv = 0.f;
+            bool found = false;
+            float lse2 = INFINITY, K1 = 0.f, K2 = 0.f, Bc = 0.f;
+            if constexpr (kMode == kFwd) {
+                if (row_ok) yv = p.y[row];
+            } else if constexpr (kMode == kDz) {
+                if (row_ok) {
+                    const int grow = p.row0 + row;
+                    yv = p.y[grow];
+                    if (yv != p.ignore_index) {
+                        const float lse_v = p.lse[grow];
+                        const float glp = p.g_lp ? p.g_lp[grow] : 0.f;
+                        const float gent = (kEnt && p.g_ent) ? p.g_ent[grow] : 0.f;
+                        const float spz = kEnt ? (lse_v - p.ent[grow]) : 0.f;  // sum_j p_j z_j
+                        const float A = p.scale * gent;
+                        Bc = p.scale * glp;
+                        K1 = A * spz - Bc;
+                        K2 = -A * p.scale;
+                        lse2 = lse_v * LOG2E;
+                        if (yv < 0 || yv >= p.V) atomicOr(p.err, ERR_BAD_TARGET);
+                    } else {
+                        yv = -1;
+                    }
+                }
+            }
+
+            for (int nt = t.n0; nt < t.n1; ++nt) {
+                if (!mbar_wait(&tfull[acc], acc_phase, limit, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t tbase = tmem_base + static_cast<uint32_t>(acc * BN) + lane_off;
+
+                if constexpr (kMode == kFwd) {
+                    const int col0 = nt * BN;
+                    const int nvalid = min(BN, p.V - col0);
+                    const long long tcol = yv - col0;
+#pragma unroll 1
+                    for (int c = 0; c < BN / 32; ++c) {
+                        uint32_t v[32];
+                        tmem_ld_32x32b_x32(tbase + c * 32, v);
+                        tmem_wait_ld();
+                        if (c == BN / 32 - 1) {
+                            tc_fence_before();
+                            mbar_arrive(&tempty[acc]);
+                        }
+                        const long long tc = tcol - c * 32;
+                        if (tc >= 0 && tc < 32) {
+                            zyv = select32(v, static_cast<int>(tc)) * p.scale;
+                            found = true;
+                        }
+                        const int nv = nvalid - c * 32;
+                        if (nv <= 0) continue;
+                        float uu[32];
+                        float cmax = -INFINITY;
+                        if (nv >= 32) {
+#pragma unroll
+                            for (int j = 0; j < 32; ++j) {
+                                uu[j] = __uint_as_float(v[j]) * p.scale2;
+                                cmax = fmaxf(cmax, uu[j]);
+                            }
+                        } else {
+#pragma unroll
+                            for (int j = 0; j < 32; ++j) {
+                                uu[j] = (j < nv) ? __uint_as_float(v[j]) * p.scale2 : -INFINITY;
+                                cmax = fmaxf(cmax, uu[j]);
+                            }
+                        }
+                        if (cmax > run_m) {
+                            // rescale the running sums to the new maximum; a row that
+                            // has seen nothing yet (run_s == 0) has nothing to rescale
+                            const float alpha = ex2_approx(run_m - cmax);
+                            if constexpr (kEnt)
+                                run_t = (run_s > 0.f) ? alpha * (run_t + run_s * (run_m - cmax)) : 0.f;
+                            run_s *= alpha;
+                            run_m = cmax;
+                        }
+                        float s0 = 0.f, s1 = 0.f, t0 = 0.f, t1 = 0.f;
+                        if (nv >= 32) {
+#pragma unroll
+                            for (int j = 0; j < 32; j += 2) {
+                                const float d0 = uu[j] - run_m, d1 = uu[j + 1] - run_m;
+                                const float e0 = ex2_approx(d0), e1 = ex2_approx(d1);
+                                s0 += e0;
+                                s1 += e1;
+                                if constexpr (kEnt) {
+                                    t0 = fmaf(e0, d0, t0);
+                                    t1 = fmaf(e1, d1, t1);
+                                }
+                            }
+                        } else {
+#pragma unroll
+                            for (int j = 0; j < 32; ++j) {
+                                if (j < nv) {
+                                    const float d0 = uu[j] - run_m;
+                                    const float e0 = ex2_approx(d0);
+                                    s0 += e0;
+                                    if constexpr (kEnt) t0 = fmaf(e0, d0, t0);
+                                }
+                            }
+                        }
+                        run_s += s0 + s1;
+                        if constexpr (kEnt) run_t += t0 + t1;
+                    }
+                } else if constexpr (kMode == kDz) {
+                    // 4 store boxes of 64 bf16 columns each
+                    const int col0 = nt * BN;
+#pragma unroll 1
+                    for (int b = 0; b < BN / 64; ++b) {
+                        const uint32_t box = store_box_acquire(ring, smem, et);
+                        uint32_t w[32];
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            uint32_t v[32];
+                            tmem_ld_32x32b_x32(tbase + b * 64 + h * 32, v);
+                            tmem_wait_ld();
+                            if (b == BN / 64 - 1 && h == 1) {
+                                tc_fence_before();
+                                mbar_arrive(&tempty[acc]);
+                            }
+                            const int cbase = col0 + b * 64 + h * 32;
+                            float dz[32];
+#pragma unroll
+                            for (int j = 0; j < 32; ++j) {
+                                const float a = __uint_as_float(v[j]);
+                                const float pj = ex2_approx(fmaf(a, p.scale2, -lse2));
+                                dz[j] = pj * fmaf(a, K2, K1);
+                            }
+                            const long long tc = yv - cbase;
+                            if (tc >= 0 && tc < 32) {
+                                const uint32_t bit = 1u << static_cast<int>(tc);
+#pragma unroll
+                                for (int j = 0; j < 32; ++j) dz[j] += ((bit >> j) & 1u) ? Bc : 0.f;
+                            }
+                            const int nv = p.V - cbase;
+                            if (nv < 32) {
+#pragma unroll
+                                for (int j = 0; j < 32; ++j)
+                                    if (j >= nv) dz[j] = 0.f;
+                            }
+#pragma unroll
+                            for (int j = 0; j < 16; ++j) w[h * 16 + j] = pack_bf16x2(dz[2 * j], dz[2 * j + 1]);
+                        }
+                        stage_row(box, r, w);
+                        store_box_release<kMode>(ring, smem, et, &tmOut, col0 + b * 64, t.mt * BM,
+                                                 false);
+                    }
+                } else {
+                    // kDx / kDw: plain conversion of the fp32 accumulator
+                    const int col0 = nt * BN;
+                    constexpr int BOX_COLS = kOutF32 ? 32 : 64;
+#pragma unroll 1
+                    for (int b = 0; b < BN / BOX_COLS; ++b) {
+                        const uint32_t box = store_box_acquire(ring, smem, et);
+                        uint32_t w[32];
+                        if constexpr (kOutF32) {
+                            tmem_ld_32x32b_x32(tbase + b * 32, w);
+                            tmem_wait_ld();
+                            if (b == BN / BOX_COLS - 1) {
+                                tc_fence_before();
+                                mbar_arrive(&tempty[acc]);
+                            }
+                        } else {
+#pragma unroll
+                            for (int h = 0; h < 2; ++h) {
+                                uint32_t v[32];
+                                tmem_ld_32x32b_x32(tbase + b * 64 + h * 32, v);
+                                tmem_wait_ld();
+                                if (b == BN / BOX_COLS - 1 && h == 1) {
+                                    tc_fence_before();
+                                    mbar_arrive(&tempty[acc]);
+                                }
+#pragma unroll
+                                for (int j = 0; j < 16; ++j)
+                                    w[h * 16 + j] = pack_bf16x2(__uint_as_float(v[2 * j]),
+                                                                __uint_as_float(v[2 * j + 1]));
+                            }
+                        }
+                        stage_row(box, r, w);
+                        store_box_release<kMode>(ring, smem, et, &tmOut, col0 + b * BOX_COLS,
+                                                 t.mt * BM, kMode == kDw && p.dw_add);
+                    }
+                }
+                acc ^= 1;
+                if (acc == 0) acc_phase ^= 1u;
+            }
+            if (!ok) break;
+
+            if constexpr (kMode == kFwd) {
+                if (row_ok) {
+                    const size_t o = static_cast<size_t>(t.split) * p.M + row;
+                    p.part_m[o] = run_m;
+                    p.part_s[o] = run_s;
+                    if constexpr (kEnt) p.part_t[o] = run_t;
+                    if (found) p.zy[row] = zyv;
+                }
+            }
+        }
+        if (!ok) {
+            atomicOr(p.err, ERR_TIMEOUT);
+            *abort_flag = 1;
+        }
+        if constexpr (kMode != kFwd) {
+            if (et == 0) bulk_wait_group<0>();
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem_base, TMEM_COLS);
+    }
+}
+
+// ------------------------------------------------------------- split merge
+
+struct MergeParams {
+    int M, S, V;
+    long long ignore_index;
+    int compute_entropy;
+    const long long* y;
+    const float* part_m;
+    const float* part_s;
+    const float* part_t;
+    const float* zy;
+    float* logprob;
+    float* lse;
+    float* entropy;
+    int* err;
+};
+
+// Combines the per-split (max, sum-exp, entropy sum) partials of each row into
+// the final lse / logprob / entropy (the "reduced" and "result" stages kept in
+// buffers separate from the raw partials).  Base-2 units inside, natural log out.
+__global__ void __launch_bounds__(256) flp_merge_kernel(const MergeParams p) {
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= p.M) return;
+    float mx = -INFINITY;
+    for (int k = 0; k < p.S; ++k) {
+        const size_t o = static_cast<size_t>(k) * p.M + i;
+        if (p.part_s[o] > 0.f) mx = fmaxf(mx, p.part_m[o]);
+    }
+    float sig = 0.f, tau = 0.f;
+    for (int k = 0; k < p.S; ++k) {
+        const size_t o = static_cast<size_t>(k) * p.M + i;
+        const float sk = p.part_s[o];
+        if (!(sk > 0.f)) continue;  // a split that saw no column contributes nothing
+        const float d = p.part_m[o] - mx;
+        const float a = exp2f(d);
+        sig = fmaf(sk, a, sig);
+        if (p.compute_entropy) tau = fmaf(p.part_t[o] + sk * d, a, tau);
+    }
+    const float l2s = log2f(sig);
+    const float lse = (mx + l2s) * LN2;
+    p.lse[i] = lse;
+    const long long yv = p.y[i];
+    float lp, ent = p.compute_entropy ? (l2s - tau / sig) * LN2 : 0.f;
+    if (yv == p.ignore_index) {
+        lp = 0.f;
+        ent = 0.f;
+    } else if (yv < 0 || yv >= p.V) {
+        lp = __int_as_float(0x7fc00000);
+        atomicOr(p.err, ERR_BAD_TARGET);
+    } else {
+        lp = p.zy[i] - lse;
+    }
+    p.logprob[i] = lp;
+    if (p.compute_entropy) p.entropy[i] = ent;
+}
+
+}  // namespace flp

@@ -1,0 +1,187 @@
+"""ctypes binding of ``libflp.so`` (the C ABI in ``include/flp.h``).
+
+Argument marshalling only: every step of the path runs in the library's CUDA
+kernels.  torch is used for device memory, streams and dtype bookkeeping.
+Loading fails loudly (``FlpError``) when the library is missing; there is no
+fallback implementation.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libflp.so")
+
+FLP_OK = 0
+FLP_ERR_INVALID_ARG = 1
+FLP_ERR_UNSUPPORTED = 2
+FLP_ERR_WORKSPACE = 3
+FLP_ERR_CUDA = 4
+FLP_ERR_BAD_TARGET = 5
+FLP_ERR_TIMEOUT = 6
+FLP_F32 = 0
+FLP_BF16 = 1
+
+EXPORTS = ("flp_workspace_query", "flp_forward", "flp_backward", "flp_get_error",
+           "flp_status_string", "flp_last_error_message")
+
+
+class FlpError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(msg)
+        self.status = status
+
+
+_lib = None
+
+
+def load(path: str = LIB_PATH):
+    """Load the CUDA library (built by ``entropy_loss_gb300.build``)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise FlpError(FLP_ERR_CUDA, f"{path} is missing: build it with entropy_loss_gb300.build.build()")
+    lib = ctypes.CDLL(path)
+    p, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+    lib.flp_workspace_query.argtypes = [i64, i64, i64, i32, i64, ctypes.POINTER(ctypes.c_size_t),
+                                        ctypes.POINTER(ctypes.c_size_t)]
+    lib.flp_forward.argtypes = [p, p, p, i64, i64, i64, i64, ctypes.c_float, i32, p, p, p, p,
+                                ctypes.c_size_t, p]
+    lib.flp_backward.argtypes = [p, p, p, i64, i64, i64, i64, ctypes.c_float, i32, p, p, p, p, p,
+                                 i32, p, i32, i32, p, ctypes.c_size_t, p]
+    lib.flp_get_error.argtypes = [p, p]
+    lib.flp_status_string.argtypes = [i32]
+    lib.flp_status_string.restype = ctypes.c_char_p
+    lib.flp_last_error_message.argtypes = []
+    lib.flp_last_error_message.restype = ctypes.c_char_p
+    for name in ("flp_workspace_query", "flp_forward", "flp_backward", "flp_get_error"):
+        getattr(lib, name).restype = i32
+    _lib = lib
+    return lib
+
+
+def _check(status: int, what: str) -> None:
+    if status != FLP_OK:
+        lib = load()
+        msg = lib.flp_status_string(status).decode()
+        detail = lib.flp_last_error_message().decode()
+        raise FlpError(status, f"{what}: {msg}" + (f" ({detail})" if detail else ""))
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def workspace_query(M: int, H: int, V: int, compute_entropy: bool = True, chunk_rows: int = 0):
+    """(forward bytes, backward bytes) on the current device."""
+    f = ctypes.c_size_t(0)
+    b = ctypes.c_size_t(0)
+    _check(load().flp_workspace_query(M, H, V, int(compute_entropy), chunk_rows, ctypes.byref(f),
+                                      ctypes.byref(b)), "flp_workspace_query")
+    return f.value, b.value
+
+
+def alloc_workspace(M: int, H: int, V: int, compute_entropy: bool = True, chunk_rows: int = 0,
+                    device=None) -> torch.Tensor:
+    """One uint8 device buffer large enough for both forward and backward."""
+    f, b = workspace_query(M, H, V, compute_entropy, chunk_rows)
+    return torch.empty(max(f, b), dtype=torch.uint8, device=device or "cuda")
+
+
+def _need(t, dtype, shape, name):
+    if t.dtype != dtype or tuple(t.shape) != tuple(shape) or not t.is_contiguous() or not t.is_cuda:
+        raise ValueError(f"{name}: expected contiguous CUDA {dtype} of shape {tuple(shape)}, "
+                         f"got {t.dtype} {tuple(t.shape)} on {t.device}")
+
+
+def forward(X, W, y, *, ignore_index: int = -100, scale: float = 1.0, compute_entropy: bool = True,
+            workspace=None, logprob=None, lse=None, entropy=None, stream=None):
+    """Per-row (logprob, lse, entropy-or-None) of softmax(scale * X W^T)."""
+    M, H = X.shape
+    V = W.shape[0]
+    _need(X, torch.bfloat16, (M, H), "X")
+    _need(W, torch.bfloat16, (V, H), "W")
+    _need(y, torch.int64, (M,), "targets")
+    dev = X.device
+    logprob = torch.empty(M, dtype=torch.float32, device=dev) if logprob is None else logprob
+    lse = torch.empty(M, dtype=torch.float32, device=dev) if lse is None else lse
+    if compute_entropy and entropy is None:
+        entropy = torch.empty(M, dtype=torch.float32, device=dev)
+    if not compute_entropy:
+        entropy = None
+    if workspace is None:
+        workspace = alloc_workspace(M, H, V, compute_entropy, device=dev)
+    _check(load().flp_forward(_ptr(X), _ptr(W), _ptr(y), M, H, V, ignore_index, float(scale),
+                              int(compute_entropy), _ptr(logprob), _ptr(lse), _ptr(entropy),
+                              _ptr(workspace), workspace.numel(), _stream(stream)), "flp_forward")
+    return logprob, lse, entropy
+
+
+def backward(X, W, y, lse, entropy, grad_logprob, grad_entropy, *, ignore_index: int = -100,
+             scale: float = 1.0, compute_entropy: bool = True, dX=None, dW=None,
+             dx_dtype=torch.bfloat16, accumulate_dW: bool = False, workspace=None, stream=None):
+    """(dX, dW) for upstream gradients of logprob and entropy (None = zero)."""
+    M, H = X.shape
+    V = W.shape[0]
+    dev = X.device
+    if dX is None:
+        dX = torch.empty(M, H, dtype=dx_dtype, device=dev)
+    if dW is None:
+        dW = torch.empty(V, H, dtype=torch.float32, device=dev)
+    dxt = FLP_F32 if dX.dtype == torch.float32 else FLP_BF16
+    if workspace is None:
+        workspace = alloc_workspace(M, H, V, compute_entropy, device=dev)
+    _check(load().flp_backward(_ptr(X), _ptr(W), _ptr(y), M, H, V, ignore_index, float(scale),
+                               int(compute_entropy), _ptr(lse),
+                               _ptr(entropy if compute_entropy else None), _ptr(grad_logprob),
+                               _ptr(grad_entropy if compute_entropy else None), _ptr(dX), dxt,
+                               _ptr(dW), FLP_F32, int(accumulate_dW), _ptr(workspace),
+                               workspace.numel(), _stream(stream)), "flp_backward")
+    return dX, dW
+
+
+def get_error(workspace, stream=None) -> int:
+    """Synchronise the stream and return the workspace's error status code."""
+    return int(load().flp_get_error(_ptr(workspace), _stream(stream)))
+
+
+class FusedLinearLogprob(torch.autograd.Function):
+    """autograd wrapper: returns (logprob, entropy-or-empty) of softmax(scale X W^T)."""
+
+    @staticmethod
+    def forward(ctx, X, W, y, ignore_index, scale, compute_entropy, workspace):
+        lp, lse, ent = forward(X, W, y, ignore_index=ignore_index, scale=scale,
+                               compute_entropy=compute_entropy, workspace=workspace)
+        ctx.save_for_backward(X, W, y, lse, ent if ent is not None else lse.new_empty(0))
+        ctx.cfg = (ignore_index, scale, compute_entropy, workspace)
+        return lp, (ent if ent is not None else lse.new_empty(0))
+
+    @staticmethod
+    def backward(ctx, g_lp, g_ent):
+        X, W, y, lse, ent = ctx.saved_tensors
+        ignore_index, scale, compute_entropy, workspace = ctx.cfg
+        g_lp = None if g_lp is None else g_lp.contiguous().float()
+        g_ent = None if (g_ent is None or not compute_entropy) else g_ent.contiguous().float()
+        dX, dW = backward(X, W, y, lse, ent if compute_entropy else None, g_lp, g_ent,
+                          ignore_index=ignore_index, scale=scale, compute_entropy=compute_entropy,
+                          dx_dtype=X.dtype, workspace=workspace)
+        return dX, dW.to(W.dtype), None, None, None, None, None
+
+
+def fused_linear_logprob(X, W, y, ignore_index: int = -100, scale: float = 1.0,
+                         compute_entropy: bool = True, workspace=None):
+    """Differentiable per-row log-prob (and entropy) of the LM head."""
+    if workspace is None:
+        workspace = alloc_workspace(X.shape[0], X.shape[1], W.shape[0], compute_entropy,
+                                    device=X.device)
+    return FusedLinearLogprob.apply(X, W, y, ignore_index, scale, compute_entropy, workspace)

@@ -1,0 +1,148 @@
+/*
+ * flp.h - C ABI of the fused linear log-prob / cross-entropy LM head for
+ * GB300 (sm_103a).
+ *
+ * Problem (Liger-Kernel v0.8.3 test/transformers page, the native SM100 fused
+ * scaled linear cross-entropy commit, section "Summary": the classifier GEMM
+ * fused with NLL/LSE and optional entropy; "Chunked Triton GRPO loss" of the
+ * Liger-Kernel pull request 1294 page: the lm_head fused into the loss with an
+ * online logsumexp so that the (N, V) logits are never materialised):
+ *
+ *   X  : bf16 [M, H], row-major, contiguous   (hidden states)
+ *   W  : bf16 [V, H], row-major, contiguous   (classifier / lm_head weight,
+ *                                              the nn.Linear layout)
+ *   y  : int64 [M]                            (targets, ignore_index allowed)
+ *   s  : fp32                                 (logit scale, 1/temperature)
+ *
+ *   z_ij      = s * sum_k X_ik W_jk   (fp32 accumulation; never stored in HBM)
+ *   lse_i     = log sum_j exp(z_ij)
+ *   logprob_i = z_{i,y_i} - lse_i
+ *   entropy_i = lse_i - sum_j p_ij z_ij,   p_ij = exp(z_ij - lse_i)
+ *
+ * Backward (same Liger-Kernel pages: "Implementation > Backward" of the native
+ * commit, "Kernel design notes" of pull request 1294): the logits are
+ * recomputed tile by tile,
+ *
+ *   dZ_ij = s * [ g_lp_i (1[j = y_i] - p_ij) + g_ent_i p_ij (sum_k p_ik z_ik - z_ij) ]
+ *
+ * is rounded to bf16, and contracted into dX = dZ W and dW = dZ^T X with fp32
+ * accumulation.
+ *
+ * Conventions shared by every entry point
+ *  - Device pointers are CUDA device addresses owned by the caller; the library
+ *    allocates no device memory and keeps no state between calls beyond cached
+ *    device attributes.  Every call is asynchronous on `stream` (a
+ *    cudaStream_t passed as void*, NULL for the legacy default stream) and
+ *    launches only on the device that is current on the calling thread.
+ *  - Argument errors are returned synchronously before anything is launched.
+ *    Required: every pointer 16-byte aligned; H % 8 == 0 (row pitch of a TMA
+ *    tensor, else FLP_ERR_UNSUPPORTED); M >= 0 (M == 0 is a no-op); V >= 1;
+ *    workspace large enough (else FLP_ERR_WORKSPACE).
+ *  - A row whose target equals ignore_index has logprob = 0, entropy = 0 and a
+ *    zero gradient row; its lse is still written.  A target outside [0, V)
+ *    that is not ignore_index yields logprob = NaN for that row and sets
+ *    FLP_ERR_BAD_TARGET in the workspace's error word (read it with
+ *    flp_get_error); the call itself still returns FLP_OK because the hot path
+ *    never synchronises.
+ *  - The workspace is caller-owned device memory of at least the queried size.
+ *    Its contents need no initialisation; a call owns it until the work it
+ *    queued on `stream` has finished.  Calls that run concurrently must use
+ *    distinct workspaces.
+ *  - Results are deterministic: no floating-point atomics are used, so two
+ *    identical calls produce bit-identical outputs.
+ */
+#ifndef FLP_H
+#define FLP_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    FLP_OK = 0,
+    FLP_ERR_INVALID_ARG = 1, /* null/misaligned pointer, negative size, bad flag */
+    FLP_ERR_UNSUPPORTED = 2, /* shape or device the kernels do not handle (H % 8 != 0,
+                                not an sm_103 device, size beyond int32 tiling) */
+    FLP_ERR_WORKSPACE = 3,   /* workspace pointer null or smaller than required */
+    FLP_ERR_CUDA = 4,        /* a CUDA runtime/driver call failed; see flp_last_error_message */
+    FLP_ERR_BAD_TARGET = 5,  /* (error word) a target outside [0, V) that is not ignore_index */
+    FLP_ERR_TIMEOUT = 6      /* (error word) a kernel's bounded wait expired; its outputs are invalid */
+} flp_status;
+
+typedef enum { FLP_F32 = 0, FLP_BF16 = 1 } flp_dtype;
+
+/*
+ * Workspace sizes, in bytes, for the given problem on the current device.
+ *   fwd_bytes : needed by flp_forward (per-split raw partials and the target
+ *               logits; the SkyRL page "perf(megatron): autotune fused LM-head
+ *               Triton kernels", section "Correctness", keeps raw and final
+ *               results in separate buffers, and so does this library).
+ *   bwd_bytes : needed by flp_backward when it processes the rows in waves of
+ *               `chunk_rows` rows (chunk_rows <= 0 selects 4096); one wave's
+ *               bf16 dZ, [chunk, ceil(V/256)*256], dominates.  The Liger-Kernel
+ *               native commit's "Memory" section reports the same kind of
+ *               reusable workspace, and pull request 1294's "Kernel design
+ *               notes" a reusable per-chunk grad_logits buffer.
+ * Either output pointer may be NULL.  The same buffer may serve both calls.
+ * Returns FLP_ERR_INVALID_ARG for negative sizes, FLP_ERR_CUDA if the device
+ * cannot be queried.
+ */
+flp_status flp_workspace_query(int64_t M, int64_t H, int64_t V, int compute_entropy,
+                               int64_t chunk_rows, size_t* fwd_bytes, size_t* bwd_bytes);
+
+/*
+ * Forward: writes logprob[M], lse[M] and (when compute_entropy != 0)
+ * entropy[M], all fp32 device arrays.  entropy must be NULL when
+ * compute_entropy == 0 and non-NULL otherwise (the SkyRL page's "Overview":
+ * compute_entropy gates the entropy buffers and kernel work).
+ * Two kernels run on `stream`: the fused tcgen05 GEMM + online
+ * max / sum-exp / target / entropy epilogue writing raw per-split partials to
+ * the workspace, then the merge of those partials into the outputs.
+ */
+flp_status flp_forward(const void* X, const void* W, const int64_t* targets, int64_t M,
+                       int64_t H, int64_t V, int64_t ignore_index, float scale,
+                       int compute_entropy, float* logprob, float* lse, float* entropy,
+                       void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Backward: given the forward's lse (and entropy when compute_entropy != 0),
+ * writes dX [M, H] (dtype dX_dtype, overwritten) and dW [V, H] (dtype must be
+ * FLP_F32; overwritten, or added to when accumulate_dW != 0).
+ *   grad_logprob, grad_entropy : fp32 [M] upstream gradients of logprob and
+ *       entropy; NULL means zero.  grad_entropy is ignored when
+ *       compute_entropy == 0.  For a mean NLL loss over N valid rows pass
+ *       grad_logprob = -1/N on every row.
+ * Rows are processed in waves of as many rows as the workspace holds (at most
+ * M, at least 128): each wave recomputes its logits tiles, writes bf16 dZ to
+ * the workspace, and runs the dX and dW contractions; dW accumulates in fp32
+ * across waves in stream order.
+ */
+flp_status flp_backward(const void* X, const void* W, const int64_t* targets, int64_t M,
+                        int64_t H, int64_t V, int64_t ignore_index, float scale,
+                        int compute_entropy, const float* lse, const float* entropy,
+                        const float* grad_logprob, const float* grad_entropy, void* dX,
+                        flp_dtype dX_dtype, void* dW, flp_dtype dW_dtype, int accumulate_dW,
+                        void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Synchronises `stream`, then reads and returns the workspace's error word
+ * (FLP_OK, FLP_ERR_BAD_TARGET or FLP_ERR_TIMEOUT) written by the most recent
+ * flp_forward / flp_backward that used this workspace.  Each of those calls
+ * clears the word when it starts.  Returns FLP_ERR_CUDA if the copy fails.
+ */
+flp_status flp_get_error(const void* workspace, void* stream);
+
+/* Static description of a status code. */
+const char* flp_status_string(flp_status status);
+
+/* Text of the last FLP_ERR_CUDA / FLP_ERR_UNSUPPORTED on the calling thread. */
+const char* flp_last_error_message(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FLP_H */
