@@ -1,0 +1,397 @@
+#!/usr/bin/env python
+"""Benchmark of the fused linear log-prob / cross-entropy LM head on GB300.
+
+One step = one forward (fused GEMM + online LSE / target / entropy epilogue,
+split merge) and one backward (dZ recompute, dX and dW contractions) over the
+headline workload M=4096, H=4096, V=131072 (bf16 inputs, fp32 accumulation),
+inputs resident in HBM.  Throughput counts four classifier GEMMs per step,
+8*M*H*V FLOP (the Liger-Kernel native commit's "Performance methodology").
+
+  python bench.py [--gpus N --steps K --warmup W] [--impl reference]
+
+--impl reference times the fp64 CPU oracle on the machine's host cores on a
+bounded row sample of the same workload (there is no other implementation to
+run: the pages ship no code).  Under torchrun every rank runs its own replica
+(the path is not sharded across GPUs); rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import shutil
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from entropy_loss_gb300 import inputs  # noqa: E402
+
+METRIC = "fwd+bwd TFLOPS & % bf16 tensor peak, fused linear logprob M4096 H4096 V128K"
+UNIT = "TFLOP/s"
+PAGES_B300_TP1_FWD_BWD_TFLOPS = 1606.5  # Liger-Kernel native commit, "M=4096 forward + backward", TP1, B300
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=inputs.HEADLINE, choices=sorted(inputs.WORKLOADS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0,
+                    help="target CPU time of the oracle baseline sample")
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------------ helpers
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if (args.impl == "ours" and torch.cuda.is_available()) else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64,
+                     device="cuda" if dist.get_backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms in a thread."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.lines: list[str] = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        exe = shutil.which("nvidia-smi")
+        if not exe:
+            return
+        self.proc = subprocess.Popen([exe, f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                      "-i", str(self.gpu), "-lms", "200"],
+                                     stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=5)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        load = [s for s in sm if s > 0.5 * max(sm)] or sm
+        return {"sm_mhz": statistics.median(load), "sm_max_mhz": max(smax), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------- our path
+
+def run_ours(args, world, rank, local):
+    from entropy_loss_gb300 import build as libbuild
+    from entropy_loss_gb300 import flp
+
+    libbuild.build()
+    flp.load()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    w = inputs.WORKLOADS[args.workload]
+    d = inputs.make_inputs(w)
+    M, H, V = w.M, w.H, w.V
+    ent = d["compute_entropy"]
+    X, W, y = d["X"].to(dev), d["W"].to(dev), d["y"].to(dev)
+    g_lp = d["g_lp"].to(dev)
+    g_ent = d["g_ent"].to(dev) if d["g_ent"] is not None else None
+    ws = flp.alloc_workspace(M, H, V, ent, device=dev)
+    lp = torch.empty(M, dtype=torch.float32, device=dev)
+    lse = torch.empty(M, dtype=torch.float32, device=dev)
+    en = torch.empty(M, dtype=torch.float32, device=dev) if ent else None
+    dX = torch.empty(M, H, dtype=torch.bfloat16, device=dev)
+    dW = torch.empty(V, H, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    kw = dict(ignore_index=d["ignore_index"], scale=d["scale"], compute_entropy=ent, workspace=ws)
+
+    def step():
+        flp.forward(X, W, y, logprob=lp, lse=lse, entropy=en, **kw)
+        flp.backward(X, W, y, lse, en, g_lp, g_ent, dX=dX, dW=dW, **kw)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    if flp.get_error(ws) != flp.FLP_OK:
+        raise RuntimeError("error word set after warm-up")
+
+    K = args.steps
+    nph = len(flp.PHASES)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2 * nph)] for _ in range(K)]
+    for row in evs:
+        for e in row:
+            e.record(stream)  # materialise the handles
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(dev.index if dev.index is not None else 0)
+    sampler.start()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_stop = torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    t_start.record(stream)
+    for k in range(K):
+        flp.set_phase_events(evs[k])
+        step()
+    t_stop.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    flp.set_phase_events(None)
+    clocks = sampler.stop()
+    ms_total = t_start.elapsed_time(t_stop)
+    ms_total = max_over_ranks(ms_total, world)
+    ms_step = ms_total / K
+    phase_ms = {}
+    for i, name in enumerate(flp.PHASES):
+        vals = [evs[k][2 * i].elapsed_time(evs[k][2 * i + 1]) for k in range(K)]
+        phase_ms[name] = statistics.mean(vals)
+    if flp.get_error(ws) != flp.FLP_OK:
+        raise RuntimeError("error word set after the timed steps")
+
+    flops_step = 8.0 * M * H * V
+    value = world * flops_step / (ms_step * 1e-3) / 1e12
+
+    # roofline of the dominant kernel (largest mean duration among the phases)
+    peaks, peak_src = load_peaks()
+    _, bwd_bytes = flp.workspace_query(M, H, V, ent)
+    wave_rows = min(M, ((ws.numel() - 1024) // (((V + 255) // 256) * 256 * 2)) // 128 * 128)
+    phase_flops = {"fwd": 2.0 * M * H * V, "dz": 2.0 * wave_rows * H * V,
+                   "dx": 2.0 * wave_rows * H * V, "dw": 2.0 * wave_rows * H * V}
+    dom = max(phase_flops, key=lambda n: phase_ms[n])
+    achieved = phase_flops[dom] / (phase_ms[dom] * 1e-3) / 1e12
+    peak = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+    roofline = {"bound": "tensor", "kernel": f"flp_tile_kernel<{dom}>", "achieved": round(achieved, 1),
+                "peak": peak, "unit": UNIT, "frac": round(achieved / peak, 4),
+                "traffic": None, "peak_source": f"bf16_tflops_sustained of {peak_src}"}
+
+    waves = -(-M // wave_rows)
+    launches = K * (2 + 3 * waves)
+
+    result = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": max(args.warmup, 3), "ms_per_step": round(ms_step, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": round(value / world / PAGES_B300_TP1_FWD_BWD_TFLOPS, 4),
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "M": M, "H": H, "V": V, "compute_entropy": ent,
+                   "scale": d["scale"], "ignore_frac": w.ignore_frac,
+                   "parallelism": "replicas" if world > 1 else "single",
+                   "l2": "inputs larger than L2 (W is %.2f GiB), no flush" % (V * H * 2 / 2**30),
+                   "wave_rows": wave_rows, "fwd_bwd_flop_per_step": flops_step},
+        "pct_of_bf16_peak": {"measured_burst": round(value / world / float(peaks.get("bf16_tflops", 1900.0)), 4),
+                             "measured_sustained": round(value / world / peak, 4),
+                             "nominal_2250": round(value / world / 2250.0, 4)},
+        "phase_ms": {k: round(v, 4) for k, v in phase_ms.items()},
+        "fwd_tflops": round(2.0 * M * H * V / ((phase_ms["fwd"] + phase_ms["merge"]) * 1e-3) / 1e12, 1),
+        "roofline": roofline,
+        "gpu_launches": launches,
+        "clocks": clocks,
+    }
+
+    if not args.no_e2e:
+        result["e2e"] = run_e2e(args, d, X.device, W, ws, world, M, H, V, ent, stream, flp)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(d, w, args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+
+
+def run_e2e(args, d, dev, W, ws, world, M, H, V, ent, stream, flp):
+    """Same step through the public API, with the step's inputs (hidden states,
+    targets, upstream grads) copied from pinned host memory each step and the
+    per-row log-probs read back.  W is the layer's resident parameter."""
+    Xh = d["X"].pin_memory()
+    yh = d["y"].pin_memory()
+    glh = d["g_lp"].pin_memory()
+    geh = d["g_ent"].pin_memory() if d["g_ent"] is not None else None
+    out_h = torch.empty(M, dtype=torch.float32).pin_memory()
+    kw = dict(ignore_index=d["ignore_index"], scale=d["scale"], compute_entropy=ent, workspace=ws)
+
+    def step():
+        X = Xh.to(dev, non_blocking=True)
+        y = yh.to(dev, non_blocking=True)
+        g1 = glh.to(dev, non_blocking=True)
+        g2 = geh.to(dev, non_blocking=True) if geh is not None else None
+        lp, lse, en = flp.forward(X, W, y, **kw)
+        flp.backward(X, W, y, lse, en, g1, g2, **kw)
+        out_h.copy_(lp, non_blocking=True)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    K = args.steps
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    a.record(stream)
+    for _ in range(K):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    ms = max_over_ranks(a.elapsed_time(b), world) / K
+    h2d = Xh.numel() * 2 + yh.numel() * 8 + glh.numel() * 4 + (geh.numel() * 4 if geh is not None else 0)
+    return {"value": round(world * 8.0 * M * H * V / (ms * 1e-3) / 1e12, 1), "unit": UNIT,
+            "ms_per_step": round(ms, 4), "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": M * 4,
+            "note": "X, targets and upstream grads copied from pinned host memory every step; "
+                    "per-row log-probs read back; W resident (the layer's parameter)"}
+
+
+# --------------------------------------------------- oracle (CPU baseline)
+
+def _oracle_sample_time(d, rows, oracle):
+    Xb, Wb = inputs.bf16_bits(d["X"]), inputs.bf16_bits(d["W"])
+    y = d["y"].numpy()
+    g1 = d["g_lp"].double().numpy()
+    g2 = d["g_ent"].double().numpy() if d["g_ent"] is not None else None
+    t0 = time.perf_counter()
+    oracle.forward(Xb, Wb, y, ignore_index=d["ignore_index"], scale=d["scale"],
+                   compute_entropy=d["compute_entropy"], rows=rows)
+    oracle.backward(Xb, Wb, y, g1, g2, ignore_index=d["ignore_index"], scale=d["scale"],
+                    compute_entropy=d["compute_entropy"], rows=rows, round_dz_bf16=False)
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(d, w, seconds):
+    """The oracle as it stands, on a seeded row sample: forward of the rows, then
+    their backward (logit recompute, dX rows, and their dW contribution over the
+    full vocabulary).  Scaled to the metric: 8*H*V FLOP per row."""
+    import numpy as np
+
+    import oracle
+    oracle.build()
+    g = np.random.default_rng(0)
+    one = g.choice(w.M, 1, replace=False)
+    t1 = _oracle_sample_time(d, one, oracle)
+    n = int(max(1, min(w.M, seconds / max(t1, 1e-6))))
+    rows = g.choice(w.M, n, replace=False)
+    t = _oracle_sample_time(d, rows, oracle)
+    value = 8.0 * w.H * w.V * n / t / 1e12
+    return {"value": value, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+            "seconds": round(t, 2),
+            "sample": f"{n} seeded rows of {w.name}: fp64 forward + backward (dX rows, their dW "
+                      f"contribution over all {w.V} vocabulary rows); 8*H*V FLOP per row"}
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    import numpy as np
+
+    import oracle
+    oracle.build()
+    w = inputs.WORKLOADS[args.workload]
+    d = inputs.make_inputs(w)
+    g = np.random.default_rng(1)
+    steps, warm = args.steps, max(args.warmup, 3)
+    t1 = _oracle_sample_time(d, g.choice(w.M, 1, replace=False), oracle)
+    budget = 150.0  # seconds for the whole run
+    n = int(max(1, min(w.M, budget / ((steps + warm) * max(t1, 1e-6)))))
+    for _ in range(warm):
+        _oracle_sample_time(d, g.choice(w.M, n, replace=False), oracle)
+    times = [_oracle_sample_time(d, g.choice(w.M, n, replace=False), oracle) for _ in range(steps)]
+    t = sum(times)
+    value = 8.0 * w.H * w.V * n * steps / t / 1e12
+    sample = (f"{n} seeded rows of {w.name} per step: fp64 forward + backward (dX rows, their dW "
+              f"contribution over all {w.V} vocabulary rows); 8*H*V FLOP per row")
+    out = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+           "steps": steps, "warmup": warm, "ms_per_step": round(1e3 * t / steps, 3),
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+           "data": "synthetic",
+           "config": {"workload": w.name, "M": w.M, "H": w.H, "V": w.V,
+                      "compute_entropy": w.compute_entropy, "scale": w.scale},
+           "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.num_threads(),
+                            "kind": "oracle", "sample": sample},
+           "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        world = int(os.environ.get("WORLD_SIZE", "1"))
+        rank = int(os.environ.get("RANK", "0"))
+        run_reference(args, world, rank)
+        return
+    world, rank, local = dist_setup(args)
+    run_ours(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -21,6 +21,16 @@ namespace {
 
 thread_local std::string g_msg;
 
+constexpr int kMaxPhaseEvents = 10;
+thread_local void* g_events[kMaxPhaseEvents] = {};
+thread_local int g_num_events = 0;
+
+// Records the caller's instrumentation event `idx` (if any) on stream s.
+void mark(int idx, cudaStream_t s) {
+    if (idx < g_num_events && g_events[idx])
+        cudaEventRecord(static_cast<cudaEvent_t>(g_events[idx]), s);
+}
+
 flp_status fail(flp_status st, const char* what) {
     g_msg = what;
     return st;
@@ -257,6 +267,14 @@ const char* flp_status_string(flp_status s) {
 
 const char* flp_last_error_message(void) { return g_msg.c_str(); }
 
+flp_status flp_set_phase_events(void* const* events, int count) {
+    if (count < 0 || count > kMaxPhaseEvents)
+        return fail(FLP_ERR_INVALID_ARG, "count must be in [0, 10]");
+    g_num_events = events ? count : 0;
+    for (int i = 0; i < kMaxPhaseEvents; ++i) g_events[i] = (events && i < count) ? events[i] : nullptr;
+    return FLP_OK;
+}
+
 flp_status flp_workspace_query(int64_t M, int64_t H, int64_t V, int compute_entropy,
                                int64_t chunk_rows, size_t* fwd_bytes, size_t* bwd_bytes) {
     if (M < 0 || H < 1 || V < 1) return fail(FLP_ERR_INVALID_ARG, "M >= 0, H >= 1 and V >= 1 required");
@@ -321,9 +339,11 @@ flp_status flp_forward(const void* X, const void* W, const int64_t* targets, int
     p.err = err;
     p.wait_limit_ns = kWaitLimitNs;
     p.debug_stall_after = -1;
+    mark(0, s);
     st = ent ? launch_tile<kFwd, true, false>(f.grid, tmX, tmW, tmX, p, s)
              : launch_tile<kFwd, false, false>(f.grid, tmX, tmW, tmX, p, s);
     if (st != FLP_OK) return st;
+    mark(1, s);
 
     MergeParams mp{};
     mp.M = static_cast<int>(M);
@@ -340,9 +360,11 @@ flp_status flp_forward(const void* X, const void* W, const int64_t* targets, int
     mp.lse = lse;
     mp.entropy = entropy;
     mp.err = err;
+    mark(2, s);
     flp_merge_kernel<<<static_cast<unsigned>(cdiv(M, 256)), 256, 0, s>>>(mp);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "flp_merge_kernel launch");
+    mark(3, s);
     return FLP_OK;
 }
 
@@ -445,9 +467,12 @@ flp_status flp_backward(const void* X, const void* W, const int64_t* targets, in
         p.wait_limit_ns = kWaitLimitNs;
         p.debug_stall_after = -1;
         const int grid_dz = std::min(p.units, sms);
+        const bool first = (r0 == 0);
+        if (first) mark(4, s);
         st = ent ? launch_tile<kDz, true, false>(grid_dz, tmXk, tmW_k, tmDZst, p, s)
                  : launch_tile<kDz, false, false>(grid_dz, tmXk, tmW_k, tmDZst, p, s);
         if (st != FLP_OK) return st;
+        if (first) mark(5, s);
 
         // (2) dX[wave] = dZ W   (K = Vp)
         TileParams q{};
@@ -464,9 +489,11 @@ flp_status flp_backward(const void* X, const void* W, const int64_t* targets, in
         q.wait_limit_ns = kWaitLimitNs;
         q.debug_stall_after = -1;
         const int grid_dx = std::min(q.units, sms);
+        if (first) mark(6, s);
         st = (dX_dtype == FLP_F32) ? launch_tile<kDx, false, true>(grid_dx, tmDZk, tmW_mn, tmDX, q, s)
                                    : launch_tile<kDx, false, false>(grid_dx, tmDZk, tmW_mn, tmDX, q, s);
         if (st != FLP_OK) return st;
+        if (first) mark(7, s);
 
         // (3) dW (+)= dZ^T X[wave]   (K = rows of the wave)
         TileParams w{};
@@ -484,8 +511,10 @@ flp_status flp_backward(const void* X, const void* W, const int64_t* targets, in
         w.wait_limit_ns = kWaitLimitNs;
         w.debug_stall_after = -1;
         const int grid_dw = std::min(w.units, sms);
+        if (first) mark(8, s);
         st = launch_tile<kDw, false, true>(grid_dw, tmDZmn, tmXmn, tmDW, w, s);
         if (st != FLP_OK) return st;
+        if (first) mark(9, s);
     }
     return FLP_OK;
 }

@@ -26,7 +26,8 @@ FLP_F32 = 0
 FLP_BF16 = 1
 
 EXPORTS = ("flp_workspace_query", "flp_forward", "flp_backward", "flp_get_error",
-           "flp_status_string", "flp_last_error_message")
+           "flp_set_phase_events", "flp_status_string", "flp_last_error_message")
+PHASES = ("fwd", "merge", "dz", "dx", "dw")
 
 
 class FlpError(RuntimeError):
@@ -54,6 +55,8 @@ def load(path: str = LIB_PATH):
     lib.flp_backward.argtypes = [p, p, p, i64, i64, i64, i64, ctypes.c_float, i32, p, p, p, p, p,
                                  i32, p, i32, i32, p, ctypes.c_size_t, p]
     lib.flp_get_error.argtypes = [p, p]
+    lib.flp_set_phase_events.argtypes = [ctypes.POINTER(ctypes.c_void_p), i32]
+    lib.flp_set_phase_events.restype = i32
     lib.flp_status_string.argtypes = [i32]
     lib.flp_status_string.restype = ctypes.c_char_p
     lib.flp_last_error_message.argtypes = []
@@ -148,6 +151,18 @@ def backward(X, W, y, lse, entropy, grad_logprob, grad_entropy, *, ignore_index:
                                _ptr(dW), FLP_F32, int(accumulate_dW), _ptr(workspace),
                                workspace.numel(), _stream(stream)), "flp_backward")
     return dX, dW
+
+
+def set_phase_events(events) -> None:
+    """Instrument the next calls on this thread: `events` is a list of up to 10
+    torch.cuda.Event (or None) recorded around the kernel phases (start, stop)
+    of PHASES in order; None turns the instrumentation off."""
+    if not events:
+        _check(load().flp_set_phase_events(None, 0), "flp_set_phase_events")
+        return
+    arr = (ctypes.c_void_p * len(events))(*[(e.cuda_event if e is not None else None)
+                                            for e in events])
+    _check(load().flp_set_phase_events(arr, len(events)), "flp_set_phase_events")
 
 
 def get_error(workspace, stream=None) -> int:

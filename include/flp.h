@@ -135,6 +135,21 @@ flp_status flp_backward(const void* X, const void* W, const int64_t* targets, in
  */
 flp_status flp_get_error(const void* workspace, void* stream);
 
+/*
+ * Optional instrumentation for benchmarks and profiling.  After this call the
+ * calling thread's flp_forward / flp_backward record events[2k] immediately
+ * before and events[2k+1] immediately after kernel phase k, on the call's
+ * stream:
+ *   k = 0  forward tile kernel          k = 1  split merge
+ *   k = 2  dZ recompute (first wave)    k = 3  dX contraction (first wave)
+ *   k = 4  dW contraction (first wave)
+ * `events` holds `count` (<= 10) caller-created cudaEvent_t handles passed as
+ * void*; NULL entries are skipped.  events == NULL or count == 0 turns the
+ * instrumentation off.  The array is copied; the events stay caller-owned.
+ * Returns FLP_ERR_INVALID_ARG when count is outside [0, 10].
+ */
+flp_status flp_set_phase_events(void* const* events, int count);
+
 /* Static description of a status code. */
 const char* flp_status_string(flp_status status);
 

@@ -1,0 +1,300 @@
+"""GPU path vs the fp64 oracle, through the C ABI (ctypes binding).
+
+Tolerances (stated by the task's target for bf16 inputs with fp32
+accumulation): logprob, lse and entropy within 2e-3 absolute; dX and dW within
+1e-2 relative L2, plus gradient cosine > 0.999 and norm ratio within 2% (the
+chunked GRPO page's gradient contract).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from entropy_loss_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+ATOL_FWD = 2e-3
+RTOL_GRAD = 1e-2
+
+
+@pytest.fixture(scope="module")
+def flp():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    from entropy_loss_gb300 import build, flp as _flp
+    build.build()
+    _flp.load()
+    return _flp
+
+
+def _np(t):
+    return t.detach().float().cpu().double().numpy()
+
+
+def check_fwd(got, want, name, atol=ATOL_FWD):
+    g = _np(got)
+    assert g.shape == want.shape
+    err = np.abs(g - want)
+    assert np.all(np.isfinite(g)), f"{name}: non-finite values"
+    assert err.max() <= atol, f"{name}: max abs err {err.max():.3e} at {int(err.argmax())}"
+
+
+def check_grad(got, want, name, rtol=RTOL_GRAD):
+    g = _np(got)
+    assert np.all(np.isfinite(g)), f"{name}: non-finite values"
+    nw = np.linalg.norm(want)
+    if nw == 0:
+        assert np.linalg.norm(g) == 0, f"{name}: expected exact zero"
+        return
+    rel = np.linalg.norm(g - want) / nw
+    cos = float(np.dot(g.ravel(), want.ravel()) / (np.linalg.norm(g) * nw))
+    ratio = np.linalg.norm(g) / nw
+    assert rel <= rtol, f"{name}: rel L2 {rel:.3e}"
+    assert cos > 0.999, f"{name}: cosine {cos}"
+    assert abs(ratio - 1) < 0.02, f"{name}: norm ratio {ratio}"
+
+
+def run_case(flp, d, *, chunk_rows=0, dx_dtype=torch.bfloat16, check_backward=True, rows=None,
+             dw_rows=None):
+    dev = torch.device("cuda")
+    X, W, y = d["X"].to(dev), d["W"].to(dev), d["y"].to(dev)
+    M, H = X.shape
+    V = W.shape[0]
+    ent = d["compute_entropy"]
+    ws = flp.alloc_workspace(M, H, V, ent, chunk_rows=chunk_rows, device=dev)
+    lp, lse, en = flp.forward(X, W, y, ignore_index=d["ignore_index"], scale=d["scale"],
+                              compute_entropy=ent, workspace=ws)
+    torch.cuda.synchronize()
+    assert flp.get_error(ws) == flp.FLP_OK
+    Xb, Wb = inputs.bf16_bits(d["X"]), inputs.bf16_bits(d["W"])
+    yn = d["y"].numpy()
+    o_lp, o_lse, o_en = oracle.forward(Xb, Wb, yn, ignore_index=d["ignore_index"], scale=d["scale"],
+                                       compute_entropy=ent, rows=rows)
+    sel = slice(None) if rows is None else torch.as_tensor(rows)
+    check_fwd(lp.cpu()[sel], o_lp, "logprob")
+    check_fwd(lse.cpu()[sel], o_lse, "lse")
+    if ent:
+        check_fwd(en.cpu()[sel], o_en, "entropy")
+    if not check_backward:
+        return dict(lp=lp, lse=lse, en=en, ws=ws)
+    g1 = d["g_lp"]
+    g2 = d["g_ent"] if ent else None
+    if dw_rows is not None:  # gradients only on a sample of rows: dW is then exact to compare
+        mask = torch.zeros(M, dtype=torch.float32)
+        mask[torch.as_tensor(dw_rows)] = 1
+        g1 = g1 * mask
+        g2 = None if g2 is None else g2 * mask
+    dX, dW = flp.backward(X, W, y, lse, en, g1.to(dev), None if g2 is None else g2.to(dev),
+                          ignore_index=d["ignore_index"], scale=d["scale"], compute_entropy=ent,
+                          dx_dtype=dx_dtype, workspace=ws)
+    torch.cuda.synchronize()
+    assert flp.get_error(ws) == flp.FLP_OK
+    g1n = g1.double().numpy()
+    g2n = None if g2 is None else g2.double().numpy()
+    if dw_rows is None and rows is None:
+        o_dx, o_dw = oracle.backward(Xb, Wb, yn, g1n, g2n, ignore_index=d["ignore_index"],
+                                     scale=d["scale"], compute_entropy=ent)
+        check_grad(dX, o_dx, "dX")
+        check_grad(dW, o_dw, "dW")
+    else:
+        if rows is not None:
+            o_dx, _ = oracle.backward(Xb, Wb, yn, g1n, g2n, ignore_index=d["ignore_index"],
+                                      scale=d["scale"], compute_entropy=ent, rows=rows,
+                                      want_dw=False)
+            if dw_rows is not None:
+                keep = np.isin(rows, dw_rows)
+                check_grad(dX.cpu()[torch.as_tensor(rows[keep])], o_dx[keep], "dX rows")
+                assert np.all(_np(dX.cpu()[torch.as_tensor(rows[~keep])]) == 0)
+            else:
+                check_grad(dX.cpu()[torch.as_tensor(rows)], o_dx, "dX rows")
+        if dw_rows is not None:
+            _, o_dw = oracle.backward(Xb, Wb, yn, g1n, g2n, ignore_index=d["ignore_index"],
+                                      scale=d["scale"], compute_entropy=ent, rows=dw_rows,
+                                      want_dx=False)
+            check_grad(dW, o_dw, "dW")
+    return dict(lp=lp, lse=lse, en=en, dX=dX, dW=dW, ws=ws)
+
+
+def case(M, H, V, seed=11, **kw):
+    kw.setdefault("w_std", 0.05)
+    kw.setdefault("ignore_frac", 0.1)
+    return inputs.make_inputs(inputs.custom(f"m{M}_h{H}_v{V}", M, H, V, seed=seed, **kw))
+
+
+# ----------------------------------------------------------------- small shapes
+
+def test_tiny_workload(flp):
+    run_case(flp, inputs.make_inputs(inputs.WORKLOADS["tiny"]))
+
+
+@pytest.mark.parametrize("M,H,V", [
+    (1, 64, 1), (1, 8, 2), (127, 64, 255), (128, 64, 256), (129, 72, 257),
+    (300, 200, 3001), (5, 8, 50257 // 16), (513, 264, 1000),
+])
+def test_edge_shapes(flp, M, H, V):
+    run_case(flp, case(M, H, V))
+
+
+@pytest.mark.parametrize("ent", [True, False])
+@pytest.mark.parametrize("scale", [0.5, 1.0, 1.0 / 0.7])
+def test_scale_and_entropy_flag(flp, ent, scale):
+    run_case(flp, case(200, 128, 1500, seed=3, scale=scale, compute_entropy=ent))
+
+
+def test_waves_and_ragged_tail(flp):
+    # 700 rows in 256-row waves: three waves, the last one ragged; dW accumulates
+    # across waves in fp32.
+    run_case(flp, case(700, 136, 2100, seed=4), chunk_rows=256)
+
+
+def test_dx_fp32(flp):
+    run_case(flp, case(260, 96, 999, seed=5), dx_dtype=torch.float32)
+
+
+def test_hot_rows_and_strongly_negative_logits(flp):
+    # rows scaled x50 and x100 (logit std ~50 and ~100), and a row whose logits
+    # are all -1000 (exp underflows without the max shift): feature 0 is zero
+    # everywhere except that row, and W's column 0 is -1000.
+    d = case(256, 64, 2000, seed=6, w_std=1.0 / 8)
+    X = d["X"].float()
+    X[:, 0] = 0
+    X[3] *= 50
+    X[77] *= 100
+    X[100, :] = 0
+    X[100, 0] = 1.0
+    W = d["W"].float()
+    W[:, 0] = -1000.0
+    d["X"] = X.to(torch.bfloat16)
+    d["W"] = W.to(torch.bfloat16)
+    r = run_case(flp, d, check_backward=False)
+    assert abs(float(r["en"][100]) - np.log(2000)) < 1e-3
+    # Backward.  dX[:, 0] = -1000 * sum_j dZ_ij is zero in exact arithmetic but
+    # not once dZ is rounded to bf16 (the contract's rounding point), so that
+    # one column measures rounding noise times 1000; every other entry of dX and
+    # all of dW are compared.
+    dev = torch.device("cuda")
+    X, W, y = d["X"].to(dev), d["W"].to(dev), d["y"].to(dev)
+    dX, dW = flp.backward(X, W, y, r["lse"], r["en"], d["g_lp"].to(dev), d["g_ent"].to(dev),
+                          workspace=r["ws"])
+    Xb, Wb = inputs.bf16_bits(d["X"]), inputs.bf16_bits(d["W"])
+    o_dx, o_dw = oracle.backward(Xb, Wb, d["y"].numpy(), d["g_lp"].double().numpy(),
+                                 d["g_ent"].double().numpy())
+    check_grad(dX[:, 1:], o_dx[:, 1:], "dX[:, 1:]")
+    check_grad(dW, o_dw, "dW")
+
+
+def test_all_rows_ignored_and_custom_ignore_index(flp):
+    d = case(130, 64, 700, seed=7)
+    d["y"][:] = -100
+    r = run_case(flp, d)
+    assert torch.all(r["lp"] == 0) and torch.all(r["en"] == 0)
+    assert torch.all(r["dX"] == 0) and torch.all(r["dW"] == 0)
+    d = case(130, 64, 700, seed=8)
+    d["y"][::3] = 5
+    d["ignore_index"] = 5
+    run_case(flp, d)
+
+
+def test_zero_gradients_and_accumulate(flp):
+    dev = torch.device("cuda")
+    d = case(300, 64, 900, seed=9)
+    X, W, y = d["X"].to(dev), d["W"].to(dev), d["y"].to(dev)
+    ws = flp.alloc_workspace(300, 64, 900, True, device=dev)
+    lp, lse, en = flp.forward(X, W, y, workspace=ws)
+    dX, dW = flp.backward(X, W, y, lse, en, None, None, workspace=ws)
+    torch.cuda.synchronize()
+    assert torch.all(dX == 0) and torch.all(dW == 0)
+    g1, g2 = d["g_lp"].to(dev), d["g_ent"].to(dev)
+    _, dW1 = flp.backward(X, W, y, lse, en, g1, g2, workspace=ws)
+    base = torch.randn(900, 64, device=dev)
+    dW2 = base.clone()
+    flp.backward(X, W, y, lse, en, g1, g2, dW=dW2, accumulate_dW=True, workspace=ws)
+    torch.cuda.synchronize()
+    torch.testing.assert_close(dW2, base + dW1, rtol=1e-6, atol=1e-6)
+
+
+def test_determinism(flp):
+    dev = torch.device("cuda")
+    d = case(700, 136, 2100, seed=10)
+    X, W, y = d["X"].to(dev), d["W"].to(dev), d["y"].to(dev)
+    g1, g2 = d["g_lp"].to(dev), d["g_ent"].to(dev)
+    ws = flp.alloc_workspace(700, 136, 2100, True, chunk_rows=256, device=dev)
+    outs = []
+    for _ in range(2):
+        lp, lse, en = flp.forward(X, W, y, workspace=ws)
+        dX, dW = flp.backward(X, W, y, lse, en, g1, g2, workspace=ws)
+        outs.append([t.clone() for t in (lp, lse, en, dX, dW)])
+    torch.cuda.synchronize()
+    for a, b in zip(*outs):
+        assert torch.equal(a, b)
+
+
+def test_bad_target_sets_error_word(flp):
+    dev = torch.device("cuda")
+    d = case(140, 64, 500, seed=12)
+    d["y"][7] = 500
+    d["y"][9] = -3
+    X, W, y = d["X"].to(dev), d["W"].to(dev), d["y"].to(dev)
+    ws = flp.alloc_workspace(140, 64, 500, True, device=dev)
+    lp, lse, en = flp.forward(X, W, y, workspace=ws)
+    assert flp.get_error(ws) == flp.FLP_ERR_BAD_TARGET
+    assert torch.isnan(lp[7]) and torch.isnan(lp[9])
+    assert torch.isfinite(lp[:7]).all()
+    # the next call clears the word
+    d2 = case(140, 64, 500, seed=12)
+    flp.forward(X, W, d2["y"].to(dev), workspace=ws)
+    assert flp.get_error(ws) == flp.FLP_OK
+
+
+def test_argument_errors(flp):
+    dev = torch.device("cuda")
+    d = case(64, 64, 300, seed=13)
+    X, W, y = d["X"].to(dev), d["W"].to(dev), d["y"].to(dev)
+    fwd, bwd = flp.workspace_query(64, 64, 300, True)
+    small = torch.empty(fwd - 1024, dtype=torch.uint8, device=dev)
+    with pytest.raises(flp.FlpError) as e:
+        flp.forward(X, W, y, workspace=small)
+    assert e.value.status == flp.FLP_ERR_WORKSPACE
+    tiny_ws = torch.empty(2048, dtype=torch.uint8, device=dev)
+    lse = torch.zeros(64, device=dev)
+    en = torch.zeros(64, device=dev)
+    with pytest.raises(flp.FlpError) as e:
+        flp.backward(X, W, y, lse, en, lse, en, workspace=tiny_ws)
+    assert e.value.status == flp.FLP_ERR_WORKSPACE
+    Xo = torch.zeros(64, 60, dtype=torch.bfloat16, device=dev)
+    Wo = torch.zeros(300, 60, dtype=torch.bfloat16, device=dev)
+    ws = flp.alloc_workspace(64, 64, 300, True, device=dev)
+    with pytest.raises(flp.FlpError) as e:
+        flp.forward(Xo[:, :60], Wo, y, workspace=ws)
+    assert e.value.status == flp.FLP_ERR_UNSUPPORTED
+
+
+def test_autograd_wrapper(flp):
+    dev = torch.device("cuda")
+    d = case(200, 64, 1000, seed=14)
+    X = d["X"].to(dev).requires_grad_(True)
+    W = d["W"].to(dev).requires_grad_(True)
+    y = d["y"].to(dev)
+    lp, en = flp.fused_linear_logprob(X, W, y)
+    (lp * d["g_lp"].to(dev)).sum().backward(retain_graph=True)
+    Xb, Wb = inputs.bf16_bits(d["X"]), inputs.bf16_bits(d["W"])
+    o_dx, o_dw = oracle.backward(Xb, Wb, d["y"].numpy(), d["g_lp"].double().numpy(), None)
+    check_grad(X.grad, o_dx, "dX")
+    check_grad(W.grad, o_dw, "dW", rtol=2e-2)  # W.grad is rounded to bf16 (W's dtype)
+
+
+# ------------------------------------------------- full-size workloads (sampled)
+
+@pytest.mark.parametrize("name", sorted(inputs.WORKLOADS))
+def test_workload_full_size_sampled(flp, name):
+    """The workload at its full size in the launch configuration the bench
+    times; forward on a seeded row sample (all tile boundaries near the end
+    included), dX on those rows, and dW exactly, with upstream gradients kept
+    on a sub-sample of rows so the oracle can form dW from them alone."""
+    w = inputs.WORKLOADS[name]
+    d = inputs.make_inputs(w)
+    n = 48 if w.M * w.V < 4e9 else 24
+    rows = inputs.sample_rows(w.M, n, seed=21).numpy()
+    dw_rows = rows[::3]
+    run_case(flp, d, rows=rows, dw_rows=dw_rows)
