@@ -71,6 +71,11 @@ WORKLOADS = {
         Workload("ragged_m20001_h4096_v128257", 20001, 4096, 128257, ignore_frac=0.05,
                  hot_row_frac=0.01, hot_row_mult=50.0, seed=1004),
         Workload("large_m32768_h5120_v152064", 32768, 5120, 152064, targets="zipf", seed=1005),
+        # the headline recipe with a quarter of the vocabulary: every operand is
+        # still larger than L2 but the device footprint stays near 1 GB, the
+        # size used for full ncu captures of the kernels
+        Workload("quarter_vocab_m4096_h4096_v32768", 4096, 4096, 32768, ignore_frac=0.05,
+                 seed=1006),
     ]
 }
 

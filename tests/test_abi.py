@@ -1,0 +1,117 @@
+"""The C ABI library on the CPU: it builds, loads, exports every symbol that
+include/flp.h declares, and rejects bad arguments before touching a device."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "flp.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from entropy_loss_gb300 import build, flp
+    build.build()
+    return flp.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^\s*(?:flp_status|const char\s*\*)\s*(flp_\w+)\s*\(", text, re.M)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("flp_workspace_query", "flp_forward", "flp_backward", "flp_get_error"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    from entropy_loss_gb300 import build
+    out = subprocess.run(["nm", "-D", "--defined-only", build.LIB], capture_output=True, text=True,
+                         check=True).stdout
+    exported = set(re.findall(r"\bT\s+(flp_\w+)", out))
+    missing = [n for n in declared_functions() if n not in exported]
+    assert not missing, f"declared but not exported: {missing}"
+    for n in declared_functions():
+        assert hasattr(lib, n)
+
+
+def test_binding_lists_the_same_exports():
+    from entropy_loss_gb300 import flp
+    assert sorted(flp.EXPORTS) == declared_functions()
+
+
+def test_status_strings(lib):
+    for code in range(0, 7):
+        assert lib.flp_status_string(code)
+    assert b"unknown" in lib.flp_status_string(99)
+
+
+def _fwd(lib, **over):
+    buf = ctypes.create_string_buffer(4096 + 16)
+    base = (ctypes.addressof(buf) + 15) // 16 * 16
+    a = dict(X=base, W=base, y=base, M=4, H=64, V=10, ign=-100, s=1.0, ent=1, lp=base, lse=base,
+             en=base, ws=base, wsb=4096, stream=None)
+    a.update(over)
+    return lib.flp_forward(a["X"], a["W"], a["y"], a["M"], a["H"], a["V"], a["ign"], a["s"], a["ent"],
+                           a["lp"], a["lse"], a["en"], a["ws"], a["wsb"], a["stream"])
+
+
+def test_forward_argument_checks_need_no_device(lib):
+    from entropy_loss_gb300 import flp
+    assert _fwd(lib, M=-1) == flp.FLP_ERR_INVALID_ARG
+    assert _fwd(lib, V=0) == flp.FLP_ERR_INVALID_ARG
+    assert _fwd(lib, H=60) == flp.FLP_ERR_UNSUPPORTED
+    assert _fwd(lib, X=None) == flp.FLP_ERR_INVALID_ARG
+    assert _fwd(lib, W=None) == flp.FLP_ERR_INVALID_ARG
+    assert _fwd(lib, y=None) == flp.FLP_ERR_INVALID_ARG
+    buf = ctypes.create_string_buffer(64)
+    odd = (ctypes.addressof(buf) + 15) // 16 * 16 + 4
+    assert _fwd(lib, X=odd) == flp.FLP_ERR_INVALID_ARG
+    assert _fwd(lib, en=None) == flp.FLP_ERR_INVALID_ARG          # entropy on but no buffer
+    assert _fwd(lib, ent=0) == flp.FLP_ERR_INVALID_ARG            # entropy off but a buffer
+    assert _fwd(lib, s=float("nan")) == flp.FLP_ERR_INVALID_ARG
+    assert _fwd(lib, M=2**31) == flp.FLP_ERR_UNSUPPORTED
+
+
+def test_backward_argument_checks_need_no_device(lib):
+    from entropy_loss_gb300 import flp
+    buf = ctypes.create_string_buffer(4096 + 16)
+    b = (ctypes.addressof(buf) + 15) // 16 * 16
+
+    def call(**o):
+        a = dict(X=b, W=b, y=b, M=4, H=64, V=10, ent=1, lse=b, en=b, g1=b, g2=b, dX=b, dxt=1, dW=b,
+                 dwt=0, acc=0, ws=b, wsb=4096)
+        a.update(o)
+        return lib.flp_backward(a["X"], a["W"], a["y"], a["M"], a["H"], a["V"], -100, 1.0, a["ent"],
+                                a["lse"], a["en"], a["g1"], a["g2"], a["dX"], a["dxt"], a["dW"],
+                                a["dwt"], a["acc"], a["ws"], a["wsb"], None)
+
+    assert call(dX=None) == flp.FLP_ERR_INVALID_ARG
+    assert call(dW=None) == flp.FLP_ERR_INVALID_ARG
+    assert call(dxt=7) == flp.FLP_ERR_INVALID_ARG
+    assert call(dwt=1) == flp.FLP_ERR_UNSUPPORTED
+    assert call(lse=None) == flp.FLP_ERR_INVALID_ARG
+    assert call(en=None) == flp.FLP_ERR_INVALID_ARG
+    assert call(H=12) == flp.FLP_ERR_UNSUPPORTED
+
+
+def test_phase_event_count_checked(lib):
+    from entropy_loss_gb300 import flp
+    assert lib.flp_set_phase_events(None, 11) == flp.FLP_ERR_INVALID_ARG
+    assert lib.flp_set_phase_events(None, -1) == flp.FLP_ERR_INVALID_ARG
+    assert lib.flp_set_phase_events(None, 0) == flp.FLP_OK
+
+
+def test_product_path_never_imports_the_oracle():
+    pkg = os.path.join(ROOT, "entropy_loss_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert not re.search(r"^\s*(import|from)\s+oracle\b", text, re.M), f
+                assert "flp_oracle" not in text and "libflp_oracle" not in text, f
