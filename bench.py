@@ -334,9 +334,12 @@ def cpu_baseline(d, w, seconds):
     import oracle
     oracle.build()
     g = np.random.default_rng(0)
-    one = g.choice(w.M, 1, replace=False)
-    t1 = _oracle_sample_time(d, one, oracle)
-    n = int(max(1, min(w.M, seconds / max(t1, 1e-6))))
+    # two-point calibration: t(n) = a + b n (a: the dW buffer and other fixed costs)
+    t1 = _oracle_sample_time(d, g.choice(w.M, 1, replace=False), oracle)
+    t8 = _oracle_sample_time(d, g.choice(w.M, 8, replace=False), oracle)
+    b = max((t8 - t1) / 7.0, 1e-6)
+    a = max(t1 - b, 0.0)
+    n = int(max(1, min(w.M, (seconds - a) / b)))
     rows = g.choice(w.M, n, replace=False)
     t = _oracle_sample_time(d, rows, oracle)
     value = 8.0 * w.H * w.V * n / t / 1e12
