@@ -531,3 +531,120 @@ flp_status flp_get_error(const void* workspace, void* stream) {
 }
 
 }  // extern "C"
+
+// ======================================================= allocation-free forward
+//
+// For callers that cannot allocate device memory (see flp_forward_noalloc in
+// include/flp.h): the forward's scratch (header with the error word, the
+// per-split partials and the target logits) lives in this file-scope device
+// array instead of a caller workspace.  Host code only ever uses the array's
+// device address, looked up once per device with that device current.
+
+static __device__ __align__(256) uint8_t g_flp_static_scratch[FLP_STATIC_SCRATCH_BYTES];
+
+namespace {
+
+void* g_static_scratch_addr[kMaxDevices] = {};
+
+flp_status static_scratch(int dev, uint8_t** out) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_static_scratch_addr[dev]) {
+        void* p = nullptr;
+        cudaError_t e = cudaGetSymbolAddress(&p, g_flp_static_scratch);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(static scratch)");
+        if (!p) return fail(FLP_ERR_CUDA, "static scratch has no device address");
+        g_static_scratch_addr[dev] = p;
+    }
+    *out = static_cast<uint8_t*>(g_static_scratch_addr[dev]);
+    return FLP_OK;
+}
+
+}  // namespace
+
+extern "C" flp_status flp_forward_noalloc(const void* X, const void* W, const int64_t* targets,
+                                          int64_t M, int64_t H, int64_t V, int64_t ignore_index,
+                                          float scale, int compute_entropy, float* logprob,
+                                          float* lse, float* entropy, void* stream) {
+    flp_status st = common_checks(X, W, targets, M, H, V);
+    if (st != FLP_OK) return st;
+    const int ent = compute_entropy ? 1 : 0;
+    if (!logprob || !lse || (ent && !entropy) || (!ent && entropy))
+        return fail(FLP_ERR_INVALID_ARG, "logprob and lse required; entropy iff compute_entropy");
+    if (!aligned16(logprob) || !aligned16(lse) || (entropy && !aligned16(entropy)))
+        return fail(FLP_ERR_INVALID_ARG, "outputs must be 16-byte aligned");
+    if (!std::isfinite(scale)) return fail(FLP_ERR_INVALID_ARG, "scale must be finite");
+    DevInfo* d;
+    int dev = 0;
+    st = device_info(&d, &dev);
+    if (st != FLP_OK) return st;
+    st = check_device(&d);
+    if (st != FLP_OK) return st;
+    const FwdPlan f = plan_forward(M, H, V, ent, d->sm_count);
+    if (f.bytes > FLP_STATIC_SCRATCH_BYTES) {
+        char buf[200];
+        snprintf(buf, sizeof buf,
+                 "problem needs %zu bytes of forward scratch; the static scratch holds %u bytes",
+                 f.bytes, static_cast<unsigned>(FLP_STATIC_SCRATCH_BYTES));
+        return fail(FLP_ERR_UNSUPPORTED, buf);
+    }
+    uint8_t* ws = nullptr;
+    st = static_scratch(dev, &ws);
+    if (st != FLP_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int* err = reinterpret_cast<int*>(ws);
+    FLP_CUDA(cudaMemsetAsync(ws, 0, kHeaderBytes, s));  // the array keeps the last call's contents
+    if (M == 0) return FLP_OK;
+
+    CUtensorMap tmX, tmW;
+    st = tmap_2d(&tmX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, X, H, M, H * 2, BK, BM);
+    if (st != FLP_OK) return st;
+    st = tmap_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, W, H, V, H * 2, BK, BN);
+    if (st != FLP_OK) return st;
+
+    TileParams p{};
+    p.units = f.units;
+    p.Mt = f.Mt;
+    p.Nt = f.Vt;
+    p.S = f.S;
+    p.tps = f.tps;
+    p.GM = f.GM;
+    p.KB = static_cast<int>(cdiv(H, BK));
+    p.M = static_cast<int>(M);
+    p.V = static_cast<int>(V);
+    p.row0 = 0;
+    p.ignore_index = ignore_index;
+    p.scale = scale;
+    p.scale2 = scale * LOG2E;
+    p.compute_entropy = ent;
+    p.y = reinterpret_cast<const long long*>(targets);
+    p.part_m = reinterpret_cast<float*>(ws + f.off_m);
+    p.part_s = reinterpret_cast<float*>(ws + f.off_s);
+    p.part_t = ent ? reinterpret_cast<float*>(ws + f.off_t) : nullptr;
+    p.zy = reinterpret_cast<float*>(ws + f.off_zy);
+    p.err = err;
+    p.wait_limit_ns = kWaitLimitNs;
+    p.debug_stall_after = -1;
+    st = ent ? launch_tile<kFwd, true, false>(f.grid, tmX, tmW, tmX, p, s)
+             : launch_tile<kFwd, false, false>(f.grid, tmX, tmW, tmX, p, s);
+    if (st != FLP_OK) return st;
+
+    MergeParams mp{};
+    mp.M = static_cast<int>(M);
+    mp.S = f.S;
+    mp.V = static_cast<int>(V);
+    mp.ignore_index = ignore_index;
+    mp.compute_entropy = ent;
+    mp.y = p.y;
+    mp.part_m = p.part_m;
+    mp.part_s = p.part_s;
+    mp.part_t = p.part_t;
+    mp.zy = p.zy;
+    mp.logprob = logprob;
+    mp.lse = lse;
+    mp.entropy = entropy;
+    mp.err = err;
+    flp_merge_kernel<<<static_cast<unsigned>(cdiv(M, 256)), 256, 0, s>>>(mp);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "flp_merge_kernel launch");
+    return FLP_OK;
+}

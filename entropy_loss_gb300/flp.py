@@ -26,7 +26,9 @@ FLP_F32 = 0
 FLP_BF16 = 1
 
 EXPORTS = ("flp_workspace_query", "flp_forward", "flp_backward", "flp_get_error",
-           "flp_set_phase_events", "flp_status_string", "flp_last_error_message")
+           "flp_set_phase_events", "flp_status_string", "flp_last_error_message",
+           "flp_forward_noalloc")
+STATIC_SCRATCH_BYTES = 16 << 20
 PHASES = ("fwd", "merge", "dz", "dx", "dw")
 
 
@@ -54,6 +56,9 @@ def load(path: str = LIB_PATH):
                                 ctypes.c_size_t, p]
     lib.flp_backward.argtypes = [p, p, p, i64, i64, i64, i64, ctypes.c_float, i32, p, p, p, p, p,
                                  i32, p, i32, i32, p, ctypes.c_size_t, p]
+    lib.flp_forward_noalloc.argtypes = [p, p, p, i64, i64, i64, i64, ctypes.c_float, i32, p, p, p,
+                                        p]
+    lib.flp_forward_noalloc.restype = i32
     lib.flp_get_error.argtypes = [p, p]
     lib.flp_set_phase_events.argtypes = [ctypes.POINTER(ctypes.c_void_p), i32]
     lib.flp_set_phase_events.restype = i32
@@ -127,6 +132,24 @@ def forward(X, W, y, *, ignore_index: int = -100, scale: float = 1.0, compute_en
     _check(load().flp_forward(_ptr(X), _ptr(W), _ptr(y), M, H, V, ignore_index, float(scale),
                               int(compute_entropy), _ptr(logprob), _ptr(lse), _ptr(entropy),
                               _ptr(workspace), workspace.numel(), _stream(stream)), "flp_forward")
+    return logprob, lse, entropy
+
+
+def forward_noalloc(X, W, y, logprob, lse, entropy=None, *, ignore_index: int = -100,
+                    scale: float = 1.0, compute_entropy: bool = True, stream=None):
+    """flp_forward_noalloc: the forward without a workspace, for callers that
+    cannot allocate device memory; its scratch is the library's fixed 16 MiB
+    device array, shared by every call (calls that overlap on the GPU race).
+    The outputs are caller-provided; nothing is allocated here."""
+    M, H = X.shape
+    V = W.shape[0]
+    _need(X, torch.bfloat16, (M, H), "X")
+    _need(W, torch.bfloat16, (V, H), "W")
+    _need(y, torch.int64, (M,), "targets")
+    _check(load().flp_forward_noalloc(_ptr(X), _ptr(W), _ptr(y), M, H, V, ignore_index,
+                                      float(scale), int(compute_entropy), _ptr(logprob), _ptr(lse),
+                                      _ptr(entropy if compute_entropy else None), _stream(stream)),
+           "flp_forward_noalloc")
     return logprob, lse, entropy
 
 

@@ -128,6 +128,34 @@ flp_status flp_backward(const void* X, const void* W, const int64_t* targets, in
                         void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * Forward that allocates nothing and takes no workspace.  The pages have no
+ * counterpart; it exists for callers that cannot call cudaMalloc and have no
+ * workspace to hand: code running inside a host framework that owns every
+ * device allocation and gives its plugins no allocator, or latency-critical
+ * loops where the implicit device synchronisation of cudaMalloc/cudaFree is
+ * not acceptable.  Arguments and outputs are those of flp_forward; the
+ * per-split partials and the error word live instead in one file-scope
+ * device array of FLP_STATIC_SCRATCH_BYTES (16 MiB) that every GPU which
+ * loads this library holds until the process exits.
+ *  - Problems whose forward workspace (flp_workspace_query's fwd_bytes) exceeds
+ *    that size are rejected with FLP_ERR_UNSUPPORTED before any launch.
+ *  - The first call on a device looks up the array's device address on that
+ *    device (cudaGetSymbolAddress, with the device current); make that first
+ *    call before any stream capture.  No cudaMalloc, cudaFree or allocating
+ *    library routine is ever called.
+ *  - Every call, on any stream, shares the one array and it keeps the last
+ *    call's contents (each call clears its error word first): calls that
+ *    overlap on the GPU race and corrupt each other's results.
+ *  - Out-of-range targets still give logprob = NaN; the error word of this
+ *    array is not readable through flp_get_error.
+ */
+#define FLP_STATIC_SCRATCH_BYTES (16u << 20)
+flp_status flp_forward_noalloc(const void* X, const void* W, const int64_t* targets, int64_t M,
+                               int64_t H, int64_t V, int64_t ignore_index, float scale,
+                               int compute_entropy, float* logprob, float* lse, float* entropy,
+                               void* stream);
+
+/*
  * Synchronises `stream`, then reads and returns the workspace's error word
  * (FLP_OK, FLP_ERR_BAD_TARGET or FLP_ERR_TIMEOUT) written by the most recent
  * flp_forward / flp_backward that used this workspace.  Each of those calls
