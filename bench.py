@@ -229,16 +229,18 @@ def run_ours(args, world, rank, local):
     _, bwd_bytes = flp.workspace_query(M, H, V, ent)
     wave_rows = min(M, ((ws.numel() - 1024) // (((V + 255) // 256) * 256 * 2)) // 128 * 128)
     phase_flops = {"fwd": 2.0 * M * H * V, "dz": 2.0 * wave_rows * H * V,
-                   "dx": 2.0 * wave_rows * H * V, "dw": 2.0 * wave_rows * H * V}
+                   "bwd_gemm": 4.0 * wave_rows * H * V}  # dX and dW of the first wave
     dom = max(phase_flops, key=lambda n: phase_ms[n])
     achieved = phase_flops[dom] / (phase_ms[dom] * 1e-3) / 1e12
     peak = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
-    roofline = {"bound": "tensor", "kernel": f"flp_tile_kernel<{dom}>", "achieved": round(achieved, 1),
+    kname = {"fwd": "flp_tile_kernel<fwd>", "dz": "flp_tile_kernel<dz>",
+             "bwd_gemm": "flp_bwd_gemm_kernel"}[dom]
+    roofline = {"bound": "tensor", "kernel": kname, "achieved": round(achieved, 1),
                 "peak": peak, "unit": UNIT, "frac": round(achieved / peak, 4),
                 "traffic": None, "peak_source": f"bf16_tflops_sustained of {peak_src}"}
 
     waves = -(-M // wave_rows)
-    launches = K * (2 + 3 * waves)
+    launches = K * (2 + 2 * waves)
 
     result = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": K,

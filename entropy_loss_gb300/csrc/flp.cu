@@ -50,7 +50,8 @@ flp_status cuda_fail(cudaError_t e, const char* where) {
     } while (0)
 
 constexpr int kMaxDevices = 64;
-constexpr size_t kHeaderBytes = 1024;      // error word + padding; keeps regions 1 KiB aligned
+constexpr size_t kHeaderBytes = 1024;      // error word, ticket counter; keeps regions 1 KiB aligned
+constexpr size_t kTicketOffset = 8;        // 64-bit tile ticket counter of the backward contractions
 constexpr int64_t kDefaultChunkRows = 4096;
 constexpr unsigned long long kWaitLimitNs = 10ull * 1000 * 1000 * 1000;  // 10 s per wait
 
@@ -208,9 +209,12 @@ flp_status ensure_attrs(DevInfo* d) {
     if (e == cudaSuccess) e = set_smem_attr<kFwd, false, false>();
     if (e == cudaSuccess) e = set_smem_attr<kDz, true, false>();
     if (e == cudaSuccess) e = set_smem_attr<kDz, false, false>();
-    if (e == cudaSuccess) e = set_smem_attr<kDx, false, false>();
-    if (e == cudaSuccess) e = set_smem_attr<kDx, false, true>();
-    if (e == cudaSuccess) e = set_smem_attr<kDw, false, true>();
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(flp_bwd_gemm_kernel<false>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_ALLOC_BWD);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(flp_bwd_gemm_kernel<true>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_ALLOC_BWD);
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
     std::lock_guard<std::mutex> lk(g_mu);
     d->attrs_set = true;
@@ -412,6 +416,7 @@ flp_status flp_backward(const void* X, const void* W, const int64_t* targets, in
         return FLP_OK;
     }
     void* dz = ws + kHeaderBytes;
+    unsigned long long ticket_base = 0;
 
     CUtensorMap tmW_k, tmW_mn, tmDW;
     st = tmap_2d(&tmW_k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, W, H, V, H * 2, BK, BN);
@@ -474,47 +479,34 @@ flp_status flp_backward(const void* X, const void* W, const int64_t* targets, in
         if (st != FLP_OK) return st;
         if (first) mark(5, s);
 
-        // (2) dX[wave] = dZ W   (K = Vp)
-        TileParams q{};
-        q.Mt = static_cast<int>(cdiv(rows, BM));
+        // (2) dX[wave] = dZ W (K = Vp) and dW (+)= dZ^T X[wave] (K = wave rows),
+        // one persistent launch; the ticket counter lives in the zeroed header
+        // and every launch consumes units + grid tickets.
+        BwdParams q{};
+        q.Mt_dx = static_cast<int>(cdiv(rows, BM));
         q.Nt = Nt_h;
-        q.S = Nt_h;
-        q.tps = 1;
-        q.GM = q.Mt;  // M-tiles fastest: concurrent CTAs share W's column block
-        q.units = q.Mt * q.Nt;
-        q.KB = static_cast<int>(Vp / BK);
-        q.M = static_cast<int>(rows);
-        q.V = static_cast<int>(V);
+        q.units_dx = q.Mt_dx * Nt_h;
+        q.units_dw = Vt * (BN / BM) * Nt_h;
+        q.KB_dx = static_cast<int>(Vp / BK);
+        q.KB_dw = static_cast<int>(cdiv(rows, BK));
+        q.dw_add = (accumulate_dW || r0 > 0) ? 1 : 0;
+        q.ticket = reinterpret_cast<unsigned long long*>(ws + kTicketOffset);
+        q.ticket_base = ticket_base;
         q.err = err;
         q.wait_limit_ns = kWaitLimitNs;
-        q.debug_stall_after = -1;
-        const int grid_dx = std::min(q.units, sms);
+        const int total = q.units_dx + q.units_dw;
+        const int grid_bw = std::min(total, sms);
+        ticket_base += static_cast<unsigned long long>(total) + grid_bw;
         if (first) mark(6, s);
-        st = (dX_dtype == FLP_F32) ? launch_tile<kDx, false, true>(grid_dx, tmDZk, tmW_mn, tmDX, q, s)
-                                   : launch_tile<kDx, false, false>(grid_dx, tmDZk, tmW_mn, tmDX, q, s);
-        if (st != FLP_OK) return st;
+        if (dX_dtype == FLP_F32)
+            flp_bwd_gemm_kernel<true><<<grid_bw, NUM_THREADS, SMEM_ALLOC_BWD, s>>>(
+                tmDZk, tmW_mn, tmDZmn, tmXmn, tmDX, tmDW, q);
+        else
+            flp_bwd_gemm_kernel<false><<<grid_bw, NUM_THREADS, SMEM_ALLOC_BWD, s>>>(
+                tmDZk, tmW_mn, tmDZmn, tmXmn, tmDX, tmDW, q);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return cuda_fail(e, "flp_bwd_gemm_kernel launch");
         if (first) mark(7, s);
-
-        // (3) dW (+)= dZ^T X[wave]   (K = rows of the wave)
-        TileParams w{};
-        w.Mt = Vt * (BN / BM);
-        w.Nt = Nt_h;
-        w.S = Nt_h;
-        w.tps = 1;
-        w.GM = 1;  // H-tiles fastest: concurrent CTAs share one dZ column block
-        w.units = w.Mt * w.Nt;
-        w.KB = static_cast<int>(cdiv(rows, BK));
-        w.M = static_cast<int>(Vp);
-        w.V = static_cast<int>(V);
-        w.dw_add = (accumulate_dW || r0 > 0) ? 1 : 0;
-        w.err = err;
-        w.wait_limit_ns = kWaitLimitNs;
-        w.debug_stall_after = -1;
-        const int grid_dw = std::min(w.units, sms);
-        if (first) mark(8, s);
-        st = launch_tile<kDw, false, true>(grid_dw, tmDZmn, tmXmn, tmDW, w, s);
-        if (st != FLP_OK) return st;
-        if (first) mark(9, s);
     }
     return FLP_OK;
 }

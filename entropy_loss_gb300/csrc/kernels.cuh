@@ -589,6 +589,328 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
 }
 
+// ----------------------------------------------- fused backward contractions
+//
+// dX and dW of one wave in a single persistent launch.  Units [0, units_dx)
+// are dX tiles (128 wave rows x 256 hidden columns, K = padded vocabulary,
+// M-tiles fastest), units [units_dx, units_dx + units_dw) are dW tiles (128
+// vocabulary rows x 256 hidden columns, K = wave rows, hidden tiles fastest).
+// CTAs take units in that order from a global ticket counter, so the long dX
+// tiles start first and the short dW tiles fill the tail evenly.  The producer
+// lane takes each ticket and hands the unit to the MMA and epilogue roles
+// through a small shared-memory ring guarded by mbarriers.
+
+constexpr int SCHED_SLOTS = 4;
+constexpr uint32_t SMEM_SCHED = SMEM_MISC + 16;                  // SCHED_SLOTS ints
+constexpr uint32_t SMEM_SCHED_BAR = SMEM_SCHED + 16;             // 2 * SCHED_SLOTS mbarriers
+constexpr uint32_t SMEM_ALLOC_BWD = SMEM_SCHED_BAR + 2 * SCHED_SLOTS * 8 + 1024;
+
+struct BwdParams {
+    int units_dx, units_dw;
+    int Mt_dx;   // 128-row tiles of the wave
+    int Nt;      // 256-column tiles of H
+    int KB_dx;   // K blocks of the padded vocabulary
+    int KB_dw;   // K blocks of the wave rows
+    int dw_add;  // 0: store dW tiles, 1: add them to dW
+    unsigned long long* ticket;   // global counter (zeroed by the call)
+    unsigned long long ticket_base;
+    int* err;
+    unsigned long long wait_limit_ns;
+};
+
+struct BwdUnit {
+    int dw, mt, nt, kb_count;
+};
+
+__device__ __forceinline__ BwdUnit decode_bwd(const BwdParams& p, int u) {
+    BwdUnit t;
+    if (u < p.units_dx) {
+        t.dw = 0;
+        t.mt = u % p.Mt_dx;
+        t.nt = u / p.Mt_dx;
+        t.kb_count = p.KB_dx;
+    } else {
+        const int v = u - p.units_dx;
+        t.dw = 1;
+        t.mt = v / p.Nt;
+        t.nt = v - t.mt * p.Nt;
+        t.kb_count = p.KB_dw;
+    }
+    return t;
+}
+
+template <bool kDxF32>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    flp_bwd_gemm_kernel(const __grid_constant__ CUtensorMap tmDzK,   // dZ, K-major A (dX)
+                        const __grid_constant__ CUtensorMap tmWmn,   // W, MN-major B (dX)
+                        const __grid_constant__ CUtensorMap tmDzMn,  // dZ, MN-major A (dW)
+                        const __grid_constant__ CUtensorMap tmXmn,   // X[wave], MN-major B (dW)
+                        const __grid_constant__ CUtensorMap tmDx,    // dX[wave] store boxes
+                        const __grid_constant__ CUtensorMap tmDw,    // dW store / add boxes
+                        const BwdParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + SMEM_BAR);
+    uint64_t* full = bars;
+    uint64_t* empty = bars + STAGES;
+    uint64_t* tfull = bars + 2 * STAGES;
+    uint64_t* tempty = bars + 2 * STAGES + 2;
+    uint64_t* drain = bars + 2 * STAGES + 4;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + SMEM_MISC);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + SMEM_MISC + 4);
+    volatile int* sched_val = reinterpret_cast<volatile int*>(smem + SMEM_SCHED);
+    uint64_t* sched_full = reinterpret_cast<uint64_t*>(smem + SMEM_SCHED_BAR);
+    uint64_t* sched_empty = sched_full + SCHED_SLOTS;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int total = p.units_dx + p.units_dw;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(&tfull[a], 1);
+            mbar_init(&tempty[a], EPI_THREADS);
+        }
+        for (int s = 0; s < SCHED_SLOTS; ++s) {
+            mbar_init(&sched_full[s], 1);
+            mbar_init(&sched_empty[s], 1 + EPI_THREADS);
+        }
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        fence_mbarrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmDzK);
+        tma_prefetch_desc(&tmWmn);
+        tma_prefetch_desc(&tmDzMn);
+        tma_prefetch_desc(&tmXmn);
+        tma_prefetch_desc(&tmDx);
+        tma_prefetch_desc(&tmDw);
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    const uint64_t limit = p.wait_limit_ns;
+
+    if (warp == 0) {
+        // ------------------------------------------- scheduler + TMA producer
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t issued_mask = 0, issued_parity = 0;
+            bool ok = true;
+            for (int it = 0; ok; ++it) {
+                const int slot = it % SCHED_SLOTS;
+                const uint32_t sph = static_cast<uint32_t>(it / SCHED_SLOTS) & 1u;
+                if (!mbar_wait(&sched_empty[slot], sph ^ 1u, limit, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                const unsigned long long tk = atomicAdd(p.ticket, 1ull) - p.ticket_base;
+                const int u = (tk < static_cast<unsigned long long>(total)) ? static_cast<int>(tk) : -1;
+                sched_val[slot] = u;
+                mbar_arrive(&sched_full[slot]);
+                if (u < 0) break;
+                const BwdUnit t = decode_bwd(p, u);
+                for (int kb = 0; kb < t.kb_count; ++kb) {
+                    if (!mbar_wait(&empty[stage], phase ^ 1u, limit, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&full[stage], STAGE_TX);
+                    uint8_t* a_dst = smem + SMEM_A + stage * A_STAGE_BYTES;
+                    uint8_t* b_dst = smem + SMEM_B + stage * B_STAGE_BYTES;
+                    if (!t.dw) {
+                        tma_load_2d(a_dst, &tmDzK, kb * BK, t.mt * BM, &full[stage]);
+#pragma unroll
+                        for (int j = 0; j < BN / 64; ++j)
+                            tma_load_2d(b_dst + j * 8192, &tmWmn, t.nt * BN + j * 64, kb * BK, &full[stage]);
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < BM / 64; ++j)
+                            tma_load_2d(a_dst + j * 8192, &tmDzMn, t.mt * BM + j * 64, kb * BK, &full[stage]);
+#pragma unroll
+                        for (int j = 0; j < BN / 64; ++j)
+                            tma_load_2d(b_dst + j * 8192, &tmXmn, t.nt * BN + j * 64, kb * BK, &full[stage]);
+                    }
+                    issued_mask |= 1u << stage;
+                    issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (!ok) {
+                atomicOr(p.err, ERR_TIMEOUT);
+                *abort_flag = 1;
+            }
+            for (int s = 0; s < STAGES; ++s)
+                if (issued_mask & (1u << s)) {
+                    volatile int no_abort = 0;
+                    mbar_wait(&full[s], (issued_parity >> s) & 1u, limit, &no_abort);
+                }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            int acc = 0;
+            uint32_t acc_phase = 0;
+            bool ok = true;
+            constexpr uint32_t idesc_dx = idesc_bf16_f32(BM, BN, 0, 1);
+            constexpr uint32_t idesc_dw = idesc_bf16_f32(BM, BN, 1, 1);
+            for (int it = 0; ok; ++it) {
+                const int slot = it % SCHED_SLOTS;
+                const uint32_t sph = static_cast<uint32_t>(it / SCHED_SLOTS) & 1u;
+                if (!mbar_wait(&sched_full[slot], sph, limit, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                const int u = sched_val[slot];
+                mbar_arrive(&sched_empty[slot]);
+                if (u < 0) break;
+                const BwdUnit t = decode_bwd(p, u);
+                if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, limit, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+                for (int kb = 0; kb < t.kb_count; ++kb) {
+                    if (!mbar_wait(&full[stage], phase, limit, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a_base = smem_addr(smem + SMEM_A + stage * A_STAGE_BYTES);
+                    const uint32_t b_base = smem_addr(smem + SMEM_B + stage * B_STAGE_BYTES);
+                    if (!t.dw) {
+#pragma unroll
+                        for (int k = 0; k < BK / UMMA_K; ++k)
+                            umma_bf16(d_tmem, operand_desc<0>(a_base, k), operand_desc<1>(b_base, k),
+                                      idesc_dx, (kb > 0 || k > 0) ? 1u : 0u);
+                    } else {
+#pragma unroll
+                        for (int k = 0; k < BK / UMMA_K; ++k)
+                            umma_bf16(d_tmem, operand_desc<1>(a_base, k), operand_desc<1>(b_base, k),
+                                      idesc_dw, (kb > 0 || k > 0) ? 1u : 0u);
+                    }
+                    umma_commit(&empty[stage]);
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                umma_commit(&tfull[acc]);
+                acc ^= 1;
+                if (acc == 0) acc_phase ^= 1u;
+            }
+            if (!ok) {
+                atomicOr(p.err, ERR_TIMEOUT);
+                *abort_flag = 1;
+            }
+            umma_commit(drain);
+            volatile int no_abort = 0;
+            mbar_wait(drain, 0, limit, &no_abort);
+        }
+    } else {
+        // --------------------------------------------------------- epilogue
+        const int et = threadIdx.x - 64;
+        const int q = warp & 3;
+        const int r = q * 32 + lane;
+        const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        bool ok = true;
+        StoreRing ring;
+        for (int it = 0; ok; ++it) {
+            const int slot = it % SCHED_SLOTS;
+            const uint32_t sph = static_cast<uint32_t>(it / SCHED_SLOTS) & 1u;
+            if (!mbar_wait(&sched_full[slot], sph, limit, abort_flag)) {
+                ok = false;
+                break;
+            }
+            const int u = sched_val[slot];
+            mbar_arrive(&sched_empty[slot]);
+            if (u < 0) break;
+            const BwdUnit t = decode_bwd(p, u);
+            if (!mbar_wait(&tfull[acc], acc_phase, limit, abort_flag)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const uint32_t tbase = tmem_base + static_cast<uint32_t>(acc * BN) + lane_off;
+            const int col0 = t.nt * BN;
+            if (!t.dw && !kDxF32) {
+#pragma unroll 1
+                for (int b = 0; b < BN / 64; ++b) {
+                    const uint32_t box = store_box_acquire(ring, smem, et);
+                    uint32_t w[32];
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        uint32_t v[32];
+                        tmem_ld_32x32b_x32(tbase + b * 64 + h * 32, v);
+                        tmem_wait_ld();
+                        if (b == BN / 64 - 1 && h == 1) {
+                            tc_fence_before();
+                            mbar_arrive(&tempty[acc]);
+                        }
+#pragma unroll
+                        for (int j = 0; j < 16; ++j)
+                            w[h * 16 + j] = pack_bf16x2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
+                    }
+                    stage_row(box, r, w);
+                    store_box_release<kDx>(ring, smem, et, &tmDx, col0 + b * 64, t.mt * BM, false);
+                }
+            } else {
+                const CUtensorMap* out = t.dw ? &tmDw : &tmDx;
+                const bool add = t.dw && p.dw_add;
+#pragma unroll 1
+                for (int b = 0; b < BN / 32; ++b) {
+                    const uint32_t box = store_box_acquire(ring, smem, et);
+                    uint32_t w[32];
+                    tmem_ld_32x32b_x32(tbase + b * 32, w);
+                    tmem_wait_ld();
+                    if (b == BN / 32 - 1) {
+                        tc_fence_before();
+                        mbar_arrive(&tempty[acc]);
+                    }
+                    stage_row(box, r, w);
+                    store_box_release<kDw>(ring, smem, et, out, col0 + b * 32, t.mt * BM, add);
+                }
+            }
+            acc ^= 1;
+            if (acc == 0) acc_phase ^= 1u;
+        }
+        if (!ok) {
+            atomicOr(p.err, ERR_TIMEOUT);
+            *abort_flag = 1;
+        }
+        if (et == 0) bulk_wait_group<0>();
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem_base, TMEM_COLS);
+    }
+}
+
 // ------------------------------------------------------------- split merge
 
 struct MergeParams {

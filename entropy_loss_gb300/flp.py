@@ -29,7 +29,7 @@ EXPORTS = ("flp_workspace_query", "flp_forward", "flp_backward", "flp_get_error"
            "flp_set_phase_events", "flp_status_string", "flp_last_error_message",
            "flp_forward_noalloc")
 STATIC_SCRATCH_BYTES = 16 << 20
-PHASES = ("fwd", "merge", "dz", "dx", "dw")
+PHASES = ("fwd", "merge", "dz", "bwd_gemm")
 
 
 class FlpError(RuntimeError):

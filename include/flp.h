@@ -169,8 +169,8 @@ flp_status flp_get_error(const void* workspace, void* stream);
  * before and events[2k+1] immediately after kernel phase k, on the call's
  * stream:
  *   k = 0  forward tile kernel          k = 1  split merge
- *   k = 2  dZ recompute (first wave)    k = 3  dX contraction (first wave)
- *   k = 4  dW contraction (first wave)
+ *   k = 2  dZ recompute (first wave)    k = 3  dX and dW contractions (first wave)
+ *   k = 4  reserved (never recorded)
  * `events` holds `count` (<= 10) caller-created cudaEvent_t handles passed as
  * void*; NULL entries are skipped.  events == NULL or count == 0 turns the
  * instrumentation off.  The array is copied; the events stay caller-owned.
