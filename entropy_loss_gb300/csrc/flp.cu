@@ -61,6 +61,7 @@ struct DevInfo {
     int sm_count = 0;
     int major = 0, minor = 0;
     bool attrs_set = false;
+    int pairs = 0;  // CTA pairs that can be resident at once (persistent grid size / 2)
 };
 DevInfo g_dev[kMaxDevices];
 std::mutex g_mu;
@@ -137,15 +138,16 @@ struct FwdPlan {
     size_t off_m, off_s, off_t, off_zy, bytes;
 };
 
-// Chooses the V-split: units are (M-tile, run of tps V-tiles); a static
-// round-robin over `sms` persistent CTAs finishes after ceil(units/sms) * tps
-// tiles.  Each extra split adds M * 24 bytes of partial traffic, charged in
-// tile-times so that near-ties favour fewer splits.
-FwdPlan plan_forward(int64_t M, int64_t H, int64_t V, int compute_entropy, int sms) {
+// Chooses the V-split: units are (256-row pair tile, run of tps 256-column
+// tiles); a static round-robin over the persistent CTA pairs finishes after
+// ceil(units / pairs) * tps tiles.  Each extra split adds M * 24 bytes of
+// partial traffic, charged in tile-times so that near-ties favour fewer splits.
+FwdPlan plan_forward(int64_t M, int64_t H, int64_t V, int compute_entropy, int pairs) {
     FwdPlan f{};
-    f.Mt = static_cast<int>(cdiv(M, BM));
+    pairs = std::max(1, pairs);
+    f.Mt = static_cast<int>(cdiv(M, PM));
     f.Vt = static_cast<int>(cdiv(V, BN));
-    const double tile_s = 2.0 * BM * BN * static_cast<double>(H) / 1.2e13;  // ~per-SM bf16 rate
+    const double tile_s = 2.0 * PM * BN * static_cast<double>(H) / 2.4e13;  // ~bf16 rate of a pair
     const double split_cost = (static_cast<double>(M) * 24.0 / 6.0e12) / tile_s;
     double best = 1e300;
     int best_tps = f.Vt;
@@ -153,7 +155,7 @@ FwdPlan plan_forward(int64_t M, int64_t H, int64_t V, int compute_entropy, int s
         const int S = static_cast<int>(cdiv(f.Vt, tps));
         if (tps > 1 && cdiv(f.Vt, tps - 1) == S) continue;  // same split count, shorter runs win
         const double units = static_cast<double>(f.Mt) * S;
-        const double waves = std::ceil(units / sms);
+        const double waves = std::ceil(units / pairs);
         const double cost = waves * tps + S * split_cost;
         if (cost < best - 1e-9) {
             best = cost;
@@ -162,12 +164,12 @@ FwdPlan plan_forward(int64_t M, int64_t H, int64_t V, int compute_entropy, int s
     }
     f.tps = best_tps;
     f.S = static_cast<int>(cdiv(f.Vt, f.tps));
-    // group of M-tiles whose X rows stay resident in L2 (about 40 MB of X)
-    const int64_t gm = std::max<int64_t>(8, 40ll * 1000 * 1000 / (BM * 2 * std::max<int64_t>(H, 1)));
+    // group of pair M-tiles whose X rows stay resident in L2 (about 40 MB of X)
+    const int64_t gm = std::max<int64_t>(4, 40ll * 1000 * 1000 / (PM * 2 * std::max<int64_t>(H, 1)));
     f.GM = static_cast<int>(std::min<int64_t>(f.Mt, gm));
     if (f.GM < 1) f.GM = 1;
     f.units = f.Mt * f.S;
-    f.grid = std::min(f.units, sms);
+    f.grid = 2 * std::min(f.units, pairs);
     const size_t part = align_up(static_cast<size_t>(f.S) * M * sizeof(float), 1024);
     f.off_m = kHeaderBytes;
     f.off_s = f.off_m + part;
@@ -196,27 +198,45 @@ BwdPlan plan_backward(int64_t M, int64_t V, int64_t chunk_rows) {
 
 bool smem_attrs_done(DevInfo* d) { return d->attrs_set; }
 
-template <int kMode, bool kEnt, bool kOutF32>
+template <int kMode, bool kEnt>
 cudaError_t set_smem_attr() {
-    return cudaFuncSetAttribute(flp_tile_kernel<kMode, kEnt, kOutF32>,
+    return cudaFuncSetAttribute(flp_tile_kernel<kMode, kEnt>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_ALLOC);
 }
 
 flp_status ensure_attrs(DevInfo* d) {
     if (smem_attrs_done(d)) return FLP_OK;
     cudaError_t e = cudaSuccess;
-    if (e == cudaSuccess) e = set_smem_attr<kFwd, true, false>();
-    if (e == cudaSuccess) e = set_smem_attr<kFwd, false, false>();
-    if (e == cudaSuccess) e = set_smem_attr<kDz, true, false>();
-    if (e == cudaSuccess) e = set_smem_attr<kDz, false, false>();
+    if (e == cudaSuccess) e = set_smem_attr<kFwd, true>();
+    if (e == cudaSuccess) e = set_smem_attr<kFwd, false>();
+    if (e == cudaSuccess) e = set_smem_attr<kDz, true>();
+    if (e == cudaSuccess) e = set_smem_attr<kDz, false>();
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(flp_bwd_gemm_kernel<false>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_ALLOC_BWD);
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_ALLOC);
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(flp_bwd_gemm_kernel<true>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_ALLOC_BWD);
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_ALLOC);
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
+    // How many clusters of two fit at once (SMs that a cluster cannot pair up
+    // stay idle); the persistent grids never exceed it.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(d->sm_count));
+    cfg.blockDim = dim3(NUM_THREADS);
+    cfg.dynamicSmemBytes = SMEM_ALLOC;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int clusters = 0;
+    e = cudaOccupancyMaxActiveClusters(&clusters, flp_tile_kernel<kFwd, true>, &cfg);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveClusters");
+    if (clusters < 1) return fail(FLP_ERR_UNSUPPORTED, "no CTA pair fits on the device");
     std::lock_guard<std::mutex> lk(g_mu);
+    d->pairs = std::min(clusters, std::max(1, d->sm_count / 2));
     d->attrs_set = true;
     return FLP_OK;
 }
@@ -229,13 +249,33 @@ flp_status check_device(DevInfo** d) {
     return ensure_attrs(*d);
 }
 
-template <int kMode, bool kEnt, bool kOutF32>
+// Launches `kernel` on `grid` CTAs grouped in clusters of two (the CTA pairs
+// that share each tcgen05.mma.cta_group::2 tile).
+template <typename... KArgs, typename... Args>
+flp_status launch_pairs(void (*kernel)(KArgs...), int grid, cudaStream_t s, const char* what,
+                        Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(NUM_THREADS);
+    cfg.dynamicSmemBytes = SMEM_ALLOC;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+    if (e == cudaSuccess) e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, what);
+    return FLP_OK;
+}
+
+template <int kMode, bool kEnt>
 flp_status launch_tile(int grid, const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& o,
                        const TileParams& p, cudaStream_t s) {
-    flp_tile_kernel<kMode, kEnt, kOutF32><<<grid, NUM_THREADS, SMEM_ALLOC, s>>>(a, b, o, p);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return cuda_fail(e, "flp_tile_kernel launch");
-    return FLP_OK;
+    return launch_pairs(flp_tile_kernel<kMode, kEnt>, grid, s, "flp_tile_kernel launch", a, b, o, p);
 }
 
 flp_status common_checks(const void* X, const void* W, const int64_t* targets, int64_t M,
@@ -283,9 +323,9 @@ flp_status flp_workspace_query(int64_t M, int64_t H, int64_t V, int compute_entr
                                int64_t chunk_rows, size_t* fwd_bytes, size_t* bwd_bytes) {
     if (M < 0 || H < 1 || V < 1) return fail(FLP_ERR_INVALID_ARG, "M >= 0, H >= 1 and V >= 1 required");
     DevInfo* d;
-    flp_status st = device_info(&d, nullptr);
+    flp_status st = check_device(&d);
     if (st != FLP_OK) return st;
-    if (fwd_bytes) *fwd_bytes = plan_forward(M, H, V, compute_entropy ? 1 : 0, d->sm_count).bytes;
+    if (fwd_bytes) *fwd_bytes = plan_forward(M, H, V, compute_entropy ? 1 : 0, d->pairs).bytes;
     if (bwd_bytes) *bwd_bytes = plan_backward(M, V, chunk_rows).bytes;
     return FLP_OK;
 }
@@ -305,7 +345,7 @@ flp_status flp_forward(const void* X, const void* W, const int64_t* targets, int
     DevInfo* d;
     st = check_device(&d);
     if (st != FLP_OK) return st;
-    const FwdPlan f = plan_forward(M, H, V, ent, d->sm_count);
+    const FwdPlan f = plan_forward(M, H, V, ent, d->pairs);
     if (!workspace || workspace_bytes < f.bytes || !aligned16(workspace))
         return fail(FLP_ERR_WORKSPACE, "forward workspace null, misaligned or too small");
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -317,7 +357,7 @@ flp_status flp_forward(const void* X, const void* W, const int64_t* targets, int
     CUtensorMap tmX, tmW;
     st = tmap_2d(&tmX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, X, H, M, H * 2, BK, BM);
     if (st != FLP_OK) return st;
-    st = tmap_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, W, H, V, H * 2, BK, BN);
+    st = tmap_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, W, H, V, H * 2, BK, BNH);
     if (st != FLP_OK) return st;
 
     TileParams p{};
@@ -334,7 +374,6 @@ flp_status flp_forward(const void* X, const void* W, const int64_t* targets, int
     p.ignore_index = ignore_index;
     p.scale = scale;
     p.scale2 = scale * LOG2E;
-    p.compute_entropy = ent;
     p.y = reinterpret_cast<const long long*>(targets);
     p.part_m = reinterpret_cast<float*>(ws + f.off_m);
     p.part_s = reinterpret_cast<float*>(ws + f.off_s);
@@ -344,8 +383,8 @@ flp_status flp_forward(const void* X, const void* W, const int64_t* targets, int
     p.wait_limit_ns = kWaitLimitNs;
     p.debug_stall_after = -1;
     mark(0, s);
-    st = ent ? launch_tile<kFwd, true, false>(f.grid, tmX, tmW, tmX, p, s)
-             : launch_tile<kFwd, false, false>(f.grid, tmX, tmW, tmX, p, s);
+    st = ent ? launch_tile<kFwd, true>(f.grid, tmX, tmW, tmX, p, s)
+             : launch_tile<kFwd, false>(f.grid, tmX, tmW, tmX, p, s);
     if (st != FLP_OK) return st;
     mark(1, s);
 
@@ -419,17 +458,17 @@ flp_status flp_backward(const void* X, const void* W, const int64_t* targets, in
     unsigned long long ticket_base = 0;
 
     CUtensorMap tmW_k, tmW_mn, tmDW;
-    st = tmap_2d(&tmW_k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, W, H, V, H * 2, BK, BN);
+    st = tmap_2d(&tmW_k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, W, H, V, H * 2, BK, BNH);
     if (st != FLP_OK) return st;
     st = tmap_2d(&tmW_mn, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, W, H, V, H * 2, 64, 64);
     if (st != FLP_OK) return st;
     st = tmap_2d(&tmDW, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, dW, H, V, H * 4, 32, BM);
     if (st != FLP_OK) return st;
 
-    const int sms = d->sm_count;
     const int Vt = static_cast<int>(Vp / BN);
     const int Nt_h = static_cast<int>(cdiv(H, BN));
-    const int64_t gm_rows = std::max<int64_t>(8, 40ll * 1000 * 1000 / (BM * 2 * H));
+    const int pairs = d->pairs;
+    const int64_t gm_rows = std::max<int64_t>(4, 40ll * 1000 * 1000 / (PM * 2 * H));
 
     for (int64_t r0 = 0; r0 < M; r0 += chunk) {
         const int64_t rows = std::min(chunk, M - r0);
@@ -449,7 +488,7 @@ flp_status flp_backward(const void* X, const void* W, const int64_t* targets, in
 
         // (1) recompute logits tiles -> bf16 dZ for this wave
         TileParams p{};
-        p.Mt = static_cast<int>(cdiv(rows, BM));
+        p.Mt = static_cast<int>(cdiv(rows, PM));
         p.Nt = Vt;
         p.S = Vt;
         p.tps = 1;
@@ -462,8 +501,7 @@ flp_status flp_backward(const void* X, const void* W, const int64_t* targets, in
         p.ignore_index = ignore_index;
         p.scale = scale;
         p.scale2 = scale * LOG2E;
-        p.compute_entropy = ent;
-        p.y = reinterpret_cast<const long long*>(targets);
+            p.y = reinterpret_cast<const long long*>(targets);
         p.lse = lse;
         p.ent = ent ? entropy : nullptr;
         p.g_lp = grad_logprob;
@@ -471,22 +509,22 @@ flp_status flp_backward(const void* X, const void* W, const int64_t* targets, in
         p.err = err;
         p.wait_limit_ns = kWaitLimitNs;
         p.debug_stall_after = -1;
-        const int grid_dz = std::min(p.units, sms);
+        const int grid_dz = 2 * std::min(p.units, pairs);
         const bool first = (r0 == 0);
         if (first) mark(4, s);
-        st = ent ? launch_tile<kDz, true, false>(grid_dz, tmXk, tmW_k, tmDZst, p, s)
-                 : launch_tile<kDz, false, false>(grid_dz, tmXk, tmW_k, tmDZst, p, s);
+        st = ent ? launch_tile<kDz, true>(grid_dz, tmXk, tmW_k, tmDZst, p, s)
+                 : launch_tile<kDz, false>(grid_dz, tmXk, tmW_k, tmDZst, p, s);
         if (st != FLP_OK) return st;
         if (first) mark(5, s);
 
         // (2) dX[wave] = dZ W (K = Vp) and dW (+)= dZ^T X[wave] (K = wave rows),
-        // one persistent launch; the ticket counter lives in the zeroed header
-        // and every launch consumes units + grid tickets.
+        // one persistent launch of CTA pairs; the ticket counter lives in the
+        // zeroed header and every launch consumes units + pairs tickets.
         BwdParams q{};
-        q.Mt_dx = static_cast<int>(cdiv(rows, BM));
+        q.Mt_dx = static_cast<int>(cdiv(rows, PM));
         q.Nt = Nt_h;
         q.units_dx = q.Mt_dx * Nt_h;
-        q.units_dw = Vt * (BN / BM) * Nt_h;
+        q.units_dw = Vt * Nt_h;
         q.KB_dx = static_cast<int>(Vp / BK);
         q.KB_dw = static_cast<int>(cdiv(rows, BK));
         q.dw_add = (accumulate_dW || r0 > 0) ? 1 : 0;
@@ -495,17 +533,15 @@ flp_status flp_backward(const void* X, const void* W, const int64_t* targets, in
         q.err = err;
         q.wait_limit_ns = kWaitLimitNs;
         const int total = q.units_dx + q.units_dw;
-        const int grid_bw = std::min(total, sms);
-        ticket_base += static_cast<unsigned long long>(total) + grid_bw;
+        const int pairs_bw = std::min(total, pairs);
+        ticket_base += static_cast<unsigned long long>(total) + pairs_bw;
         if (first) mark(6, s);
-        if (dX_dtype == FLP_F32)
-            flp_bwd_gemm_kernel<true><<<grid_bw, NUM_THREADS, SMEM_ALLOC_BWD, s>>>(
-                tmDZk, tmW_mn, tmDZmn, tmXmn, tmDX, tmDW, q);
-        else
-            flp_bwd_gemm_kernel<false><<<grid_bw, NUM_THREADS, SMEM_ALLOC_BWD, s>>>(
-                tmDZk, tmW_mn, tmDZmn, tmXmn, tmDX, tmDW, q);
-        cudaError_t e = cudaGetLastError();
-        if (e != cudaSuccess) return cuda_fail(e, "flp_bwd_gemm_kernel launch");
+        st = (dX_dtype == FLP_F32)
+                 ? launch_pairs(flp_bwd_gemm_kernel<true>, 2 * pairs_bw, s, "flp_bwd_gemm_kernel launch",
+                                tmDZk, tmW_mn, tmDZmn, tmXmn, tmDX, tmDW, q)
+                 : launch_pairs(flp_bwd_gemm_kernel<false>, 2 * pairs_bw, s, "flp_bwd_gemm_kernel launch",
+                                tmDZk, tmW_mn, tmDZmn, tmXmn, tmDX, tmDW, q);
+        if (st != FLP_OK) return st;
         if (first) mark(7, s);
     }
     return FLP_OK;
@@ -571,7 +607,7 @@ extern "C" flp_status flp_forward_noalloc(const void* X, const void* W, const in
     if (st != FLP_OK) return st;
     st = check_device(&d);
     if (st != FLP_OK) return st;
-    const FwdPlan f = plan_forward(M, H, V, ent, d->sm_count);
+    const FwdPlan f = plan_forward(M, H, V, ent, d->pairs);
     if (f.bytes > FLP_STATIC_SCRATCH_BYTES) {
         char buf[200];
         snprintf(buf, sizeof buf,
@@ -590,7 +626,7 @@ extern "C" flp_status flp_forward_noalloc(const void* X, const void* W, const in
     CUtensorMap tmX, tmW;
     st = tmap_2d(&tmX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, X, H, M, H * 2, BK, BM);
     if (st != FLP_OK) return st;
-    st = tmap_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, W, H, V, H * 2, BK, BN);
+    st = tmap_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, W, H, V, H * 2, BK, BNH);
     if (st != FLP_OK) return st;
 
     TileParams p{};
@@ -607,7 +643,6 @@ extern "C" flp_status flp_forward_noalloc(const void* X, const void* W, const in
     p.ignore_index = ignore_index;
     p.scale = scale;
     p.scale2 = scale * LOG2E;
-    p.compute_entropy = ent;
     p.y = reinterpret_cast<const long long*>(targets);
     p.part_m = reinterpret_cast<float*>(ws + f.off_m);
     p.part_s = reinterpret_cast<float*>(ws + f.off_s);
@@ -616,8 +651,8 @@ extern "C" flp_status flp_forward_noalloc(const void* X, const void* W, const in
     p.err = err;
     p.wait_limit_ns = kWaitLimitNs;
     p.debug_stall_after = -1;
-    st = ent ? launch_tile<kFwd, true, false>(f.grid, tmX, tmW, tmX, p, s)
-             : launch_tile<kFwd, false, false>(f.grid, tmX, tmW, tmX, p, s);
+    st = ent ? launch_tile<kFwd, true>(f.grid, tmX, tmW, tmX, p, s)
+             : launch_tile<kFwd, false>(f.grid, tmX, tmW, tmX, p, s);
     if (st != FLP_OK) return st;
 
     MergeParams mp{};

@@ -1,29 +1,34 @@
 // kernels.cuh - sm_103a kernels of the fused linear log-prob / cross-entropy head.
 //
-// One warp-specialised, persistent tile kernel serves the four contractions of
-// the path; a mode template parameter selects the operand layouts and the
-// epilogue:
+// Every contraction of the path runs on CTA pairs (clusters of two CTAs on two
+// SMs) that share one 256 x 256 output tile: tcgen05.mma.cta_group::2 with
+// M = 256 (128 rows of A in each CTA) and N = 256 (B split along N, 128 rows
+// in each CTA), fp32 accumulators in both CTAs' TMEM.  Each SM therefore loads
+// 16 KiB of A and 16 KiB of B per 64-deep K step for 2 * 128 * 256 * 64 MACs.
 //
-//   kFwd : z = s X W^T tiles -> online max / sum-exp / (entropy) / target
-//          pick per row, raw per-split partials (forward, fused epilogue)
-//   kDz  : z tiles recomputed -> dZ = s[g_lp(onehot - p) + g_ent p(sum pz - z)]
-//          rounded to bf16, TMA-stored into the wave's dZ buffer
-//   kDx  : dX[wave] = dZ W          (A = dZ K-major, B = W MN-major)
-//   kDw  : dW (+)= dZ^T X[wave]     (A = dZ MN-major, B = X MN-major)
+//   flp_tile_kernel<kFwd> : z = s X W^T tiles -> online max / sum-exp /
+//                           (entropy) / target pick per row -> raw per-split
+//                           partials (forward, fused epilogue)
+//   flp_tile_kernel<kDz>  : z tiles recomputed -> dZ = s[g_lp(onehot - p) +
+//                           g_ent p(sum pz - z)] in bf16, TMA-stored to the
+//                           wave's dZ buffer
+//   flp_bwd_gemm_kernel   : dX[wave] = dZ W and dW (+)= dZ^T X[wave] in one
+//                           persistent launch with a ticket-counter scheduler
 //
-// Roles (192 threads, one CTA per SM):
-//   warp 0      TMA producer (one elected lane)
-//   warp 1      TMEM allocator and tcgen05.mma issuer (one elected lane)
-//   warps 2..5  epilogue: thread == accumulator row (TMEM lane), 4 x 32 lanes
-// Accumulators: two 128 x 256 fp32 buffers in TMEM (512 columns), so the
-// epilogue of one tile overlaps the MMAs of the next.
-// Operand tiles: 128 rows (A) and 256 rows (B) by 64 bf16 (one 128-byte
-// swizzle atom) per pipeline stage, moved by TMA into 1024-byte aligned shared
-// memory in the canonical 128B-swizzled layouts that the smem descriptors name.
+// Roles (192 threads per CTA, one CTA per SM):
+//   warp 0      TMA producer (one lane) for this CTA's halves of A and B
+//   warp 1      TMEM allocation (both CTAs) and, in the leader CTA (cluster
+//               rank 0), the single thread that issues the pair MMAs
+//   warps 2..5  epilogue: thread == accumulator row (TMEM lane) of this CTA
+// Barriers: both CTAs' TMA loads complete on the leader's `full` barrier; the
+// leader's MMA commits are multicast to both CTAs' `empty` (stage free) and
+// `tfull` (accumulator ready) barriers; both CTAs' epilogues release an
+// accumulator on the leader's `tempty` barrier.  Two 256-column accumulators
+// (512 TMEM columns) let a tile's epilogue overlap the next tile's MMAs.
 //
 // Every mbarrier wait is bounded (globaltimer); on expiry the kernel raises the
-// timeout bit in the error word, stops issuing work, waits (bounded) for its own
-// copies and MMAs in flight, frees its TMEM and returns.
+// timeout bit in the error word, stops issuing work, lets its copies and MMAs
+// in flight finish (a bounded wait), frees its TMEM and returns.
 #pragma once
 #include <cstdint>
 #include <cuda.h>
@@ -31,20 +36,24 @@
 
 namespace flp {
 
-constexpr int BM = 128;           // rows per tile (UMMA M)
-constexpr int BN = 256;           // columns per tile (UMMA N)
-constexpr int BK = 64;            // K per pipeline stage
+constexpr int BM = 128;           // rows of A per CTA (TMEM lanes)
+constexpr int PM = 256;           // rows of the pair tile (UMMA M)
+constexpr int BN = 256;           // columns of the pair tile (UMMA N)
+constexpr int BNH = BN / 2;       // rows of B held by each CTA of the pair
+constexpr int BK = 64;            // K per pipeline stage (one 128-byte swizzle atom)
 constexpr int UMMA_K = 16;        // K per tcgen05.mma (bf16)
-constexpr int STAGES = 4;
+constexpr int STAGES = 6;
 constexpr int NUM_THREADS = 192;
 constexpr int EPI_THREADS = 128;
 constexpr uint32_t TMEM_COLS = 512;
+constexpr uint16_t PAIR_MASK = 0x3;
 
 constexpr uint32_t A_STAGE_BYTES = BM * BK * 2;    // 16 KiB
-constexpr uint32_t B_STAGE_BYTES = BN * BK * 2;    // 32 KiB
-constexpr uint32_t STAGE_TX = A_STAGE_BYTES + B_STAGE_BYTES;
+constexpr uint32_t B_STAGE_BYTES = BNH * BK * 2;   // 16 KiB
+constexpr uint32_t PAIR_STAGE_TX = 2 * (A_STAGE_BYTES + B_STAGE_BYTES);  // lands on the leader's barrier
 constexpr uint32_t STG_BYTES = 128 * 128;          // one 128-row x 128-byte store box
 constexpr uint32_t NUM_STG = 2;
+constexpr int SCHED_SLOTS = 4;
 
 constexpr int ERR_BAD_TARGET = 1;
 constexpr int ERR_TIMEOUT = 2;
@@ -52,89 +61,97 @@ constexpr int ERR_TIMEOUT = 2;
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr float LN2 = 0.6931471805599453f;
 
-enum Mode : int { kFwd = 0, kDz = 1, kDx = 2, kDw = 3 };
+enum Mode : int { kFwd = 0, kDz = 1 };
 
-// Offsets inside the (1024-byte aligned) dynamic shared memory block.
+// Offsets inside the (1024-byte aligned) dynamic shared memory block; the
+// layout is identical in both CTAs of a pair, which the pair MMA relies on.
 constexpr uint32_t SMEM_A = 0;
 constexpr uint32_t SMEM_B = SMEM_A + STAGES * A_STAGE_BYTES;
 constexpr uint32_t SMEM_STG = SMEM_B + STAGES * B_STAGE_BYTES;
 constexpr uint32_t SMEM_BAR = SMEM_STG + NUM_STG * STG_BYTES;
-constexpr uint32_t NUM_BARS = 2 * STAGES + 4 + 1;
-constexpr uint32_t SMEM_MISC = SMEM_BAR + NUM_BARS * 8;
-constexpr uint32_t SMEM_TOTAL = SMEM_MISC + 16;
+// full[STAGES], empty[STAGES], tfull[2], tempty[2], drain, sched_full[4], sched_empty[4]
+constexpr uint32_t NUM_BARS = 2 * STAGES + 4 + 1 + 2 * SCHED_SLOTS;
+constexpr uint32_t SMEM_MISC = SMEM_BAR + NUM_BARS * 8;  // tmem slot, abort flag, sched slots
+constexpr uint32_t SMEM_TOTAL = SMEM_MISC + 8 + 4 * SCHED_SLOTS;
 constexpr uint32_t SMEM_ALLOC = SMEM_TOTAL + 1024;  // slack for 1024-byte alignment
 
-struct TileParams {
-    // schedule: units are runs [n0, n1) of N-tiles that share one M-tile
-    int units, Mt, Nt, S, tps, GM;
-    int KB;  // K blocks of 64
-    // problem
-    int M;     // valid rows of this launch (all rows for kFwd, the wave's rows otherwise)
-    int V;     // vocabulary size (kFwd / kDz column mask)
-    int row0;  // first global row of the wave (kDz)
-    long long ignore_index;
-    float scale;   // s
-    float scale2;  // s * log2(e)
-    int compute_entropy;
-    int dw_add;  // kDw: 0 = TMA store, 1 = TMA reduce-add into dW
-    const long long* y;
-    const float* lse;
-    const float* ent;
-    const float* g_lp;
-    const float* g_ent;
-    float* part_m;
-    float* part_s;
-    float* part_t;
-    float* zy;
-    int* err;
-    unsigned long long wait_limit_ns;
-    int debug_stall_after;  // < 0: off; else the producer stops after this many stages
+struct Smem {
+    uint8_t* base;
+    uint64_t* full;
+    uint64_t* empty;
+    uint64_t* tfull;
+    uint64_t* tempty;
+    uint64_t* drain;
+    uint64_t* sched_full;
+    uint64_t* sched_empty;
+    uint32_t* tmem_slot;
+    volatile int* abort_flag;
+    volatile int* sched_val;
 };
 
-struct Unit {
-    int mt, n0, n1, split;
-};
-
-__device__ __forceinline__ Unit decode_unit(const TileParams& p, int u) {
-    const int per_group = p.GM * p.S;
-    const int g = u / per_group;
-    const int first_m = g * p.GM;
-    const int gm = min(p.GM, p.Mt - first_m);
-    const int r = u - g * per_group;
-    Unit t;
-    t.split = r / gm;
-    t.mt = first_m + (r - t.split * gm);
-    t.n0 = t.split * p.tps;
-    t.n1 = min(p.Nt, t.n0 + p.tps);
-    return t;
+__device__ __forceinline__ Smem smem_layout(uint8_t* raw) {
+    Smem s;
+    s.base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) &
+                                        ~static_cast<uintptr_t>(1023));
+    uint64_t* bars = reinterpret_cast<uint64_t*>(s.base + SMEM_BAR);
+    s.full = bars;
+    s.empty = bars + STAGES;
+    s.tfull = bars + 2 * STAGES;
+    s.tempty = bars + 2 * STAGES + 2;
+    s.drain = bars + 2 * STAGES + 4;
+    s.sched_full = bars + 2 * STAGES + 5;
+    s.sched_empty = s.sched_full + SCHED_SLOTS;
+    s.tmem_slot = reinterpret_cast<uint32_t*>(s.base + SMEM_MISC);
+    s.abort_flag = reinterpret_cast<volatile int*>(s.base + SMEM_MISC + 4);
+    s.sched_val = reinterpret_cast<volatile int*>(s.base + SMEM_MISC + 8);
+    return s;
 }
 
-template <int kMode>
-struct ModeCfg {
-    static constexpr int a_mn = (kMode == kDw) ? 1 : 0;
-    static constexpr int b_mn = (kMode == kDx || kMode == kDw) ? 1 : 0;
-    static constexpr uint32_t idesc = idesc_bf16_f32(BM, BN, a_mn, b_mn);
-};
-
-// ----------------------------------------------------------------- producer
-
-template <int kMode>
-__device__ __forceinline__ void issue_stage_loads(const CUtensorMap* tmA, const CUtensorMap* tmB,
-                                                  uint8_t* a_dst, uint8_t* b_dst, uint64_t* bar,
-                                                  int mt, int nt, int kb) {
-    if constexpr (ModeCfg<kMode>::a_mn == 0) {
-        tma_load_2d(a_dst, tmA, kb * BK, mt * BM, bar);  // box: 64 k x 128 rows
-    } else {
-#pragma unroll
-        for (int j = 0; j < BM / 64; ++j)  // box: 64 m x 64 k rows, one per 64-wide MN atom
-            tma_load_2d(a_dst + j * 8192, tmA, mt * BM + j * 64, kb * BK, bar);
+// Barrier set-up, TMEM allocation on both CTAs, and the cluster handshake that
+// makes the peer's barriers visible before any remote arrive or TMA signal.
+__device__ __forceinline__ uint32_t pair_prologue(const Smem& sm, int warp) {
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&sm.full[s], 1);
+            mbar_init(&sm.empty[s], 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(&sm.tfull[a], 1);
+            mbar_init(&sm.tempty[a], 2 * EPI_THREADS);
+        }
+        mbar_init(sm.drain, 1);
+        for (int s = 0; s < SCHED_SLOTS; ++s) {
+            mbar_init(&sm.sched_full[s], 1);
+            mbar_init(&sm.sched_empty[s], 2 + 2 * EPI_THREADS);
+        }
+        *sm.abort_flag = 0;
+        fence_mbarrier_init();
     }
-    if constexpr (ModeCfg<kMode>::b_mn == 0) {
-        tma_load_2d(b_dst, tmB, kb * BK, nt * BN, bar);  // box: 64 k x 256 rows
-    } else {
-#pragma unroll
-        for (int j = 0; j < BN / 64; ++j)
-            tma_load_2d(b_dst + j * 8192, tmB, nt * BN + j * 64, kb * BK, bar);
+    if (warp == 1) {
+        tmem_alloc_pair(sm.tmem_slot, TMEM_COLS);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before();
+    cluster_sync();
+    tc_fence_after();
+    return *sm.tmem_slot;
+}
+
+// Teardown: on an abort give copies in flight a bounded grace period, then a
+// cluster handshake (no CTA leaves while its peer may still touch its shared
+// memory or TMEM) and the pair TMEM release.
+__device__ __forceinline__ void pair_epilogue(const Smem& sm, int warp, uint32_t tmem_base) {
+    if (*sm.abort_flag) {
+        const uint64_t t0 = globaltimer_ns();
+        while (globaltimer_ns() - t0 < 2000000ull) {
+        }
+    }
+    tc_fence_before();
+    __syncwarp();
+    cluster_sync();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc_pair(tmem_base, TMEM_COLS);
     }
 }
 
@@ -142,9 +159,9 @@ __device__ __forceinline__ void issue_stage_loads(const CUtensorMap* tmA, const 
 template <int kMN>
 __device__ __forceinline__ uint64_t operand_desc(uint32_t base, int k) {
     if constexpr (kMN == 0)
-        return sdesc_sw128(base + k * (UMMA_K * 2), 16, 1024);  // K-major: advance 32 B in the atom
+        return sdesc_sw128(base + k * (UMMA_K * 2), 16, 1024);  // K-major: 32 B inside the atom
     else
-        return sdesc_sw128(base + k * (UMMA_K * 128), 8192, 1024);  // MN-major: advance 16 rows
+        return sdesc_sw128(base + k * (UMMA_K * 128), 8192, 1024);  // MN-major: 16 rows of 128 B
 }
 
 // ------------------------------------------------------------ epilogue pieces
@@ -173,8 +190,8 @@ __device__ __forceinline__ void stage_row(uint32_t box_base, int r, const uint32
                      w[4 * c + 3]);
 }
 
-// Bookkeeping of the two store boxes: before reusing a box wait until the
-// bulk store that last read it has finished reading.
+// Two store boxes used in turn: before a box is rewritten, the bulk store
+// that last read it must have finished reading.
 struct StoreRing {
     uint32_t n = 0;
 };
@@ -188,10 +205,8 @@ __device__ __forceinline__ uint32_t store_box_acquire(StoreRing& ring, uint8_t* 
     return smem_addr(smem + SMEM_STG + buf * STG_BYTES);
 }
 
-template <int kMode>
 __device__ __forceinline__ void store_box_release(StoreRing& ring, uint8_t* smem, int et,
-                                                  const CUtensorMap* tmOut, int x, int y,
-                                                  bool add) {
+                                                  const CUtensorMap* tmOut, int x, int y, bool add) {
     const uint32_t buf = ring.n & 1u;
     fence_proxy_async_smem();
     named_bar_sync(1, EPI_THREADS);
@@ -206,81 +221,114 @@ __device__ __forceinline__ void store_box_release(StoreRing& ring, uint8_t* smem
     ring.n++;
 }
 
-// ------------------------------------------------------------------- kernel
+// fp32 accumulator columns [c0, c0 + 64) of this thread's row -> 32 packed bf16 pairs.
+__device__ __forceinline__ void tmem_row64_to_bf16(uint32_t taddr, uint32_t (&w)[32]) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(taddr + h * 32, v);
+        tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+            w[h * 16 + j] = pack_bf16x2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
+    }
+}
 
-template <int kMode, bool kEnt, bool kOutF32>
+// ------------------------------------------------------- forward / dZ kernel
+
+struct TileParams {
+    // schedule: units are runs [n0, n1) of 256-column tiles sharing one 256-row pair tile
+    int units, Mt, Nt, S, tps, GM;
+    int KB;    // K blocks of 64 (H / 64, rounded up)
+    int M;     // rows of this launch (all rows for kFwd, the wave's rows for kDz)
+    int V;     // vocabulary size (column mask)
+    int row0;  // first global row of the wave (kDz)
+    long long ignore_index;
+    float scale;   // s
+    float scale2;  // s * log2(e)
+    const long long* y;
+    const float* lse;
+    const float* ent;
+    const float* g_lp;
+    const float* g_ent;
+    float* part_m;
+    float* part_s;
+    float* part_t;
+    float* zy;
+    int* err;
+    unsigned long long wait_limit_ns;
+    int debug_stall_after;  // < 0: off; else the producers stop after this many stages
+};
+
+struct Unit {
+    int mt, n0, n1, split;
+};
+
+// Units are ordered in groups of GM pair M-tiles; inside a group the split index
+// is outermost, so the pairs running at the same time share W tiles while the
+// group's X rows stay resident in L2.
+__device__ __forceinline__ Unit decode_unit(const TileParams& p, int u) {
+    const int per_group = p.GM * p.S;
+    const int g = u / per_group;
+    const int first_m = g * p.GM;
+    const int gm = min(p.GM, p.Mt - first_m);
+    const int r = u - g * per_group;
+    Unit t;
+    t.split = r / gm;
+    t.mt = first_m + (r - t.split * gm);
+    t.n0 = t.split * p.tps;
+    t.n1 = min(p.Nt, t.n0 + p.tps);
+    return t;
+}
+
+template <int kMode, bool kEnt>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     flp_tile_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmOut, const TileParams p) {
     extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + SMEM_BAR);
-    uint64_t* full = bars;
-    uint64_t* empty = bars + STAGES;
-    uint64_t* tfull = bars + 2 * STAGES;
-    uint64_t* tempty = bars + 2 * STAGES + 2;
-    uint64_t* drain = bars + 2 * STAGES + 4;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + SMEM_MISC);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + SMEM_MISC + 4);
-
+    const Smem sm = smem_layout(smem_raw);
+    uint8_t* smem = sm.base;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
+    const bool leader = (rank == 0);
+    const int pair = blockIdx.x >> 1;
+    const int npairs = gridDim.x >> 1;
 
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < STAGES; ++s) {
-            mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 1);
-        }
-        for (int a = 0; a < 2; ++a) {
-            mbar_init(&tfull[a], 1);
-            mbar_init(&tempty[a], EPI_THREADS);
-        }
-        mbar_init(drain, 1);
-        *abort_flag = 0;
-        fence_mbarrier_init();
-    }
     if (warp == 0 && lane == 0) {
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
-        if constexpr (kMode != kFwd) tma_prefetch_desc(&tmOut);
+        if constexpr (kMode == kDz) tma_prefetch_desc(&tmOut);
     }
-    if (warp == 1) {
-        tmem_alloc(tmem_slot, TMEM_COLS);
-        tmem_relinquish();
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem_base = *tmem_slot;
+    const uint32_t tmem_base = pair_prologue(sm, warp);
     const uint64_t limit = p.wait_limit_ns;
+    volatile int* abort_flag = sm.abort_flag;
 
     if (warp == 0) {
         // ------------------------------------------------------ TMA producer
         if (lane == 0) {
             int stage = 0;
             uint32_t phase = 0;
-            uint32_t issued_mask = 0, issued_parity = 0;
             long long issued = 0;
             bool ok = true;
-            for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
+            for (int u = pair; u < p.units && ok; u += npairs) {
                 const Unit t = decode_unit(p, u);
                 for (int nt = t.n0; nt < t.n1 && ok; ++nt) {
                     for (int kb = 0; kb < p.KB; ++kb) {
                         if (p.debug_stall_after >= 0 && issued >= p.debug_stall_after) {
-                            ok = false;  // injected stall: stop feeding the MMA warp
+                            ok = false;  // injected stall: stop feeding the MMA
                             break;
                         }
-                        if (!mbar_wait(&empty[stage], phase ^ 1u, limit, abort_flag)) {
+                        if (!mbar_wait(&sm.empty[stage], phase ^ 1u, limit, abort_flag)) {
                             ok = false;
                             break;
                         }
-                        mbar_arrive_expect_tx(&full[stage], STAGE_TX);
-                        issue_stage_loads<kMode>(&tmA, &tmB, smem + SMEM_A + stage * A_STAGE_BYTES,
-                                                 smem + SMEM_B + stage * B_STAGE_BYTES,
-                                                 &full[stage], t.mt, nt, kb);
-                        issued_mask |= 1u << stage;
-                        issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+                        if (leader) mbar_arrive_expect_tx(&sm.full[stage], PAIR_STAGE_TX);
+                        const uint32_t bar = mapa_shared(smem_addr(&sm.full[stage]), 0);
+                        tma_load_2d_pair(smem + SMEM_A + stage * A_STAGE_BYTES, &tmA, kb * BK,
+                                         t.mt * PM + static_cast<int>(rank) * BM, bar);
+                        tma_load_2d_pair(smem + SMEM_B + stage * B_STAGE_BYTES, &tmB, kb * BK,
+                                         nt * BN + static_cast<int>(rank) * BNH, bar);
                         ++issued;
                         if (++stage == STAGES) {
                             stage = 0;
@@ -293,34 +341,27 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 atomicOr(p.err, ERR_TIMEOUT);
                 *abort_flag = 1;
             }
-            // Wait (bounded) for every load this thread issued to land before
-            // the CTA can exit and its shared memory be reused.
-            for (int s = 0; s < STAGES; ++s)
-                if (issued_mask & (1u << s)) {
-                    volatile int no_abort = 0;
-                    mbar_wait(&full[s], (issued_parity >> s) & 1u, limit, &no_abort);
-                }
         }
     } else if (warp == 1) {
-        // ------------------------------------------------------- MMA issuer
-        if (lane == 0) {
+        // ---------------------------------------------- MMA issuer (leader)
+        if (lane == 0 && leader) {
             int stage = 0;
             uint32_t phase = 0;
             int acc = 0;
             uint32_t acc_phase = 0;
             bool ok = true;
-            constexpr uint32_t idesc = ModeCfg<kMode>::idesc;
-            for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
+            constexpr uint32_t idesc = idesc_bf16_f32(PM, BN, 0, 0);
+            for (int u = pair; u < p.units && ok; u += npairs) {
                 const Unit t = decode_unit(p, u);
                 for (int nt = t.n0; nt < t.n1 && ok; ++nt) {
-                    if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, limit, abort_flag)) {
+                    if (!mbar_wait(&sm.tempty[acc], acc_phase ^ 1u, limit, abort_flag)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
                     const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
                     for (int kb = 0; kb < p.KB; ++kb) {
-                        if (!mbar_wait(&full[stage], phase, limit, abort_flag)) {
+                        if (!mbar_wait(&sm.full[stage], phase, limit, abort_flag)) {
                             ok = false;
                             break;
                         }
@@ -328,19 +369,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         const uint32_t a_base = smem_addr(smem + SMEM_A + stage * A_STAGE_BYTES);
                         const uint32_t b_base = smem_addr(smem + SMEM_B + stage * B_STAGE_BYTES);
 #pragma unroll
-                        for (int k = 0; k < BK / UMMA_K; ++k) {
-                            umma_bf16(d_tmem, operand_desc<ModeCfg<kMode>::a_mn>(a_base, k),
-                                      operand_desc<ModeCfg<kMode>::b_mn>(b_base, k), idesc,
-                                      (kb > 0 || k > 0) ? 1u : 0u);
-                        }
-                        umma_commit(&empty[stage]);  // frees the smem stage once read
+                        for (int k = 0; k < BK / UMMA_K; ++k)
+                            umma_bf16_pair(d_tmem, operand_desc<0>(a_base, k),
+                                           operand_desc<0>(b_base, k), idesc,
+                                           (kb > 0 || k > 0) ? 1u : 0u);
+                        umma_commit_pair_mc(&sm.empty[stage], PAIR_MASK);  // stage free in both CTAs
                         if (++stage == STAGES) {
                             stage = 0;
                             phase ^= 1u;
                         }
                     }
                     if (!ok) break;
-                    umma_commit(&tfull[acc]);  // accumulator ready for the epilogue
+                    umma_commit_pair_mc(&sm.tfull[acc], PAIR_MASK);  // accumulator ready in both CTAs
                     acc ^= 1;
                     if (acc == 0) acc_phase ^= 1u;
                 }
@@ -349,35 +389,35 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 atomicOr(p.err, ERR_TIMEOUT);
                 *abort_flag = 1;
             }
-            // Every MMA this thread issued completes before TMEM is freed.
-            umma_commit(drain);
+            umma_commit_pair_mc(sm.drain, 0x1);  // every MMA issued so far has completed
             volatile int no_abort = 0;
-            mbar_wait(drain, 0, limit, &no_abort);
+            mbar_wait(sm.drain, 0, limit, &no_abort);
         }
     } else {
         // --------------------------------------------------------- epilogue
-        const int et = threadIdx.x - 64;         // 0..127
-        const int q = warp & 3;                  // TMEM lane quadrant of this warp
-        const int r = q * 32 + lane;             // accumulator row == TMEM lane
+        const int et = threadIdx.x - 64;  // 0..127
+        const int q = warp & 3;           // TMEM lane quadrant of this warp
+        const int r = q * 32 + lane;      // accumulator row == TMEM lane
         const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
+        const uint32_t tempty_leader0 = mapa_shared(smem_addr(&sm.tempty[0]), 0);
+        const uint32_t tempty_leader1 = mapa_shared(smem_addr(&sm.tempty[1]), 0);
         int acc = 0;
         uint32_t acc_phase = 0;
         bool ok = true;
         StoreRing ring;
 
-        for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
+        for (int u = pair; u < p.units && ok; u += npairs) {
             const Unit t = decode_unit(p, u);
-            const int row = t.mt * BM + r;  // row inside this launch
+            const int row = t.mt * PM + static_cast<int>(rank) * BM + r;  // row inside this launch
             const bool row_ok = row < p.M;
 
-            // ---- per-unit row state
             long long yv = -1;
             float run_m = -INFINITY, run_s = 0.f, run_t = 0.f, zyv = 0.f;
             bool found = false;
             float lse2 = INFINITY, K1 = 0.f, K2 = 0.f, Bc = 0.f;
             if constexpr (kMode == kFwd) {
                 if (row_ok) yv = p.y[row];
-            } else if constexpr (kMode == kDz) {
+            } else {
                 if (row_ok) {
                     const int grow = p.row0 + row;
                     yv = p.y[grow];
@@ -399,15 +439,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
 
             for (int nt = t.n0; nt < t.n1; ++nt) {
-                if (!mbar_wait(&tfull[acc], acc_phase, limit, abort_flag)) {
+                if (!mbar_wait(&sm.tfull[acc], acc_phase, limit, abort_flag)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
                 const uint32_t tbase = tmem_base + static_cast<uint32_t>(acc * BN) + lane_off;
+                const int col0 = nt * BN;
 
                 if constexpr (kMode == kFwd) {
-                    const int col0 = nt * BN;
                     const int nvalid = min(BN, p.V - col0);
                     const long long tcol = yv - col0;
 #pragma unroll 1
@@ -417,7 +457,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         tmem_wait_ld();
                         if (c == BN / 32 - 1) {
                             tc_fence_before();
-                            mbar_arrive(&tempty[acc]);
+                            mbar_arrive_cluster(acc ? tempty_leader1 : tempty_leader0);
                         }
                         const long long tc = tcol - c * 32;
                         if (tc >= 0 && tc < 32) {
@@ -477,9 +517,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         run_s += s0 + s1;
                         if constexpr (kEnt) run_t += t0 + t1;
                     }
-                } else if constexpr (kMode == kDz) {
-                    // 4 store boxes of 64 bf16 columns each
-                    const int col0 = nt * BN;
+                } else {
+                    // dZ: 4 store boxes of 64 bf16 columns each
 #pragma unroll 1
                     for (int b = 0; b < BN / 64; ++b) {
                         const uint32_t box = store_box_acquire(ring, smem, et);
@@ -491,7 +530,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                             tmem_wait_ld();
                             if (b == BN / 64 - 1 && h == 1) {
                                 tc_fence_before();
-                                mbar_arrive(&tempty[acc]);
+                                mbar_arrive_cluster(acc ? tempty_leader1 : tempty_leader0);
                             }
                             const int cbase = col0 + b * 64 + h * 32;
                             float dz[32];
@@ -517,43 +556,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                             for (int j = 0; j < 16; ++j) w[h * 16 + j] = pack_bf16x2(dz[2 * j], dz[2 * j + 1]);
                         }
                         stage_row(box, r, w);
-                        store_box_release<kMode>(ring, smem, et, &tmOut, col0 + b * 64, t.mt * BM,
-                                                 false);
-                    }
-                } else {
-                    // kDx / kDw: plain conversion of the fp32 accumulator
-                    const int col0 = nt * BN;
-                    constexpr int BOX_COLS = kOutF32 ? 32 : 64;
-#pragma unroll 1
-                    for (int b = 0; b < BN / BOX_COLS; ++b) {
-                        const uint32_t box = store_box_acquire(ring, smem, et);
-                        uint32_t w[32];
-                        if constexpr (kOutF32) {
-                            tmem_ld_32x32b_x32(tbase + b * 32, w);
-                            tmem_wait_ld();
-                            if (b == BN / BOX_COLS - 1) {
-                                tc_fence_before();
-                                mbar_arrive(&tempty[acc]);
-                            }
-                        } else {
-#pragma unroll
-                            for (int h = 0; h < 2; ++h) {
-                                uint32_t v[32];
-                                tmem_ld_32x32b_x32(tbase + b * 64 + h * 32, v);
-                                tmem_wait_ld();
-                                if (b == BN / BOX_COLS - 1 && h == 1) {
-                                    tc_fence_before();
-                                    mbar_arrive(&tempty[acc]);
-                                }
-#pragma unroll
-                                for (int j = 0; j < 16; ++j)
-                                    w[h * 16 + j] = pack_bf16x2(__uint_as_float(v[2 * j]),
-                                                                __uint_as_float(v[2 * j + 1]));
-                            }
-                        }
-                        stage_row(box, r, w);
-                        store_box_release<kMode>(ring, smem, et, &tmOut, col0 + b * BOX_COLS,
-                                                 t.mt * BM, kMode == kDw && p.dw_add);
+                        store_box_release(ring, smem, et, &tmOut, col0 + b * 64,
+                                          t.mt * PM + static_cast<int>(rank) * BM, false);
                     }
                 }
                 acc ^= 1;
@@ -575,44 +579,35 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             atomicOr(p.err, ERR_TIMEOUT);
             *abort_flag = 1;
         }
-        if constexpr (kMode != kFwd) {
+        if constexpr (kMode == kDz) {
             if (et == 0) bulk_wait_group<0>();
         }
     }
 
-    tc_fence_before();
-    __syncthreads();
-    if (warp == 1) {
-        __syncwarp();
-        tc_fence_after();
-        tmem_dealloc(tmem_base, TMEM_COLS);
-    }
+    pair_epilogue(sm, warp, tmem_base);
 }
 
 // ----------------------------------------------- fused backward contractions
 //
-// dX and dW of one wave in a single persistent launch.  Units [0, units_dx)
-// are dX tiles (128 wave rows x 256 hidden columns, K = padded vocabulary,
-// M-tiles fastest), units [units_dx, units_dx + units_dw) are dW tiles (128
-// vocabulary rows x 256 hidden columns, K = wave rows, hidden tiles fastest).
-// CTAs take units in that order from a global ticket counter, so the long dX
-// tiles start first and the short dW tiles fill the tail evenly.  The producer
-// lane takes each ticket and hands the unit to the MMA and epilogue roles
-// through a small shared-memory ring guarded by mbarriers.
-
-constexpr int SCHED_SLOTS = 4;
-constexpr uint32_t SMEM_SCHED = SMEM_MISC + 16;                  // SCHED_SLOTS ints
-constexpr uint32_t SMEM_SCHED_BAR = SMEM_SCHED + 16;             // 2 * SCHED_SLOTS mbarriers
-constexpr uint32_t SMEM_ALLOC_BWD = SMEM_SCHED_BAR + 2 * SCHED_SLOTS * 8 + 1024;
+// dX and dW of one wave in a single persistent launch of CTA pairs.  Units
+// [0, units_dx) are dX pair tiles (256 wave rows x 256 hidden columns, K =
+// padded vocabulary, row tiles fastest); units [units_dx, units_dx + units_dw)
+// are dW pair tiles (256 vocabulary rows x 256 hidden columns, K = wave rows,
+// hidden tiles fastest).  The leader CTA's producer takes tickets from a global
+// counter, so the long dX tiles start first and the short dW tiles fill the
+// tail evenly, and publishes each unit to both CTAs through a shared-memory
+// ring (mirrored into the peer with st.shared::cluster) guarded by mbarriers:
+// sched_full in each CTA, sched_empty in the leader (counting the leader's MMA
+// thread, the peer's producer and both CTAs' epilogue threads).
 
 struct BwdParams {
     int units_dx, units_dw;
-    int Mt_dx;   // 128-row tiles of the wave
+    int Mt_dx;   // 256-row pair tiles of the wave
     int Nt;      // 256-column tiles of H
     int KB_dx;   // K blocks of the padded vocabulary
     int KB_dw;   // K blocks of the wave rows
     int dw_add;  // 0: store dW tiles, 1: add them to dW
-    unsigned long long* ticket;   // global counter (zeroed by the call)
+    unsigned long long* ticket;  // global counter (zeroed by the call)
     unsigned long long ticket_base;
     int* err;
     unsigned long long wait_limit_ns;
@@ -649,41 +644,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         const __grid_constant__ CUtensorMap tmDw,    // dW store / add boxes
                         const BwdParams p) {
     extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + SMEM_BAR);
-    uint64_t* full = bars;
-    uint64_t* empty = bars + STAGES;
-    uint64_t* tfull = bars + 2 * STAGES;
-    uint64_t* tempty = bars + 2 * STAGES + 2;
-    uint64_t* drain = bars + 2 * STAGES + 4;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + SMEM_MISC);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + SMEM_MISC + 4);
-    volatile int* sched_val = reinterpret_cast<volatile int*>(smem + SMEM_SCHED);
-    uint64_t* sched_full = reinterpret_cast<uint64_t*>(smem + SMEM_SCHED_BAR);
-    uint64_t* sched_empty = sched_full + SCHED_SLOTS;
-
+    const Smem sm = smem_layout(smem_raw);
+    uint8_t* smem = sm.base;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
+    const bool leader = (rank == 0);
     const int total = p.units_dx + p.units_dw;
+    const int rofs = static_cast<int>(rank) * BM;  // this CTA's rows / columns inside a pair tile
 
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < STAGES; ++s) {
-            mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 1);
-        }
-        for (int a = 0; a < 2; ++a) {
-            mbar_init(&tfull[a], 1);
-            mbar_init(&tempty[a], EPI_THREADS);
-        }
-        for (int s = 0; s < SCHED_SLOTS; ++s) {
-            mbar_init(&sched_full[s], 1);
-            mbar_init(&sched_empty[s], 1 + EPI_THREADS);
-        }
-        mbar_init(drain, 1);
-        *abort_flag = 0;
-        fence_mbarrier_init();
-    }
     if (warp == 0 && lane == 0) {
         tma_prefetch_desc(&tmDzK);
         tma_prefetch_desc(&tmWmn);
@@ -692,59 +661,64 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         tma_prefetch_desc(&tmDx);
         tma_prefetch_desc(&tmDw);
     }
-    if (warp == 1) {
-        tmem_alloc(tmem_slot, TMEM_COLS);
-        tmem_relinquish();
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem_base = *tmem_slot;
+    const uint32_t tmem_base = pair_prologue(sm, warp);
     const uint64_t limit = p.wait_limit_ns;
+    volatile int* abort_flag = sm.abort_flag;
 
     if (warp == 0) {
         // ------------------------------------------- scheduler + TMA producer
         if (lane == 0) {
             int stage = 0;
             uint32_t phase = 0;
-            uint32_t issued_mask = 0, issued_parity = 0;
             bool ok = true;
             for (int it = 0; ok; ++it) {
                 const int slot = it % SCHED_SLOTS;
                 const uint32_t sph = static_cast<uint32_t>(it / SCHED_SLOTS) & 1u;
-                if (!mbar_wait(&sched_empty[slot], sph ^ 1u, limit, abort_flag)) {
-                    ok = false;
-                    break;
-                }
-                const unsigned long long tk = atomicAdd(p.ticket, 1ull) - p.ticket_base;
-                const int u = (tk < static_cast<unsigned long long>(total)) ? static_cast<int>(tk) : -1;
-                sched_val[slot] = u;
-                mbar_arrive(&sched_full[slot]);
-                if (u < 0) break;
-                const BwdUnit t = decode_bwd(p, u);
-                for (int kb = 0; kb < t.kb_count; ++kb) {
-                    if (!mbar_wait(&empty[stage], phase ^ 1u, limit, abort_flag)) {
+                int u;
+                if (leader) {
+                    if (!mbar_wait(&sm.sched_empty[slot], sph ^ 1u, limit, abort_flag)) {
                         ok = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(&full[stage], STAGE_TX);
+                    const unsigned long long tk = atomicAdd(p.ticket, 1ull) - p.ticket_base;
+                    u = (tk < static_cast<unsigned long long>(total)) ? static_cast<int>(tk) : -1;
+                    sm.sched_val[slot] = u;
+                    st_shared_cluster_u32(mapa_shared(smem_addr(const_cast<int*>(&sm.sched_val[slot])), 1),
+                                          static_cast<uint32_t>(u));
+                    mbar_arrive(&sm.sched_full[slot]);
+                    mbar_arrive_cluster(mapa_shared(smem_addr(&sm.sched_full[slot]), 1));
+                } else {
+                    if (!mbar_wait<true>(&sm.sched_full[slot], sph, limit, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    u = sm.sched_val[slot];
+                    mbar_arrive_cluster(mapa_shared(smem_addr(&sm.sched_empty[slot]), 0));
+                }
+                if (u < 0) break;
+                const BwdUnit t = decode_bwd(p, u);
+                for (int kb = 0; kb < t.kb_count; ++kb) {
+                    if (!mbar_wait(&sm.empty[stage], phase ^ 1u, limit, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    if (leader) mbar_arrive_expect_tx(&sm.full[stage], PAIR_STAGE_TX);
+                    const uint32_t bar = mapa_shared(smem_addr(&sm.full[stage]), 0);
                     uint8_t* a_dst = smem + SMEM_A + stage * A_STAGE_BYTES;
                     uint8_t* b_dst = smem + SMEM_B + stage * B_STAGE_BYTES;
                     if (!t.dw) {
-                        tma_load_2d(a_dst, &tmDzK, kb * BK, t.mt * BM, &full[stage]);
+                        tma_load_2d_pair(a_dst, &tmDzK, kb * BK, t.mt * PM + rofs, bar);
 #pragma unroll
-                        for (int j = 0; j < BN / 64; ++j)
-                            tma_load_2d(b_dst + j * 8192, &tmWmn, t.nt * BN + j * 64, kb * BK, &full[stage]);
+                        for (int j = 0; j < BNH / 64; ++j)
+                            tma_load_2d_pair(b_dst + j * 8192, &tmWmn, t.nt * BN + rofs + j * 64, kb * BK, bar);
                     } else {
 #pragma unroll
                         for (int j = 0; j < BM / 64; ++j)
-                            tma_load_2d(a_dst + j * 8192, &tmDzMn, t.mt * BM + j * 64, kb * BK, &full[stage]);
+                            tma_load_2d_pair(a_dst + j * 8192, &tmDzMn, t.mt * PM + rofs + j * 64, kb * BK, bar);
 #pragma unroll
-                        for (int j = 0; j < BN / 64; ++j)
-                            tma_load_2d(b_dst + j * 8192, &tmXmn, t.nt * BN + j * 64, kb * BK, &full[stage]);
+                        for (int j = 0; j < BNH / 64; ++j)
+                            tma_load_2d_pair(b_dst + j * 8192, &tmXmn, t.nt * BN + rofs + j * 64, kb * BK, bar);
                     }
-                    issued_mask |= 1u << stage;
-                    issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
                     if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1u;
@@ -755,41 +729,36 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 atomicOr(p.err, ERR_TIMEOUT);
                 *abort_flag = 1;
             }
-            for (int s = 0; s < STAGES; ++s)
-                if (issued_mask & (1u << s)) {
-                    volatile int no_abort = 0;
-                    mbar_wait(&full[s], (issued_parity >> s) & 1u, limit, &no_abort);
-                }
         }
     } else if (warp == 1) {
-        // ------------------------------------------------------- MMA issuer
-        if (lane == 0) {
+        // ---------------------------------------------- MMA issuer (leader)
+        if (lane == 0 && leader) {
             int stage = 0;
             uint32_t phase = 0;
             int acc = 0;
             uint32_t acc_phase = 0;
             bool ok = true;
-            constexpr uint32_t idesc_dx = idesc_bf16_f32(BM, BN, 0, 1);
-            constexpr uint32_t idesc_dw = idesc_bf16_f32(BM, BN, 1, 1);
+            constexpr uint32_t idesc_dx = idesc_bf16_f32(PM, BN, 0, 1);
+            constexpr uint32_t idesc_dw = idesc_bf16_f32(PM, BN, 1, 1);
             for (int it = 0; ok; ++it) {
                 const int slot = it % SCHED_SLOTS;
                 const uint32_t sph = static_cast<uint32_t>(it / SCHED_SLOTS) & 1u;
-                if (!mbar_wait(&sched_full[slot], sph, limit, abort_flag)) {
+                if (!mbar_wait(&sm.sched_full[slot], sph, limit, abort_flag)) {
                     ok = false;
                     break;
                 }
-                const int u = sched_val[slot];
-                mbar_arrive(&sched_empty[slot]);
+                const int u = sm.sched_val[slot];
+                mbar_arrive(&sm.sched_empty[slot]);
                 if (u < 0) break;
                 const BwdUnit t = decode_bwd(p, u);
-                if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, limit, abort_flag)) {
+                if (!mbar_wait(&sm.tempty[acc], acc_phase ^ 1u, limit, abort_flag)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
                 for (int kb = 0; kb < t.kb_count; ++kb) {
-                    if (!mbar_wait(&full[stage], phase, limit, abort_flag)) {
+                    if (!mbar_wait(&sm.full[stage], phase, limit, abort_flag)) {
                         ok = false;
                         break;
                     }
@@ -799,22 +768,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     if (!t.dw) {
 #pragma unroll
                         for (int k = 0; k < BK / UMMA_K; ++k)
-                            umma_bf16(d_tmem, operand_desc<0>(a_base, k), operand_desc<1>(b_base, k),
-                                      idesc_dx, (kb > 0 || k > 0) ? 1u : 0u);
+                            umma_bf16_pair(d_tmem, operand_desc<0>(a_base, k), operand_desc<1>(b_base, k),
+                                           idesc_dx, (kb > 0 || k > 0) ? 1u : 0u);
                     } else {
 #pragma unroll
                         for (int k = 0; k < BK / UMMA_K; ++k)
-                            umma_bf16(d_tmem, operand_desc<1>(a_base, k), operand_desc<1>(b_base, k),
-                                      idesc_dw, (kb > 0 || k > 0) ? 1u : 0u);
+                            umma_bf16_pair(d_tmem, operand_desc<1>(a_base, k), operand_desc<1>(b_base, k),
+                                           idesc_dw, (kb > 0 || k > 0) ? 1u : 0u);
                     }
-                    umma_commit(&empty[stage]);
+                    umma_commit_pair_mc(&sm.empty[stage], PAIR_MASK);
                     if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1u;
                     }
                 }
                 if (!ok) break;
-                umma_commit(&tfull[acc]);
+                umma_commit_pair_mc(&sm.tfull[acc], PAIR_MASK);
                 acc ^= 1;
                 if (acc == 0) acc_phase ^= 1u;
             }
@@ -822,9 +791,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 atomicOr(p.err, ERR_TIMEOUT);
                 *abort_flag = 1;
             }
-            umma_commit(drain);
+            umma_commit_pair_mc(sm.drain, 0x1);
             volatile int no_abort = 0;
-            mbar_wait(drain, 0, limit, &no_abort);
+            mbar_wait(sm.drain, 0, limit, &no_abort);
         }
     } else {
         // --------------------------------------------------------- epilogue
@@ -832,6 +801,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int q = warp & 3;
         const int r = q * 32 + lane;
         const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
+        const uint32_t tempty_leader0 = mapa_shared(smem_addr(&sm.tempty[0]), 0);
+        const uint32_t tempty_leader1 = mapa_shared(smem_addr(&sm.tempty[1]), 0);
         int acc = 0;
         uint32_t acc_phase = 0;
         bool ok = true;
@@ -839,41 +810,34 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         for (int it = 0; ok; ++it) {
             const int slot = it % SCHED_SLOTS;
             const uint32_t sph = static_cast<uint32_t>(it / SCHED_SLOTS) & 1u;
-            if (!mbar_wait(&sched_full[slot], sph, limit, abort_flag)) {
+            if (!mbar_wait<true>(&sm.sched_full[slot], sph, limit, abort_flag)) {
                 ok = false;
                 break;
             }
-            const int u = sched_val[slot];
-            mbar_arrive(&sched_empty[slot]);
+            const int u = sm.sched_val[slot];
+            mbar_arrive_cluster(mapa_shared(smem_addr(&sm.sched_empty[slot]), 0));
             if (u < 0) break;
             const BwdUnit t = decode_bwd(p, u);
-            if (!mbar_wait(&tfull[acc], acc_phase, limit, abort_flag)) {
+            if (!mbar_wait(&sm.tfull[acc], acc_phase, limit, abort_flag)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
             const uint32_t tbase = tmem_base + static_cast<uint32_t>(acc * BN) + lane_off;
             const int col0 = t.nt * BN;
+            const int row0 = t.mt * PM + rofs;
             if (!t.dw && !kDxF32) {
 #pragma unroll 1
                 for (int b = 0; b < BN / 64; ++b) {
                     const uint32_t box = store_box_acquire(ring, smem, et);
                     uint32_t w[32];
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        uint32_t v[32];
-                        tmem_ld_32x32b_x32(tbase + b * 64 + h * 32, v);
-                        tmem_wait_ld();
-                        if (b == BN / 64 - 1 && h == 1) {
-                            tc_fence_before();
-                            mbar_arrive(&tempty[acc]);
-                        }
-#pragma unroll
-                        for (int j = 0; j < 16; ++j)
-                            w[h * 16 + j] = pack_bf16x2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
+                    tmem_row64_to_bf16(tbase + b * 64, w);
+                    if (b == BN / 64 - 1) {
+                        tc_fence_before();
+                        mbar_arrive_cluster(acc ? tempty_leader1 : tempty_leader0);
                     }
                     stage_row(box, r, w);
-                    store_box_release<kDx>(ring, smem, et, &tmDx, col0 + b * 64, t.mt * BM, false);
+                    store_box_release(ring, smem, et, &tmDx, col0 + b * 64, row0, false);
                 }
             } else {
                 const CUtensorMap* out = t.dw ? &tmDw : &tmDx;
@@ -886,10 +850,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     tmem_wait_ld();
                     if (b == BN / 32 - 1) {
                         tc_fence_before();
-                        mbar_arrive(&tempty[acc]);
+                        mbar_arrive_cluster(acc ? tempty_leader1 : tempty_leader0);
                     }
                     stage_row(box, r, w);
-                    store_box_release<kDw>(ring, smem, et, out, col0 + b * 32, t.mt * BM, add);
+                    store_box_release(ring, smem, et, out, col0 + b * 32, row0, add);
                 }
             }
             acc ^= 1;
@@ -902,13 +866,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (et == 0) bulk_wait_group<0>();
     }
 
-    tc_fence_before();
-    __syncthreads();
-    if (warp == 1) {
-        __syncwarp();
-        tc_fence_after();
-        tmem_dealloc(tmem_base, TMEM_COLS);
-    }
+    pair_epilogue(sm, warp, tmem_base);
 }
 
 // ------------------------------------------------------------- split merge
