@@ -522,6 +522,7 @@ flp_status flp_backward(const void* X, const void* W, const int64_t* targets, in
         // zeroed header and every launch consumes units + pairs tickets.
         BwdParams q{};
         q.Mt_dx = static_cast<int>(cdiv(rows, PM));
+        q.GM_dx = std::min(q.Mt_dx, 8);
         q.Nt = Nt_h;
         q.units_dx = q.Mt_dx * Nt_h;
         q.units_dw = Vt * Nt_h;

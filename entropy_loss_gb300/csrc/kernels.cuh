@@ -603,6 +603,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 struct BwdParams {
     int units_dx, units_dw;
     int Mt_dx;   // 256-row pair tiles of the wave
+    int GM_dx;   // dX tiles are ordered in groups of GM_dx row tiles (L2 reuse of dZ rows and W columns)
     int Nt;      // 256-column tiles of H
     int KB_dx;   // K blocks of the padded vocabulary
     int KB_dw;   // K blocks of the wave rows
@@ -621,8 +622,12 @@ __device__ __forceinline__ BwdUnit decode_bwd(const BwdParams& p, int u) {
     BwdUnit t;
     if (u < p.units_dx) {
         t.dw = 0;
-        t.mt = u % p.Mt_dx;
-        t.nt = u / p.Mt_dx;
+        const int per_group = p.GM_dx * p.Nt;
+        const int g = u / per_group;
+        const int gm = min(p.GM_dx, p.Mt_dx - g * p.GM_dx);
+        const int r = u - g * per_group;
+        t.nt = r / gm;
+        t.mt = g * p.GM_dx + (r - t.nt * gm);
         t.kb_count = p.KB_dx;
     } else {
         const int v = u - p.units_dx;
@@ -671,6 +676,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             int stage = 0;
             uint32_t phase = 0;
             bool ok = true;
+            // the leader holds the next ticket one unit ahead, so the global
+            // atomic's latency overlaps the current unit's loads
+            unsigned long long next_tk = leader ? atomicAdd(p.ticket, 1ull) : 0ull;
             for (int it = 0; ok; ++it) {
                 const int slot = it % SCHED_SLOTS;
                 const uint32_t sph = static_cast<uint32_t>(it / SCHED_SLOTS) & 1u;
@@ -680,8 +688,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         ok = false;
                         break;
                     }
-                    const unsigned long long tk = atomicAdd(p.ticket, 1ull) - p.ticket_base;
+                    const unsigned long long tk = next_tk - p.ticket_base;
                     u = (tk < static_cast<unsigned long long>(total)) ? static_cast<int>(tk) : -1;
+                    if (u >= 0) next_tk = atomicAdd(p.ticket, 1ull);
                     sm.sched_val[slot] = u;
                     st_shared_cluster_u32(mapa_shared(smem_addr(const_cast<int*>(&sm.sched_val[slot])), 1),
                                           static_cast<uint32_t>(u));
