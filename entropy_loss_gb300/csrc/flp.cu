@@ -676,3 +676,57 @@ extern "C" flp_status flp_forward_noalloc(const void* X, const void* W, const in
     if (e != cudaSuccess) return cuda_fail(e, "flp_merge_kernel launch");
     return FLP_OK;
 }
+
+// ================================================ bounded-wait self-test
+
+extern "C" flp_status flp_selftest_wait_timeout(void* workspace, size_t workspace_bytes,
+                                                int stall_after, int64_t wait_limit_ns,
+                                                void* stream) {
+    if (!workspace || !aligned16(workspace) || workspace_bytes < FLP_SELFTEST_WORKSPACE_BYTES)
+        return fail(FLP_ERR_WORKSPACE, "self-test needs FLP_SELFTEST_WORKSPACE_BYTES of workspace");
+    if (wait_limit_ns <= 0 || wait_limit_ns > 60ll * 1000 * 1000 * 1000)
+        return fail(FLP_ERR_INVALID_ARG, "wait_limit_ns must be in (0, 60 s]");
+    DevInfo* d;
+    flp_status st = check_device(&d);
+    if (st != FLP_OK) return st;
+    constexpr int64_t M = 256, H = 256, V = 512;
+    const FwdPlan f = plan_forward(M, H, V, 1, d->pairs);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    const size_t off_x = align_up(f.bytes, 1024);
+    const size_t off_w = off_x + align_up(M * H * 2, 1024);
+    const size_t off_y = off_w + align_up(V * H * 2, 1024);
+    if (off_y + M * 8 > FLP_SELFTEST_WORKSPACE_BYTES)
+        return fail(FLP_ERR_UNSUPPORTED, "self-test layout exceeds its workspace");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    FLP_CUDA(cudaMemsetAsync(ws, 0, off_y + M * 8, s));  // header, inputs (zeros) and targets (0)
+
+    CUtensorMap tmX, tmW;
+    st = tmap_2d(&tmX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, ws + off_x, H, M, H * 2, BK, BM);
+    if (st != FLP_OK) return st;
+    st = tmap_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, ws + off_w, H, V, H * 2, BK, BNH);
+    if (st != FLP_OK) return st;
+    TileParams p{};
+    p.units = f.units;
+    p.Mt = f.Mt;
+    p.Nt = f.Vt;
+    p.S = f.S;
+    p.tps = f.tps;
+    p.GM = f.GM;
+    p.KB = static_cast<int>(cdiv(H, BK));
+    p.M = static_cast<int>(M);
+    p.V = static_cast<int>(V);
+    p.ignore_index = -100;
+    p.scale = 1.f;
+    p.scale2 = LOG2E;
+    p.y = reinterpret_cast<const long long*>(ws + off_y);
+    p.part_m = reinterpret_cast<float*>(ws + f.off_m);
+    p.part_s = reinterpret_cast<float*>(ws + f.off_s);
+    p.part_t = reinterpret_cast<float*>(ws + f.off_t);
+    p.zy = reinterpret_cast<float*>(ws + f.off_zy);
+    p.err = reinterpret_cast<int*>(ws);
+    p.wait_limit_ns = static_cast<unsigned long long>(wait_limit_ns);
+    p.debug_stall_after = stall_after < 0 ? -1 : stall_after;
+    st = launch_tile<kFwd, true>(f.grid, tmX, tmW, tmX, p, s);
+    if (st != FLP_OK) return st;
+    return flp_get_error(workspace, stream);
+}

@@ -107,6 +107,15 @@ __device__ __forceinline__ Smem smem_layout(uint8_t* raw) {
     return s;
 }
 
+// Records a timeout in the error word and tells both CTAs of the pair to stop
+// waiting (the peer's flag is written through the cluster window).
+__device__ __forceinline__ void raise_abort(const Smem& sm, int* err) {
+    atomicOr(err, ERR_TIMEOUT);
+    *sm.abort_flag = 1;
+    const uint32_t peer = cluster_ctarank() ^ 1u;
+    st_shared_cluster_u32(mapa_shared(smem_addr(const_cast<int*>(sm.abort_flag)), peer), 1u);
+}
+
 // Barrier set-up, TMEM allocation on both CTAs, and the cluster handshake that
 // makes the peer's barriers visible before any remote arrive or TMA signal.
 __device__ __forceinline__ uint32_t pair_prologue(const Smem& sm, int warp) {
@@ -338,8 +347,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
             }
             if (!ok && p.debug_stall_after < 0) {
-                atomicOr(p.err, ERR_TIMEOUT);
-                *abort_flag = 1;
+                raise_abort(sm, p.err);
             }
         }
     } else if (warp == 1) {
@@ -386,8 +394,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
             }
             if (!ok) {
-                atomicOr(p.err, ERR_TIMEOUT);
-                *abort_flag = 1;
+                raise_abort(sm, p.err);
             }
             umma_commit_pair_mc(sm.drain, 0x1);  // every MMA issued so far has completed
             volatile int no_abort = 0;
@@ -576,8 +583,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
         }
         if (!ok) {
-            atomicOr(p.err, ERR_TIMEOUT);
-            *abort_flag = 1;
+            raise_abort(sm, p.err);
         }
         if constexpr (kMode == kDz) {
             if (et == 0) bulk_wait_group<0>();
@@ -735,8 +741,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
             }
             if (!ok) {
-                atomicOr(p.err, ERR_TIMEOUT);
-                *abort_flag = 1;
+                raise_abort(sm, p.err);
             }
         }
     } else if (warp == 1) {
@@ -797,8 +802,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 if (acc == 0) acc_phase ^= 1u;
             }
             if (!ok) {
-                atomicOr(p.err, ERR_TIMEOUT);
-                *abort_flag = 1;
+                raise_abort(sm, p.err);
             }
             umma_commit_pair_mc(sm.drain, 0x1);
             volatile int no_abort = 0;
@@ -869,8 +873,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if (acc == 0) acc_phase ^= 1u;
         }
         if (!ok) {
-            atomicOr(p.err, ERR_TIMEOUT);
-            *abort_flag = 1;
+            raise_abort(sm, p.err);
         }
         if (et == 0) bulk_wait_group<0>();
     }

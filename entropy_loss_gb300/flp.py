@@ -27,7 +27,8 @@ FLP_BF16 = 1
 
 EXPORTS = ("flp_workspace_query", "flp_forward", "flp_backward", "flp_get_error",
            "flp_set_phase_events", "flp_status_string", "flp_last_error_message",
-           "flp_forward_noalloc")
+           "flp_forward_noalloc", "flp_selftest_wait_timeout")
+SELFTEST_WORKSPACE_BYTES = 1 << 20
 STATIC_SCRATCH_BYTES = 16 << 20
 PHASES = ("fwd", "merge", "dz", "bwd_gemm")
 
@@ -59,6 +60,8 @@ def load(path: str = LIB_PATH):
     lib.flp_forward_noalloc.argtypes = [p, p, p, i64, i64, i64, i64, ctypes.c_float, i32, p, p, p,
                                         p]
     lib.flp_forward_noalloc.restype = i32
+    lib.flp_selftest_wait_timeout.argtypes = [p, ctypes.c_size_t, i32, i64, p]
+    lib.flp_selftest_wait_timeout.restype = i32
     lib.flp_get_error.argtypes = [p, p]
     lib.flp_set_phase_events.argtypes = [ctypes.POINTER(ctypes.c_void_p), i32]
     lib.flp_set_phase_events.restype = i32
@@ -186,6 +189,17 @@ def set_phase_events(events) -> None:
     arr = (ctypes.c_void_p * len(events))(*[(e.cuda_event if e is not None else None)
                                             for e in events])
     _check(load().flp_set_phase_events(arr, len(events)), "flp_set_phase_events")
+
+
+def selftest_wait_timeout(stall_after: int, wait_limit_ns: int, workspace=None, stream=None) -> int:
+    """Run the forward kernel with its producers stopped after `stall_after`
+    stages (< 0: no stall) and every wait bounded by `wait_limit_ns`; returns
+    the error status the run leaves (FLP_ERR_TIMEOUT when the stall was
+    detected, FLP_OK for a normal run)."""
+    if workspace is None:
+        workspace = torch.empty(SELFTEST_WORKSPACE_BYTES, dtype=torch.uint8, device="cuda")
+    return int(load().flp_selftest_wait_timeout(_ptr(workspace), workspace.numel(), stall_after,
+                                                wait_limit_ns, _stream(stream)))
 
 
 def get_error(workspace, stream=None) -> int:

@@ -178,6 +178,23 @@ flp_status flp_get_error(const void* workspace, void* stream);
  */
 flp_status flp_set_phase_events(void* const* events, int count);
 
+/*
+ * Self-test of the kernels' bounded waits (a diagnostic; the pages have no
+ * counterpart).  Runs the forward tile kernel on a small internal problem
+ * (M = 256, H = 256, V = 512, all-zero inputs) laid out in `workspace`
+ * (caller-owned device memory of at least FLP_SELFTEST_WORKSPACE_BYTES).
+ * With stall_after >= 0 the TMA producers stop after that many pipeline
+ * stages, so the MMA issuer waits for data that never arrives: every wait
+ * gives up after wait_limit_ns, the kernel records FLP_ERR_TIMEOUT in the
+ * error word, lets its copies and MMAs in flight finish, frees its TMEM and
+ * returns; nothing faults and the context stays usable.  With stall_after < 0
+ * the same launch runs normally.  Synchronises `stream` and returns the error
+ * word (FLP_ERR_TIMEOUT, or FLP_OK), or an argument / CUDA error.
+ */
+#define FLP_SELFTEST_WORKSPACE_BYTES (1u << 20)
+flp_status flp_selftest_wait_timeout(void* workspace, size_t workspace_bytes, int stall_after,
+                                     int64_t wait_limit_ns, void* stream);
+
 /* Static description of a status code. */
 const char* flp_status_string(flp_status status);
 

@@ -115,3 +115,13 @@ def test_product_path_never_imports_the_oracle():
                 text = open(os.path.join(dirpath, f)).read()
                 assert not re.search(r"^\s*(import|from)\s+oracle\b", text, re.M), f
                 assert "flp_oracle" not in text and "libflp_oracle" not in text, f
+
+
+def test_selftest_argument_checks_need_no_device(lib):
+    from entropy_loss_gb300 import flp
+    buf = ctypes.create_string_buffer(64)
+    base = (ctypes.addressof(buf) + 15) // 16 * 16
+    assert lib.flp_selftest_wait_timeout(None, 1 << 20, 1, 1000, None) == flp.FLP_ERR_WORKSPACE
+    assert lib.flp_selftest_wait_timeout(base, 1024, 1, 1000, None) == flp.FLP_ERR_WORKSPACE
+    assert lib.flp_selftest_wait_timeout(base, 1 << 20, 1, 0, None) == flp.FLP_ERR_INVALID_ARG
+    assert lib.flp_selftest_wait_timeout(base, 1 << 20, 1, 61 * 10**9, None) == flp.FLP_ERR_INVALID_ARG
