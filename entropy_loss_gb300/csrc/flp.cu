@@ -52,7 +52,7 @@ flp_status cuda_fail(cudaError_t e, const char* where) {
 constexpr int kMaxDevices = 64;
 constexpr size_t kHeaderBytes = 1024;      // error word, ticket counter; keeps regions 1 KiB aligned
 constexpr size_t kTicketOffset = 8;        // 64-bit tile ticket counter of the backward contractions
-constexpr int64_t kDefaultChunkRows = 4096;
+constexpr int64_t kDefaultChunkRows = 8192;
 constexpr unsigned long long kWaitLimitNs = 10ull * 1000 * 1000 * 1000;  // 10 s per wait
 
 struct DevInfo {
@@ -404,7 +404,7 @@ flp_status flp_forward(const void* X, const void* W, const int64_t* targets, int
     mp.entropy = entropy;
     mp.err = err;
     mark(2, s);
-    flp_merge_kernel<<<static_cast<unsigned>(cdiv(M, 256)), 256, 0, s>>>(mp);
+    flp_merge_kernel<<<static_cast<unsigned>(cdiv(M, MERGE_ROWS)), MERGE_ROWS * MERGE_WAYS, 0, s>>>(mp);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "flp_merge_kernel launch");
     mark(3, s);
@@ -671,7 +671,7 @@ extern "C" flp_status flp_forward_noalloc(const void* X, const void* W, const in
     mp.lse = lse;
     mp.entropy = entropy;
     mp.err = err;
-    flp_merge_kernel<<<static_cast<unsigned>(cdiv(M, 256)), 256, 0, s>>>(mp);
+    flp_merge_kernel<<<static_cast<unsigned>(cdiv(M, MERGE_ROWS)), MERGE_ROWS * MERGE_WAYS, 0, s>>>(mp);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "flp_merge_kernel launch");
     return FLP_OK;

@@ -898,32 +898,57 @@ struct MergeParams {
     int* err;
 };
 
-// Combines the per-split (max, sum-exp, entropy sum) partials of each row into
-// the final lse / logprob / entropy (the "reduced" and "result" stages kept in
-// buffers separate from the raw partials).  Base-2 units inside, natural log out.
-__global__ void __launch_bounds__(256) flp_merge_kernel(const MergeParams p) {
-    const int i = blockIdx.x * blockDim.x + threadIdx.x;
-    if (i >= p.M) return;
-    float mx = -INFINITY;
-    for (int k = 0; k < p.S; ++k) {
-        const size_t o = static_cast<size_t>(k) * p.M + i;
-        if (p.part_s[o] > 0.f) mx = fmaxf(mx, p.part_m[o]);
+// Online combination of two (max, sum-exp, entropy sum) triples in base-2
+// units: the sums are rescaled to the larger max; a triple with sum 0 (a split
+// that saw no column) contributes nothing, so no 0 * inf arises.
+struct Stats {
+    float m, s, t;
+};
+
+__device__ __forceinline__ Stats combine(Stats a, Stats b) {
+    if (!(b.s > 0.f)) return a;
+    if (!(a.s > 0.f)) return b;
+    const float m = fmaxf(a.m, b.m);
+    const float da = a.m - m, db = b.m - m;
+    const float ea = exp2f(da), eb = exp2f(db);
+    Stats r;
+    r.m = m;
+    r.s = a.s * ea + b.s * eb;
+    r.t = (a.t + a.s * da) * ea + (b.t + b.s * db) * eb;
+    return r;
+}
+
+constexpr int MERGE_ROWS = 32;   // rows per block (one per lane)
+constexpr int MERGE_WAYS = 8;    // warps per block; warp w reads splits w, w + 8, ...
+
+// Combines the per-split partials of each row into the final lse / logprob /
+// entropy (the "reduced" and "result" stages kept in buffers separate from the
+// raw partials).  Each warp reads a stripe of splits for 32 consecutive rows
+// (coalesced), the stripes are combined through shared memory.  Base-2 units
+// inside, natural log out.
+__global__ void __launch_bounds__(MERGE_ROWS * MERGE_WAYS) flp_merge_kernel(const MergeParams p) {
+    __shared__ Stats part[MERGE_WAYS][MERGE_ROWS];
+    const int lane = threadIdx.x & 31;
+    const int w = threadIdx.x >> 5;
+    const int i = blockIdx.x * MERGE_ROWS + lane;
+    Stats acc{-INFINITY, 0.f, 0.f};
+    if (i < p.M) {
+        for (int k = w; k < p.S; k += MERGE_WAYS) {
+            const size_t o = static_cast<size_t>(k) * p.M + i;
+            Stats v{p.part_m[o], p.part_s[o], p.compute_entropy ? p.part_t[o] : 0.f};
+            acc = combine(acc, v);
+        }
     }
-    float sig = 0.f, tau = 0.f;
-    for (int k = 0; k < p.S; ++k) {
-        const size_t o = static_cast<size_t>(k) * p.M + i;
-        const float sk = p.part_s[o];
-        if (!(sk > 0.f)) continue;  // a split that saw no column contributes nothing
-        const float d = p.part_m[o] - mx;
-        const float a = exp2f(d);
-        sig = fmaf(sk, a, sig);
-        if (p.compute_entropy) tau = fmaf(p.part_t[o] + sk * d, a, tau);
-    }
-    const float l2s = log2f(sig);
-    const float lse = (mx + l2s) * LN2;
+    part[w][lane] = acc;
+    __syncthreads();
+    if (w != 0 || i >= p.M) return;
+#pragma unroll
+    for (int j = 1; j < MERGE_WAYS; ++j) acc = combine(acc, part[j][lane]);
+    const float l2s = log2f(acc.s);
+    const float lse = (acc.m + l2s) * LN2;
     p.lse[i] = lse;
     const long long yv = p.y[i];
-    float lp, ent = p.compute_entropy ? (l2s - tau / sig) * LN2 : 0.f;
+    float lp, ent = p.compute_entropy ? (l2s - acc.t / acc.s) * LN2 : 0.f;
     if (yv == p.ignore_index) {
         lp = 0.f;
         ent = 0.f;

@@ -76,6 +76,11 @@ WORKLOADS = {
         # size used for full ncu captures of the kernels
         Workload("quarter_vocab_m4096_h4096_v32768", 4096, 4096, 32768, ignore_frac=0.05,
                  seed=1006),
+        # the model-shape campaign of the native commit (M = 8192 tokens, random
+        # inputs): small H makes the per-logit epilogue relatively heavier
+        Workload("m8192_h2048_v151936", 8192, 2048, 151936, seed=1007),
+        Workload("m8192_h5120_v202048", 8192, 5120, 202048, seed=1008),
+        Workload("m8192_h7168_v129280", 8192, 7168, 129280, seed=1009),
     ]
 }
 

@@ -81,7 +81,7 @@ typedef enum { FLP_F32 = 0, FLP_BF16 = 1 } flp_dtype;
  *               Triton kernels", section "Correctness", keeps raw and final
  *               results in separate buffers, and so does this library).
  *   bwd_bytes : needed by flp_backward when it processes the rows in waves of
- *               `chunk_rows` rows (chunk_rows <= 0 selects 4096); one wave's
+ *               `chunk_rows` rows (chunk_rows <= 0 selects 8192); one wave's
  *               bf16 dZ, [chunk, ceil(V/256)*256], dominates.  The Liger-Kernel
  *               native commit's "Memory" section reports the same kind of
  *               reusable workspace, and pull request 1294's "Kernel design
