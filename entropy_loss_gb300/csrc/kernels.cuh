@@ -685,23 +685,35 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             // the leader holds the next ticket one unit ahead, so the global
             // atomic's latency overlaps the current unit's loads
             unsigned long long next_tk = leader ? atomicAdd(p.ticket, 1ull) : 0ull;
+            // The leader keeps one unit published ahead of the one it loads, so
+            // the peer finds the next unit in its ring when it needs it.
+            int published = 0;
+            bool ended = false;  // the terminating (-1) unit is in the ring
             for (int it = 0; ok; ++it) {
                 const int slot = it % SCHED_SLOTS;
                 const uint32_t sph = static_cast<uint32_t>(it / SCHED_SLOTS) & 1u;
                 int u;
                 if (leader) {
-                    if (!mbar_wait(&sm.sched_empty[slot], sph ^ 1u, limit, abort_flag)) {
-                        ok = false;
-                        break;
+                    while (!ended && published < it + 2) {
+                        const int ps = published % SCHED_SLOTS;
+                        const uint32_t pph = static_cast<uint32_t>(published / SCHED_SLOTS) & 1u;
+                        if (!mbar_wait(&sm.sched_empty[ps], pph ^ 1u, limit, abort_flag)) {
+                            ok = false;
+                            break;
+                        }
+                        const unsigned long long tk = next_tk - p.ticket_base;
+                        const int pu = (tk < static_cast<unsigned long long>(total)) ? static_cast<int>(tk) : -1;
+                        if (pu >= 0) next_tk = atomicAdd(p.ticket, 1ull);
+                        sm.sched_val[ps] = pu;
+                        st_shared_cluster_u32(mapa_shared(smem_addr(const_cast<int*>(&sm.sched_val[ps])), 1),
+                                              static_cast<uint32_t>(pu));
+                        mbar_arrive(&sm.sched_full[ps]);
+                        mbar_arrive_cluster(mapa_shared(smem_addr(&sm.sched_full[ps]), 1));
+                        ++published;
+                        if (pu < 0) ended = true;
                     }
-                    const unsigned long long tk = next_tk - p.ticket_base;
-                    u = (tk < static_cast<unsigned long long>(total)) ? static_cast<int>(tk) : -1;
-                    if (u >= 0) next_tk = atomicAdd(p.ticket, 1ull);
-                    sm.sched_val[slot] = u;
-                    st_shared_cluster_u32(mapa_shared(smem_addr(const_cast<int*>(&sm.sched_val[slot])), 1),
-                                          static_cast<uint32_t>(u));
-                    mbar_arrive(&sm.sched_full[slot]);
-                    mbar_arrive_cluster(mapa_shared(smem_addr(&sm.sched_full[slot]), 1));
+                    if (!ok) break;
+                    u = sm.sched_val[slot];  // written by this thread; not reused before `published` passes it + 4
                 } else {
                     if (!mbar_wait<true>(&sm.sched_full[slot], sph, limit, abort_flag)) {
                         ok = false;
