@@ -84,6 +84,35 @@ def max_over_ranks(x: float, world: int) -> float:
     return float(t.item())
 
 
+def kernel_sources_digest() -> str:
+    """sha256 over the CUDA sources' names and contents (sorted by name)."""
+    import glob
+    import hashlib
+    h = hashlib.sha256()
+    for f in sorted(glob.glob(os.path.join(ROOT, "entropy_loss_gb300", "csrc", "*"))):
+        with open(f, "rb") as fh:
+            h.update(os.path.basename(f).encode() + b"\0" + fh.read() + b"\0")
+    return h.hexdigest()
+
+
+def profiled_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary of
+    `workload`, or None when there is none or the kernel sources changed since."""
+    path = os.path.join(ROOT, "profiles", f"dram_traffic_{workload}.md")
+    try:
+        with open(path) as f:
+            lines = f.read().splitlines()
+    except OSError:
+        return None
+    digest = kernel_sources_digest()
+    for ln in lines:
+        parts = ln.split()
+        if (len(parts) == 5 and parts[0] == "traffic-per-launch" and parts[1] == kernel
+                and parts[3] == "sources-sha256"):
+            return float(parts[2]) if parts[4] == digest else None
+    return None
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -237,7 +266,8 @@ def run_ours(args, world, rank, local):
              "bwd_gemm": "flp_bwd_gemm_kernel"}[dom]
     roofline = {"bound": "tensor", "kernel": kname, "achieved": round(achieved, 1),
                 "peak": peak, "unit": UNIT, "frac": round(achieved / peak, 4),
-                "traffic": None, "peak_source": f"bf16_tflops_sustained of {peak_src}"}
+                "traffic": profiled_traffic(kname, w.name),
+                "peak_source": f"bf16_tflops_sustained of {peak_src}"}
 
     waves = -(-M // wave_rows)
     launches = K * (2 + 2 * waves)
