@@ -392,9 +392,14 @@ def run_reference(args, world, rank):
     d = inputs.make_inputs(w)
     g = np.random.default_rng(1)
     steps, warm = args.steps, max(args.warmup, 3)
+    # two-point calibration t(n) = a + b n (a: the fp64 dW buffer and other
+    # fixed costs), then rows per step so the whole run takes about `budget`
     t1 = _oracle_sample_time(d, g.choice(w.M, 1, replace=False), oracle)
+    t8 = _oracle_sample_time(d, g.choice(w.M, 8, replace=False), oracle)
+    b = max((t8 - t1) / 7.0, 1e-6)
+    a = max(t1 - b, 0.0)
     budget = 150.0  # seconds for the whole run
-    n = int(max(1, min(w.M, budget / ((steps + warm) * max(t1, 1e-6)))))
+    n = int(max(1, min(w.M, (budget / (steps + warm) - a) / b)))
     for _ in range(warm):
         _oracle_sample_time(d, g.choice(w.M, n, replace=False), oracle)
     times = [_oracle_sample_time(d, g.choice(w.M, n, replace=False), oracle) for _ in range(steps)]

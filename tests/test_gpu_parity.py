@@ -148,6 +148,24 @@ def test_waves_and_ragged_tail(flp):
     run_case(flp, case(700, 136, 2100, seed=4), chunk_rows=256)
 
 
+@pytest.mark.parametrize("M", [4097, 5000])
+def test_wave_boundaries_4096(flp, M):
+    # 4096-row waves: one extra row (4097) and a two-wave tail (5000), the
+    # boundary cases the native commit's "Correctness" section lists.
+    run_case(flp, case(M, 64, 1000, seed=15), chunk_rows=4096)
+
+
+def test_odd_vocabulary_50257(flp):
+    # the odd vocabulary that exercises the vocabulary-tail path (chunked GRPO
+    # page, "Correctness"): 50257 = 196 * 256 + 81
+    run_case(flp, case(300, 64, 50257, seed=16))
+
+
+def test_large_hidden_small_rows(flp):
+    # a long K loop (H = 16384) on a handful of rows and a ragged vocabulary
+    run_case(flp, case(70, 16384, 700, seed=17, w_std=0.01))
+
+
 def test_dx_fp32(flp):
     run_case(flp, case(260, 96, 999, seed=5), dx_dtype=torch.float32)
 
