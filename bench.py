@@ -48,6 +48,9 @@ def parse():
     ap.add_argument("--workload", default=inputs.HEADLINE, choices=sorted(inputs.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--chunk-rows", type=int, default=0,
+                    help="backward wave size in rows (0: the library default); smaller waves "
+                         "trade speed for a smaller workspace")
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="target CPU time of the oracle baseline sample")
     return ap.parse_args()
@@ -198,7 +201,7 @@ def run_ours(args, world, rank, local):
     X, W, y = d["X"].to(dev), d["W"].to(dev), d["y"].to(dev)
     g_lp = d["g_lp"].to(dev)
     g_ent = d["g_ent"].to(dev) if d["g_ent"] is not None else None
-    ws = flp.alloc_workspace(M, H, V, ent, device=dev)
+    ws = flp.alloc_workspace(M, H, V, ent, chunk_rows=args.chunk_rows, device=dev)
     lp = torch.empty(M, dtype=torch.float32, device=dev)
     lse = torch.empty(M, dtype=torch.float32, device=dev)
     en = torch.empty(M, dtype=torch.float32, device=dev) if ent else None
@@ -281,7 +284,8 @@ def run_ours(args, world, rank, local):
                    "scale": d["scale"], "ignore_frac": w.ignore_frac,
                    "parallelism": "replicas" if world > 1 else "single",
                    "l2": "inputs larger than L2 (W is %.2f GiB), no flush" % (V * H * 2 / 2**30),
-                   "wave_rows": wave_rows, "fwd_bwd_flop_per_step": flops_step},
+                   "wave_rows": wave_rows, "workspace_bytes": int(ws.numel()),
+                   "fwd_bwd_flop_per_step": flops_step},
         "pct_of_bf16_peak": {"measured_burst": round(value / world / float(peaks.get("bf16_tflops", 1900.0)), 4),
                              "measured_sustained": round(value / world / peak, 4),
                              "nominal_2250": round(value / world / 2250.0, 4)},
