@@ -60,6 +60,9 @@ def _load():
                 fn = getattr(lib, name)
                 fn.argtypes = args
                 fn.restype = ctypes.c_int
+            lib.flpo_loss.argtypes = [p, p, i64, i64, ctypes.c_int, p, p, p, ctypes.c_double,
+                                      ctypes.c_double, ctypes.c_double, p, p, p]
+            lib.flpo_loss.restype = ctypes.c_int
             lib.flpo_num_threads.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -141,3 +144,27 @@ def backward(X, W, y, g_lp, g_ent, ignore_index=-100, scale=1.0, compute_entropy
 def bf16_bits_to_f64(a: np.ndarray) -> np.ndarray:
     """Exact widening of bf16 bit patterns (uint16) to fp64."""
     return (np.asarray(a, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+LOSS_NLL_MEAN = 1
+LOSS_GRPO = 2
+
+
+def loss(logprob, y, kind, ignore_index=-100, old_logprob=None, advantage=None,
+         ref_logprob=None, eps_low=0.2, eps_high=0.2, beta=0.0):
+    """Loss head on per-row log-probs: returns (per_row, grad_logprob, scalar)."""
+    lib = _load()
+    lp = np.ascontiguousarray(logprob, dtype=np.float64)
+    y = np.ascontiguousarray(y, dtype=np.int64)
+    M = lp.shape[0]
+    conv = (lambda a: None if a is None else np.ascontiguousarray(a, dtype=np.float64))
+    old, adv, ref = conv(old_logprob), conv(advantage), conv(ref_logprob)
+    per_row = np.zeros(M)
+    grad = np.zeros(M)
+    out = np.zeros(1)
+    st = lib.flpo_loss(_ptr(lp), _ptr(y), M, int(ignore_index), int(kind), _ptr(old), _ptr(adv),
+                       _ptr(ref), float(eps_low), float(eps_high), float(beta), _ptr(per_row),
+                       _ptr(grad), _ptr(out))
+    if st != FLPO_OK:
+        raise OracleError(f"oracle loss failed with status {st}")
+    return per_row, grad, float(out[0])

@@ -305,3 +305,62 @@ int flpo_num_threads(void) {
     return 1;
 #endif
 }
+
+/*
+ * Loss heads on the per-row log-probs (the chunked GRPO loss of "Triton MoE
+ * improvements and chunked GRPO improvements", section "Chunked Triton GRPO
+ * loss": a loss on top of the lm_head's per-token log-probs, aggregated over
+ * the valid tokens).  Rows whose target is ignore_index are not tokens of the
+ * loss.  With N valid rows:
+ *
+ *   kind 1 (token-mean NLL):  loss = -(1/N) sum_i lp_i
+ *   kind 2 (clipped surrogate, token-level ratio, token-mean):
+ *       r_i    = exp(lp_i - old_i)
+ *       surr_i = min(r_i A_i, clip(r_i, 1 - eps_low, 1 + eps_high) A_i)
+ *       kl_i   = exp(ref_i - lp_i) - (ref_i - lp_i) - 1      (when ref given)
+ *       loss   = (1/N) sum_i [ -surr_i + beta kl_i ]
+ *
+ * Outputs: per-row loss terms (0 on ignored rows), the scalar loss, and the
+ * gradient of the scalar loss with respect to each row's log-prob (the
+ * upstream gradient the backward takes).  The gradient is the derivative of
+ * the definition: the min picks r A unless the clipped term is strictly
+ * smaller, and a clipped ratio has zero derivative.
+ */
+int flpo_loss(const double* lp, const int64_t* y, int64_t M, int64_t ignore_index, int kind,
+              const double* old_lp, const double* adv, const double* ref_lp, double eps_low,
+              double eps_high, double beta, double* per_row, double* grad, double* loss) {
+    if (M < 0 || (kind != 1 && kind != 2)) return FLPO_INVALID_ARG;
+    if (kind == 2 && (!old_lp || !adv)) return FLPO_INVALID_ARG;
+    int64_t n = 0;
+    for (int64_t i = 0; i < M; ++i)
+        if (y[i] != ignore_index) ++n;
+    double total = 0.0;
+    for (int64_t i = 0; i < M; ++i) {
+        double term = 0.0, g = 0.0;
+        if (y[i] != ignore_index) {
+            if (kind == 1) {
+                term = -lp[i];
+                g = -1.0;
+            } else {
+                double r = exp(lp[i] - old_lp[i]);
+                double lo = 1.0 - eps_low, hi = 1.0 + eps_high;
+                double rc = r < lo ? lo : (r > hi ? hi : r);
+                double s1 = r * adv[i], s2 = rc * adv[i];
+                double surr = s1 <= s2 ? s1 : s2;
+                double dsurr = s1 <= s2 ? r * adv[i] : 0.0;
+                term = -surr;
+                g = -dsurr;
+                if (ref_lp && beta != 0.0) {
+                    double d = ref_lp[i] - lp[i];
+                    term += beta * (exp(d) - d - 1.0);
+                    g += beta * (1.0 - exp(d));
+                }
+            }
+        }
+        if (per_row) per_row[i] = term;
+        total += term;
+        if (grad) grad[i] = n > 0 ? g / (double)n : 0.0;
+    }
+    if (loss) *loss = n > 0 ? total / (double)n : 0.0;
+    return FLPO_OK;
+}
