@@ -14,6 +14,7 @@
 
 #include "flp.h"
 #include "kernels.cuh"
+#include "loss.cuh"
 
 using namespace flp;
 
@@ -729,4 +730,46 @@ extern "C" flp_status flp_selftest_wait_timeout(void* workspace, size_t workspac
     st = launch_tile<kFwd, true>(f.grid, tmX, tmW, tmX, p, s);
     if (st != FLP_OK) return st;
     return flp_get_error(workspace, stream);
+}
+
+// ============================================================ loss heads
+
+extern "C" flp_status flp_loss(const float* logprob, const int64_t* targets, int64_t M,
+                               int64_t ignore_index, int kind, const float* old_logprob,
+                               const float* advantage, const float* ref_logprob, float eps_low,
+                               float eps_high, float beta, float* per_token_loss,
+                               float* grad_logprob, float* loss, void* stream) {
+    if (M < 0) return fail(FLP_ERR_INVALID_ARG, "M >= 0 required");
+    if (kind != FLP_LOSS_NLL_MEAN && kind != FLP_LOSS_CLIPPED_SURROGATE)
+        return fail(FLP_ERR_INVALID_ARG, "unknown loss kind");
+    if (!loss || (M > 0 && (!logprob || !targets)))
+        return fail(FLP_ERR_INVALID_ARG, "logprob, targets and loss must be non-null");
+    if (kind == FLP_LOSS_CLIPPED_SURROGATE && M > 0 && (!old_logprob || !advantage))
+        return fail(FLP_ERR_INVALID_ARG, "the clipped surrogate needs old_logprob and advantage");
+    if (!(eps_low >= 0.f && eps_low <= 1.f && eps_high >= 0.f && std::isfinite(eps_high) &&
+          std::isfinite(beta)))
+        return fail(FLP_ERR_INVALID_ARG, "eps_low in [0, 1], eps_high >= 0 and beta finite required");
+    DevInfo* d;
+    flp_status st = device_info(&d, nullptr);
+    if (st != FLP_OK) return st;
+    LossParams p{};
+    p.lp = logprob;
+    p.y = reinterpret_cast<const long long*>(targets);
+    p.M = M;
+    p.ignore_index = ignore_index;
+    p.kind = kind;
+    p.old_lp = old_logprob;
+    p.adv = advantage;
+    p.ref_lp = ref_logprob;
+    p.eps_low = eps_low;
+    p.eps_high = eps_high;
+    p.beta = beta;
+    p.per_row = per_token_loss;
+    p.grad = grad_logprob;
+    p.loss = loss;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    flp_loss_kernel<<<1, LOSS_THREADS, 0, s>>>(p);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "flp_loss_kernel launch");
+    return FLP_OK;
 }

@@ -27,7 +27,9 @@ FLP_BF16 = 1
 
 EXPORTS = ("flp_workspace_query", "flp_forward", "flp_backward", "flp_get_error",
            "flp_set_phase_events", "flp_status_string", "flp_last_error_message",
-           "flp_forward_noalloc", "flp_selftest_wait_timeout")
+           "flp_forward_noalloc", "flp_selftest_wait_timeout", "flp_loss")
+FLP_LOSS_NLL_MEAN = 1
+FLP_LOSS_CLIPPED_SURROGATE = 2
 SELFTEST_WORKSPACE_BYTES = 1 << 20
 STATIC_SCRATCH_BYTES = 16 << 20
 PHASES = ("fwd", "merge", "dz", "bwd_gemm")
@@ -62,6 +64,9 @@ def load(path: str = LIB_PATH):
     lib.flp_forward_noalloc.restype = i32
     lib.flp_selftest_wait_timeout.argtypes = [p, ctypes.c_size_t, i32, i64, p]
     lib.flp_selftest_wait_timeout.restype = i32
+    lib.flp_loss.argtypes = [p, p, i64, i64, i32, p, p, p, ctypes.c_float, ctypes.c_float,
+                             ctypes.c_float, p, p, p, p]
+    lib.flp_loss.restype = i32
     lib.flp_get_error.argtypes = [p, p]
     lib.flp_set_phase_events.argtypes = [ctypes.POINTER(ctypes.c_void_p), i32]
     lib.flp_set_phase_events.restype = i32
@@ -200,6 +205,24 @@ def selftest_wait_timeout(stall_after: int, wait_limit_ns: int, workspace=None, 
         workspace = torch.empty(SELFTEST_WORKSPACE_BYTES, dtype=torch.uint8, device="cuda")
     return int(load().flp_selftest_wait_timeout(_ptr(workspace), workspace.numel(), stall_after,
                                                 wait_limit_ns, _stream(stream)))
+
+
+def loss(logprob, y, kind=FLP_LOSS_NLL_MEAN, *, ignore_index: int = -100, old_logprob=None,
+         advantage=None, ref_logprob=None, eps_low: float = 0.2, eps_high: float = 0.2,
+         beta: float = 0.0, per_token=True, stream=None):
+    """Loss head on per-row log-probs: (scalar loss [1], grad_logprob [M],
+    per-token terms [M] or None).  grad_logprob is the upstream gradient for
+    `backward`."""
+    M = logprob.shape[0]
+    dev = logprob.device
+    out = torch.empty(1, dtype=torch.float32, device=dev)
+    grad = torch.empty(M, dtype=torch.float32, device=dev)
+    per = torch.empty(M, dtype=torch.float32, device=dev) if per_token else None
+    _check(load().flp_loss(_ptr(logprob), _ptr(y), M, ignore_index, int(kind), _ptr(old_logprob),
+                           _ptr(advantage), _ptr(ref_logprob), float(eps_low), float(eps_high),
+                           float(beta), _ptr(per), _ptr(grad), _ptr(out), _stream(stream)),
+           "flp_loss")
+    return out, grad, per
 
 
 def get_error(workspace, stream=None) -> int:

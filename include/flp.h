@@ -156,6 +156,29 @@ flp_status flp_forward_noalloc(const void* X, const void* W, const int64_t* targ
                                void* stream);
 
 /*
+ * Loss heads on the forward's per-row log-probs (the chunked GRPO page,
+ * "Chunked Triton GRPO loss": a loss on top of the lm_head's per-token
+ * log-probs).  With N = the number of rows whose target is not ignore_index:
+ *   FLP_LOSS_NLL_MEAN           loss = -(1/N) sum_i lp_i
+ *   FLP_LOSS_CLIPPED_SURROGATE  r_i = exp(lp_i - old_i),
+ *       loss = (1/N) sum_i [ -min(r_i A_i, clip(r_i, 1 - eps_low, 1 + eps_high) A_i)
+ *                            + beta (exp(ref_i - lp_i) - (ref_i - lp_i) - 1) ]
+ *       (token-level ratio, two-sided clip, k3 KL estimator against a
+ *       reference policy when ref_logprob != NULL).
+ * All arrays are fp32 [M] device arrays: old_logprob and advantage are
+ * required for the clipped surrogate and ignored otherwise; per_token_loss
+ * (the bracketed terms, 0 on ignored rows) and grad_logprob (d loss / d lp_i,
+ * the upstream gradient to hand to flp_backward) may be NULL; loss is one
+ * fp32 on the device.  One block with fixed-order fp64 reductions:
+ * deterministic.  N = 0 gives loss 0 and zero gradients.
+ */
+typedef enum { FLP_LOSS_NLL_MEAN = 1, FLP_LOSS_CLIPPED_SURROGATE = 2 } flp_loss_kind;
+flp_status flp_loss(const float* logprob, const int64_t* targets, int64_t M, int64_t ignore_index,
+                    int kind, const float* old_logprob, const float* advantage,
+                    const float* ref_logprob, float eps_low, float eps_high, float beta,
+                    float* per_token_loss, float* grad_logprob, float* loss, void* stream);
+
+/*
  * Synchronises `stream`, then reads and returns the workspace's error word
  * (FLP_OK, FLP_ERR_BAD_TARGET or FLP_ERR_TIMEOUT) written by the most recent
  * flp_forward / flp_backward that used this workspace.  Each of those calls

@@ -125,3 +125,16 @@ def test_selftest_argument_checks_need_no_device(lib):
     assert lib.flp_selftest_wait_timeout(base, 1024, 1, 1000, None) == flp.FLP_ERR_WORKSPACE
     assert lib.flp_selftest_wait_timeout(base, 1 << 20, 1, 0, None) == flp.FLP_ERR_INVALID_ARG
     assert lib.flp_selftest_wait_timeout(base, 1 << 20, 1, 61 * 10**9, None) == flp.FLP_ERR_INVALID_ARG
+
+
+def test_loss_argument_checks_need_no_device(lib):
+    from entropy_loss_gb300 import flp
+    import ctypes as C
+    buf = C.create_string_buffer(64)
+    b = (C.addressof(buf) + 15) // 16 * 16
+    f = C.c_float
+    assert lib.flp_loss(b, b, 4, -100, 7, b, b, None, f(0.2), f(0.2), f(0), b, b, b, None) == flp.FLP_ERR_INVALID_ARG
+    assert lib.flp_loss(b, b, -1, -100, 1, None, None, None, f(0.2), f(0.2), f(0), b, b, b, None) == flp.FLP_ERR_INVALID_ARG
+    assert lib.flp_loss(b, b, 4, -100, 2, None, b, None, f(0.2), f(0.2), f(0), b, b, b, None) == flp.FLP_ERR_INVALID_ARG
+    assert lib.flp_loss(b, b, 4, -100, 2, b, b, None, f(-0.1), f(0.2), f(0), b, b, b, None) == flp.FLP_ERR_INVALID_ARG
+    assert lib.flp_loss(b, b, 4, -100, 1, None, None, None, f(0.2), f(0.2), f(0), b, b, None, None) == flp.FLP_ERR_INVALID_ARG
