@@ -285,6 +285,7 @@ flp_status common_checks(const void* X, const void* W, const int64_t* targets, i
     if (H % 8 != 0) return fail(FLP_ERR_UNSUPPORTED, "H must be a multiple of 8 (TMA row pitch)");
     if (M > (int64_t)INT_MAX - BM || V > (int64_t)INT_MAX - BN || H > (int64_t)INT_MAX - BN)
         return fail(FLP_ERR_UNSUPPORTED, "dimension too large for int32 tile coordinates");
+    if (M == 0) return FLP_OK;  // nothing is read: empty inputs may be null
     if (!X || !W || !targets) return fail(FLP_ERR_INVALID_ARG, "X, W and targets must be non-null");
     if (!aligned16(X) || !aligned16(W) || !aligned16(targets))
         return fail(FLP_ERR_INVALID_ARG, "X, W and targets must be 16-byte aligned");
@@ -338,7 +339,7 @@ flp_status flp_forward(const void* X, const void* W, const int64_t* targets, int
     flp_status st = common_checks(X, W, targets, M, H, V);
     if (st != FLP_OK) return st;
     const int ent = compute_entropy ? 1 : 0;
-    if (!logprob || !lse || (ent && !entropy) || (!ent && entropy))
+    if (M > 0 && (!logprob || !lse || (ent && !entropy) || (!ent && entropy)))
         return fail(FLP_ERR_INVALID_ARG, "logprob and lse required; entropy iff compute_entropy");
     if (!aligned16(logprob) || !aligned16(lse) || (entropy && !aligned16(entropy)))
         return fail(FLP_ERR_INVALID_ARG, "outputs must be 16-byte aligned");
@@ -421,7 +422,7 @@ flp_status flp_backward(const void* X, const void* W, const int64_t* targets, in
     flp_status st = common_checks(X, W, targets, M, H, V);
     if (st != FLP_OK) return st;
     const int ent = compute_entropy ? 1 : 0;
-    if (!dX || !dW) return fail(FLP_ERR_INVALID_ARG, "dX and dW must be non-null");
+    if ((M > 0 && !dX) || !dW) return fail(FLP_ERR_INVALID_ARG, "dX and dW must be non-null");
     if (dX_dtype != FLP_BF16 && dX_dtype != FLP_F32)
         return fail(FLP_ERR_INVALID_ARG, "dX_dtype must be FLP_BF16 or FLP_F32");
     if (dW_dtype != FLP_F32) return fail(FLP_ERR_UNSUPPORTED, "dW_dtype must be FLP_F32");
@@ -598,7 +599,7 @@ extern "C" flp_status flp_forward_noalloc(const void* X, const void* W, const in
     flp_status st = common_checks(X, W, targets, M, H, V);
     if (st != FLP_OK) return st;
     const int ent = compute_entropy ? 1 : 0;
-    if (!logprob || !lse || (ent && !entropy) || (!ent && entropy))
+    if (M > 0 && (!logprob || !lse || (ent && !entropy) || (!ent && entropy)))
         return fail(FLP_ERR_INVALID_ARG, "logprob and lse required; entropy iff compute_entropy");
     if (!aligned16(logprob) || !aligned16(lse) || (entropy && !aligned16(entropy)))
         return fail(FLP_ERR_INVALID_ARG, "outputs must be 16-byte aligned");

@@ -166,6 +166,42 @@ def test_large_hidden_small_rows(flp):
     run_case(flp, case(70, 16384, 700, seed=17, w_std=0.01))
 
 
+@pytest.mark.parametrize("scale", [-0.8, 0.0])
+def test_negative_and_zero_scale(flp, scale):
+    run_case(flp, case(200, 64, 777, seed=18, scale=scale))
+
+
+def test_wide_ignore_index_and_far_bad_target(flp):
+    dev = torch.device("cuda")
+    d = case(150, 64, 500, seed=19)
+    big = 1 << 40
+    d["y"][d["y"] == -100] = big
+    d["ignore_index"] = big
+    run_case(flp, d)
+    d["y"][3] = -(1 << 40)  # out of range, far beyond int32
+    X, W, y = d["X"].to(dev), d["W"].to(dev), d["y"].to(dev)
+    ws = flp.alloc_workspace(150, 64, 500, True, device=dev)
+    lp, _, _ = flp.forward(X, W, y, ignore_index=big, workspace=ws)
+    assert flp.get_error(ws) == flp.FLP_ERR_BAD_TARGET and torch.isnan(lp[3])
+
+
+def test_zero_rows(flp):
+    dev = torch.device("cuda")
+    X = torch.empty(0, 64, dtype=torch.bfloat16, device=dev)
+    W = torch.randn(300, 64, device=dev).to(torch.bfloat16)
+    y = torch.empty(0, dtype=torch.int64, device=dev)
+    lp, lse, en = flp.forward(X, W, y)
+    assert lp.numel() == 0
+    dW = torch.full((300, 64), 7.0, device=dev)
+    _, dW = flp.backward(X, W, y, lse, en, lp, en, dW=dW)
+    torch.cuda.synchronize()
+    assert torch.all(dW == 0)
+    dW.fill_(7.0)
+    flp.backward(X, W, y, lse, en, lp, en, dW=dW, accumulate_dW=True)
+    torch.cuda.synchronize()
+    assert torch.all(dW == 7.0)
+
+
 def test_dx_fp32(flp):
     run_case(flp, case(260, 96, 999, seed=5), dx_dtype=torch.float32)
 
