@@ -12,6 +12,8 @@
 #include <mutex>
 #include <string>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "flp.h"
 #include "kernels.cuh"
 #include "loss.cuh"
@@ -21,6 +23,14 @@ using namespace flp;
 namespace {
 
 thread_local std::string g_msg;
+
+// Named host range for profilers (NVTX; a no-op unless a tool is attached).
+struct NvtxRange {
+    explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+    ~NvtxRange() { nvtxRangePop(); }
+    NvtxRange(const NvtxRange&) = delete;
+    NvtxRange& operator=(const NvtxRange&) = delete;
+};
 
 constexpr int kMaxPhaseEvents = 10;
 thread_local void* g_events[kMaxPhaseEvents] = {};
@@ -336,6 +346,7 @@ flp_status flp_forward(const void* X, const void* W, const int64_t* targets, int
                        int64_t H, int64_t V, int64_t ignore_index, float scale,
                        int compute_entropy, float* logprob, float* lse, float* entropy,
                        void* workspace, size_t workspace_bytes, void* stream) {
+    NvtxRange range("flp_forward");
     flp_status st = common_checks(X, W, targets, M, H, V);
     if (st != FLP_OK) return st;
     const int ent = compute_entropy ? 1 : 0;
@@ -419,6 +430,7 @@ flp_status flp_backward(const void* X, const void* W, const int64_t* targets, in
                         const float* grad_logprob, const float* grad_entropy, void* dX,
                         flp_dtype dX_dtype, void* dW, flp_dtype dW_dtype, int accumulate_dW,
                         void* workspace, size_t workspace_bytes, void* stream) {
+    NvtxRange range("flp_backward");
     flp_status st = common_checks(X, W, targets, M, H, V);
     if (st != FLP_OK) return st;
     const int ent = compute_entropy ? 1 : 0;
@@ -473,6 +485,7 @@ flp_status flp_backward(const void* X, const void* W, const int64_t* targets, in
     const int64_t gm_rows = std::max<int64_t>(4, 40ll * 1000 * 1000 / (PM * 2 * H));
 
     for (int64_t r0 = 0; r0 < M; r0 += chunk) {
+        NvtxRange wave_range("flp_backward_wave");
         const int64_t rows = std::min(chunk, M - r0);
         const uint8_t* Xc = static_cast<const uint8_t*>(X) + r0 * H * 2;
         uint8_t* dXc = static_cast<uint8_t*>(dX) + r0 * H * dx_es;
