@@ -260,6 +260,28 @@ flp_status check_device(DevInfo** d) {
     return ensure_attrs(*d);
 }
 
+// A device pointer must live on the device the call launches on (the one
+// current on the calling thread); host or managed-elsewhere memory is refused.
+flp_status check_on_current_device(const void* p, const char* what) {
+    if (!p) return FLP_OK;
+    int dev = 0;
+    FLP_CUDA(cudaGetDevice(&dev));
+    cudaPointerAttributes a{};
+    cudaError_t e = cudaPointerGetAttributes(&a, p);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaPointerGetAttributes");
+    if (a.type != cudaMemoryTypeDevice && a.type != cudaMemoryTypeManaged) {
+        char buf[160];
+        snprintf(buf, sizeof buf, "%s is not device memory", what);
+        return fail(FLP_ERR_INVALID_ARG, buf);
+    }
+    if (a.type == cudaMemoryTypeDevice && a.device != dev) {
+        char buf[160];
+        snprintf(buf, sizeof buf, "%s lives on device %d but the current device is %d", what, a.device, dev);
+        return fail(FLP_ERR_INVALID_ARG, buf);
+    }
+    return FLP_OK;
+}
+
 // Launches `kernel` on `grid` CTAs grouped in clusters of two (the CTA pairs
 // that share each tcgen05.mma.cta_group::2 tile).
 template <typename... KArgs, typename... Args>
@@ -358,6 +380,7 @@ flp_status flp_forward(const void* X, const void* W, const int64_t* targets, int
     DevInfo* d;
     st = check_device(&d);
     if (st != FLP_OK) return st;
+    if (M > 0 && (st = check_on_current_device(X, "X")) != FLP_OK) return st;
     const FwdPlan f = plan_forward(M, H, V, ent, d->pairs);
     if (!workspace || workspace_bytes < f.bytes || !aligned16(workspace))
         return fail(FLP_ERR_WORKSPACE, "forward workspace null, misaligned or too small");
@@ -448,6 +471,7 @@ flp_status flp_backward(const void* X, const void* W, const int64_t* targets, in
     DevInfo* d;
     st = check_device(&d);
     if (st != FLP_OK) return st;
+    if (M > 0 && (st = check_on_current_device(X, "X")) != FLP_OK) return st;
     if (!workspace || !aligned16(workspace) || workspace_bytes < kHeaderBytes)
         return fail(FLP_ERR_WORKSPACE, "backward workspace null, misaligned or too small");
     // Largest wave (multiple of 128 rows, at most M rounded up) the workspace holds.
@@ -623,6 +647,7 @@ extern "C" flp_status flp_forward_noalloc(const void* X, const void* W, const in
     if (st != FLP_OK) return st;
     st = check_device(&d);
     if (st != FLP_OK) return st;
+    if (M > 0 && (st = check_on_current_device(X, "X")) != FLP_OK) return st;
     const FwdPlan f = plan_forward(M, H, V, ent, d->pairs);
     if (f.bytes > FLP_STATIC_SCRATCH_BYTES) {
         char buf[200];

@@ -317,6 +317,17 @@ def test_argument_errors(flp):
     with pytest.raises(flp.FlpError) as e:
         flp.backward(X, W, y, lse, en, lse, en, workspace=tiny_ws)
     assert e.value.status == flp.FLP_ERR_WORKSPACE
+    # host memory handed over as X is refused before any launch
+    import ctypes
+    Xh = d["X"].pin_memory()
+    lib = flp.load()
+    lp_, lse_, en_ = (torch.empty(64, device=dev) for _ in range(3))
+    ws_ = flp.alloc_workspace(64, 64, 300, True, device=dev)
+    p = lambda t: ctypes.c_void_p(t.data_ptr())
+    st = lib.flp_forward(p(Xh), p(W), p(y), 64, 64, 300, -100, 1.0, 1, p(lp_), p(lse_), p(en_),
+                         p(ws_), ws_.numel(), ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert st == flp.FLP_ERR_INVALID_ARG
+    assert b"not device memory" in lib.flp_last_error_message()
     Xo = torch.zeros(64, 60, dtype=torch.bfloat16, device=dev)
     Wo = torch.zeros(300, 60, dtype=torch.bfloat16, device=dev)
     ws = flp.alloc_workspace(64, 64, 300, True, device=dev)
