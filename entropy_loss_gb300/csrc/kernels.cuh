@@ -473,20 +473,52 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         }
                         const int nv = nvalid - c * 32;
                         if (nv <= 0) continue;
+                        if (nv >= 32) {
+                            // full chunk: packed fp32 pairs halve the FP32 instruction count
+                            uint64_t up[16];
+                            const uint64_t sc2 = f2_pack(p.scale2, p.scale2);
+                            float cmax = -INFINITY;
+#pragma unroll
+                            for (int j = 0; j < 16; ++j) {
+                                up[j] = f2_mul(f2_pack(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1])), sc2);
+                                float a, b;
+                                f2_unpack(up[j], a, b);
+                                cmax = fmaxf(cmax, fmaxf(a, b));
+                            }
+                            if (cmax > run_m) {
+                                const float alpha = ex2_approx(run_m - cmax);
+                                if constexpr (kEnt)
+                                    run_t = (run_s > 0.f) ? alpha * (run_t + run_s * (run_m - cmax)) : 0.f;
+                                run_s *= alpha;
+                                run_m = cmax;
+                            }
+                            const uint64_t negm = f2_pack(-run_m, -run_m);
+                            uint64_t sacc = f2_pack(0.f, 0.f), tacc = f2_pack(0.f, 0.f);
+#pragma unroll
+                            for (int j = 0; j < 16; ++j) {
+                                const uint64_t d = f2_add(up[j], negm);
+                                float d0, d1;
+                                f2_unpack(d, d0, d1);
+                                const uint64_t e = f2_pack(ex2_approx(d0), ex2_approx(d1));
+                                sacc = f2_add(sacc, e);
+                                if constexpr (kEnt) tacc = f2_fma(e, d, tacc);
+                            }
+                            float s0, s1, t0, t1;
+                            f2_unpack(sacc, s0, s1);
+                            run_s += s0 + s1;
+                            if constexpr (kEnt) {
+                                f2_unpack(tacc, t0, t1);
+                                run_t += t0 + t1;
+                            }
+                            continue;
+                        }
+                        // the vocabulary tail: columns >= V are left out of every sum
                         float uu[32];
                         float cmax = -INFINITY;
-                        if (nv >= 32) {
 #pragma unroll
-                            for (int j = 0; j < 32; ++j) {
-                                uu[j] = __uint_as_float(v[j]) * p.scale2;
-                                cmax = fmaxf(cmax, uu[j]);
-                            }
-                        } else {
-#pragma unroll
-                            for (int j = 0; j < 32; ++j) {
-                                uu[j] = (j < nv) ? __uint_as_float(v[j]) * p.scale2 : -INFINITY;
-                                cmax = fmaxf(cmax, uu[j]);
-                            }
+                        for (int j = 0; j < 32; ++j) {
+                            uu[j] = (j < nv) ? __uint_as_float(v[j]) * p.scale2 : -INFINITY;
+                            cmax = fmaxf(cmax, uu[j]);
                         }
                         if (cmax > run_m) {
                             // rescale the running sums to the new maximum; a row that
@@ -497,32 +529,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                             run_s *= alpha;
                             run_m = cmax;
                         }
-                        float s0 = 0.f, s1 = 0.f, t0 = 0.f, t1 = 0.f;
-                        if (nv >= 32) {
+                        float s0 = 0.f, t0 = 0.f;
 #pragma unroll
-                            for (int j = 0; j < 32; j += 2) {
-                                const float d0 = uu[j] - run_m, d1 = uu[j + 1] - run_m;
-                                const float e0 = ex2_approx(d0), e1 = ex2_approx(d1);
+                        for (int j = 0; j < 32; ++j) {
+                            if (j < nv) {
+                                const float d0 = uu[j] - run_m;
+                                const float e0 = ex2_approx(d0);
                                 s0 += e0;
-                                s1 += e1;
-                                if constexpr (kEnt) {
-                                    t0 = fmaf(e0, d0, t0);
-                                    t1 = fmaf(e1, d1, t1);
-                                }
-                            }
-                        } else {
-#pragma unroll
-                            for (int j = 0; j < 32; ++j) {
-                                if (j < nv) {
-                                    const float d0 = uu[j] - run_m;
-                                    const float e0 = ex2_approx(d0);
-                                    s0 += e0;
-                                    if constexpr (kEnt) t0 = fmaf(e0, d0, t0);
-                                }
+                                if constexpr (kEnt) t0 = fmaf(e0, d0, t0);
                             }
                         }
-                        run_s += s0 + s1;
-                        if constexpr (kEnt) run_t += t0 + t1;
+                        run_s += s0;
+                        if constexpr (kEnt) run_t += t0;
                     }
                 } else {
                     // dZ: 4 store boxes of 64 bf16 columns each
@@ -541,11 +559,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                             }
                             const int cbase = col0 + b * 64 + h * 32;
                             float dz[32];
+                            {
+                                // packed fp32 pairs: p = 2^(acc s log2e - LSE2), dz = p (K1 + K2 acc)
+                                const uint64_t sc2 = f2_pack(p.scale2, p.scale2);
+                                const uint64_t nl = f2_pack(-lse2, -lse2);
+                                const uint64_t k1 = f2_pack(K1, K1), k2 = f2_pack(K2, K2);
 #pragma unroll
-                            for (int j = 0; j < 32; ++j) {
-                                const float a = __uint_as_float(v[j]);
-                                const float pj = ex2_approx(fmaf(a, p.scale2, -lse2));
-                                dz[j] = pj * fmaf(a, K2, K1);
+                                for (int j = 0; j < 16; ++j) {
+                                    const uint64_t a = f2_pack(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
+                                    float x0, x1;
+                                    f2_unpack(f2_fma(a, sc2, nl), x0, x1);
+                                    const uint64_t pp = f2_pack(ex2_approx(x0), ex2_approx(x1));
+                                    f2_unpack(f2_mul(pp, f2_fma(a, k2, k1)), dz[2 * j], dz[2 * j + 1]);
+                                }
                             }
                             const long long tc = yv - cbase;
                             if (tc >= 0 && tc < 32) {
