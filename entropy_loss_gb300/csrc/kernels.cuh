@@ -483,7 +483,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                                 up[j] = f2_mul(f2_pack(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1])), sc2);
                                 float a, b;
                                 f2_unpack(up[j], a, b);
-                                cmax = fmaxf(cmax, fmaxf(a, b));
+                                cmax = fmax3(cmax, a, b);
                             }
                             if (cmax > run_m) {
                                 const float alpha = ex2_approx(run_m - cmax);

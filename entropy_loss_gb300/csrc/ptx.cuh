@@ -265,6 +265,13 @@ __device__ __forceinline__ void umma_commit_pair_mc(uint64_t* bar, uint16_t mask
 
 // ------------------------------------------------------------------- math
 
+// max(a, b, c) in one instruction.
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
 // Packed fp32 pairs (two lanes per instruction, round-to-nearest).
 __device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
     uint64_t r;
