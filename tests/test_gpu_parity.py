@@ -131,6 +131,8 @@ def test_tiny_workload(flp):
 @pytest.mark.parametrize("M,H,V", [
     (1, 64, 1), (1, 8, 2), (127, 64, 255), (128, 64, 256), (129, 72, 257),
     (300, 200, 3001), (5, 8, 50257 // 16), (513, 264, 1000),
+    # around the 256-row pair tiles and 256-column vocabulary tiles, H < 64
+    (255, 56, 511), (256, 128, 512), (257, 136, 513), (511, 64, 767), (512, 64, 1024),
 ])
 def test_edge_shapes(flp, M, H, V):
     run_case(flp, case(M, H, V))
