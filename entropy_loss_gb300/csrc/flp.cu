@@ -215,6 +215,12 @@ cudaError_t set_smem_attr() {
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_ALLOC);
 }
 
+template <bool kDxF32, bool kDwBf16>
+cudaError_t set_bwd_smem_attr() {
+    return cudaFuncSetAttribute(flp_bwd_gemm_kernel<kDxF32, kDwBf16>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_ALLOC);
+}
+
 flp_status ensure_attrs(DevInfo* d) {
     if (smem_attrs_done(d)) return FLP_OK;
     cudaError_t e = cudaSuccess;
@@ -222,12 +228,10 @@ flp_status ensure_attrs(DevInfo* d) {
     if (e == cudaSuccess) e = set_smem_attr<kFwd, false>();
     if (e == cudaSuccess) e = set_smem_attr<kDz, true>();
     if (e == cudaSuccess) e = set_smem_attr<kDz, false>();
-    if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(flp_bwd_gemm_kernel<false>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_ALLOC);
-    if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(flp_bwd_gemm_kernel<true>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_ALLOC);
+    if (e == cudaSuccess) e = set_bwd_smem_attr<false, false>();
+    if (e == cudaSuccess) e = set_bwd_smem_attr<true, false>();
+    if (e == cudaSuccess) e = set_bwd_smem_attr<false, true>();
+    if (e == cudaSuccess) e = set_bwd_smem_attr<true, true>();
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
     // How many clusters of two fit at once (SMs that a cluster cannot pair up
     // stay idle); the persistent grids never exceed it.
@@ -460,7 +464,10 @@ flp_status flp_backward(const void* X, const void* W, const int64_t* targets, in
     if ((M > 0 && !dX) || !dW) return fail(FLP_ERR_INVALID_ARG, "dX and dW must be non-null");
     if (dX_dtype != FLP_BF16 && dX_dtype != FLP_F32)
         return fail(FLP_ERR_INVALID_ARG, "dX_dtype must be FLP_BF16 or FLP_F32");
-    if (dW_dtype != FLP_F32) return fail(FLP_ERR_UNSUPPORTED, "dW_dtype must be FLP_F32");
+    if (dW_dtype != FLP_F32 && dW_dtype != FLP_BF16)
+        return fail(FLP_ERR_INVALID_ARG, "dW_dtype must be FLP_F32 or FLP_BF16");
+    if (dW_dtype == FLP_BF16 && accumulate_dW)
+        return fail(FLP_ERR_UNSUPPORTED, "a bf16 dW cannot be accumulated into (fp32 accumulation); use an fp32 dW");
     if (M > 0 && (!lse || (ent && !entropy)))
         return fail(FLP_ERR_INVALID_ARG, "lse (and entropy when compute_entropy) required");
     if (!aligned16(dX) || !aligned16(dW) || (lse && !aligned16(lse)) ||
@@ -480,16 +487,21 @@ flp_status flp_backward(const void* X, const void* W, const int64_t* targets, in
     const int64_t mr = std::max<int64_t>(BM, cdiv(M, BM) * BM);
     const int64_t chunk = std::min(mr, fit / BM * BM);
     if (chunk < BM) return fail(FLP_ERR_WORKSPACE, "backward workspace holds fewer than 128 rows of dZ");
+    if (dW_dtype == FLP_BF16 && chunk < M)
+        return fail(FLP_ERR_UNSUPPORTED,
+                    "a bf16 dW needs the backward in one wave (waves accumulate dW in fp32): pass a "
+                    "workspace that holds all M rows of dZ, or an fp32 dW");
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     int* err = reinterpret_cast<int*>(ws);
     FLP_CUDA(cudaMemsetAsync(ws, 0, kHeaderBytes, s));
     const size_t dx_es = dX_dtype == FLP_F32 ? 4 : 2;
+    const size_t dw_es = dW_dtype == FLP_F32 ? 4 : 2;
     const bool no_grad = (grad_logprob == nullptr) && (!ent || grad_entropy == nullptr);
     if (M == 0 || no_grad) {
         if (M > 0) FLP_CUDA(cudaMemsetAsync(dX, 0, static_cast<size_t>(M) * H * dx_es, s));
-        if (!accumulate_dW) FLP_CUDA(cudaMemsetAsync(dW, 0, static_cast<size_t>(V) * H * 4, s));
+        if (!accumulate_dW) FLP_CUDA(cudaMemsetAsync(dW, 0, static_cast<size_t>(V) * H * dw_es, s));
         return FLP_OK;
     }
     void* dz = ws + kHeaderBytes;
@@ -500,7 +512,10 @@ flp_status flp_backward(const void* X, const void* W, const int64_t* targets, in
     if (st != FLP_OK) return st;
     st = tmap_2d(&tmW_mn, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, W, H, V, H * 2, 64, 64);
     if (st != FLP_OK) return st;
-    st = tmap_2d(&tmDW, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, dW, H, V, H * 4, 32, BM);
+    if (dW_dtype == FLP_BF16)
+        st = tmap_2d(&tmDW, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dW, H, V, H * 2, 64, BM);
+    else
+        st = tmap_2d(&tmDW, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, dW, H, V, H * 4, 32, BM);
     if (st != FLP_OK) return st;
 
     const int Vt = static_cast<int>(Vp / BN);
@@ -576,11 +591,16 @@ flp_status flp_backward(const void* X, const void* W, const int64_t* targets, in
         const int pairs_bw = std::min(total, pairs);
         ticket_base += static_cast<unsigned long long>(total) + pairs_bw;
         if (first) mark(6, s);
-        st = (dX_dtype == FLP_F32)
-                 ? launch_pairs(flp_bwd_gemm_kernel<true>, 2 * pairs_bw, s, "flp_bwd_gemm_kernel launch",
-                                tmDZk, tmW_mn, tmDZmn, tmXmn, tmDX, tmDW, q)
-                 : launch_pairs(flp_bwd_gemm_kernel<false>, 2 * pairs_bw, s, "flp_bwd_gemm_kernel launch",
-                                tmDZk, tmW_mn, tmDZmn, tmXmn, tmDX, tmDW, q);
+        const char* what = "flp_bwd_gemm_kernel launch";
+        const int g = 2 * pairs_bw;
+        if (dX_dtype == FLP_F32)
+            st = (dW_dtype == FLP_BF16)
+                     ? launch_pairs(flp_bwd_gemm_kernel<true, true>, g, s, what, tmDZk, tmW_mn, tmDZmn, tmXmn, tmDX, tmDW, q)
+                     : launch_pairs(flp_bwd_gemm_kernel<true, false>, g, s, what, tmDZk, tmW_mn, tmDZmn, tmXmn, tmDX, tmDW, q);
+        else
+            st = (dW_dtype == FLP_BF16)
+                     ? launch_pairs(flp_bwd_gemm_kernel<false, true>, g, s, what, tmDZk, tmW_mn, tmDZmn, tmXmn, tmDX, tmDW, q)
+                     : launch_pairs(flp_bwd_gemm_kernel<false, false>, g, s, what, tmDZk, tmW_mn, tmDZmn, tmXmn, tmDX, tmDW, q);
         if (st != FLP_OK) return st;
         if (first) mark(7, s);
     }

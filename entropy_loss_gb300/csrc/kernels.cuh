@@ -671,7 +671,9 @@ __device__ __forceinline__ BwdUnit decode_bwd(const BwdParams& p, int u) {
     return t;
 }
 
-template <bool kDxF32>
+// kDxF32: dX boxes in fp32 (else bf16).  kDwBf16: dW boxes in bf16, stored
+// (single wave, no accumulation; else fp32, stored or added).
+template <bool kDxF32, bool kDwBf16>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     flp_bwd_gemm_kernel(const __grid_constant__ CUtensorMap tmDzK,   // dZ, K-major A (dX)
                         const __grid_constant__ CUtensorMap tmWmn,   // W, MN-major B (dX)
@@ -877,7 +879,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const uint32_t tbase = tmem_base + static_cast<uint32_t>(acc * BN) + lane_off;
             const int col0 = t.nt * BN;
             const int row0 = t.mt * PM + rofs;
-            if (!t.dw && !kDxF32) {
+            const bool bf16_out = t.dw ? kDwBf16 : !kDxF32;
+            if (bf16_out) {
+                const CUtensorMap* out = t.dw ? &tmDw : &tmDx;
 #pragma unroll 1
                 for (int b = 0; b < BN / 64; ++b) {
                     const uint32_t box = store_box_acquire(ring, smem, et);
@@ -888,7 +892,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         mbar_arrive_cluster(acc ? tempty_leader1 : tempty_leader0);
                     }
                     stage_row(box, r, w);
-                    store_box_release(ring, smem, et, &tmDx, col0 + b * 64, row0, false);
+                    store_box_release(ring, smem, et, out, col0 + b * 64, row0, false);
                 }
             } else {
                 const CUtensorMap* out = t.dw ? &tmDw : &tmDx;

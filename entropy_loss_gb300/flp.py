@@ -163,23 +163,26 @@ def forward_noalloc(X, W, y, logprob, lse, entropy=None, *, ignore_index: int = 
 
 def backward(X, W, y, lse, entropy, grad_logprob, grad_entropy, *, ignore_index: int = -100,
              scale: float = 1.0, compute_entropy: bool = True, dX=None, dW=None,
-             dx_dtype=torch.bfloat16, accumulate_dW: bool = False, workspace=None, stream=None):
-    """(dX, dW) for upstream gradients of logprob and entropy (None = zero)."""
+             dx_dtype=torch.bfloat16, dw_dtype=torch.float32, accumulate_dW: bool = False,
+             workspace=None, stream=None):
+    """(dX, dW) for upstream gradients of logprob and entropy (None = zero).
+    dW may be fp32 (accumulated in fp32 across waves) or bf16 (one wave only)."""
     M, H = X.shape
     V = W.shape[0]
     dev = X.device
     if dX is None:
         dX = torch.empty(M, H, dtype=dx_dtype, device=dev)
     if dW is None:
-        dW = torch.empty(V, H, dtype=torch.float32, device=dev)
+        dW = torch.empty(V, H, dtype=dw_dtype, device=dev)
     dxt = FLP_F32 if dX.dtype == torch.float32 else FLP_BF16
+    dwt = FLP_F32 if dW.dtype == torch.float32 else FLP_BF16
     if workspace is None:
         workspace = alloc_workspace(M, H, V, compute_entropy, device=dev)
     _check(load().flp_backward(_ptr(X), _ptr(W), _ptr(y), M, H, V, ignore_index, float(scale),
                                int(compute_entropy), _ptr(lse),
                                _ptr(entropy if compute_entropy else None), _ptr(grad_logprob),
                                _ptr(grad_entropy if compute_entropy else None), _ptr(dX), dxt,
-                               _ptr(dW), FLP_F32, int(accumulate_dW), _ptr(workspace),
+                               _ptr(dW), dwt, int(accumulate_dW), _ptr(workspace),
                                workspace.numel(), _stream(stream)), "flp_backward")
     return dX, dW
 
@@ -247,9 +250,15 @@ class FusedLinearLogprob(torch.autograd.Function):
         ignore_index, scale, compute_entropy, workspace = ctx.cfg
         g_lp = None if g_lp is None else g_lp.contiguous().float()
         g_ent = None if (g_ent is None or not compute_entropy) else g_ent.contiguous().float()
+        # a bf16 weight gets its bf16 gradient straight from the epilogue when
+        # one backward wave covers every row; otherwise fp32 waves, then a cast
+        M, V = X.shape[0], W.shape[0]
+        wave_rows = (workspace.numel() - 1024) // (((V + 255) // 256) * 256 * 2) // 128 * 128
+        direct = W.dtype == torch.bfloat16 and wave_rows >= M
         dX, dW = backward(X, W, y, lse, ent if compute_entropy else None, g_lp, g_ent,
                           ignore_index=ignore_index, scale=scale, compute_entropy=compute_entropy,
-                          dx_dtype=X.dtype, workspace=workspace)
+                          dx_dtype=X.dtype, dw_dtype=torch.bfloat16 if direct else torch.float32,
+                          workspace=workspace)
         return dX, dW.to(W.dtype), None, None, None, None, None
 
 

@@ -109,8 +109,12 @@ flp_status flp_forward(const void* X, const void* W, const int64_t* targets, int
 
 /*
  * Backward: given the forward's lse (and entropy when compute_entropy != 0),
- * writes dX [M, H] (dtype dX_dtype, overwritten) and dW [V, H] (dtype must be
- * FLP_F32; overwritten, or added to when accumulate_dW != 0).
+ * writes dX [M, H] (dtype dX_dtype, overwritten) and dW [V, H] (dtype
+ * dW_dtype; overwritten, or added to when accumulate_dW != 0).  An FLP_F32 dW
+ * accumulates in fp32 across waves.  An FLP_BF16 dW is written once, rounded
+ * from the fp32 accumulator, so it needs the whole backward in one wave (a
+ * workspace that holds all M rows of dZ) and no accumulate_dW; otherwise the
+ * call returns FLP_ERR_UNSUPPORTED before launching anything.
  *   grad_logprob, grad_entropy : fp32 [M] upstream gradients of logprob and
  *       entropy; NULL means zero.  grad_entropy is ignored when
  *       compute_entropy == 0.  For a mean NLL loss over N valid rows pass

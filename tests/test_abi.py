@@ -94,7 +94,8 @@ def test_backward_argument_checks_need_no_device(lib):
     assert call(dX=None) == flp.FLP_ERR_INVALID_ARG
     assert call(dW=None) == flp.FLP_ERR_INVALID_ARG
     assert call(dxt=7) == flp.FLP_ERR_INVALID_ARG
-    assert call(dwt=1) == flp.FLP_ERR_UNSUPPORTED
+    assert call(dwt=7) == flp.FLP_ERR_INVALID_ARG
+    assert call(dwt=1, acc=1) == flp.FLP_ERR_UNSUPPORTED  # bf16 dW cannot be accumulated into
     assert call(lse=None) == flp.FLP_ERR_INVALID_ARG
     assert call(en=None) == flp.FLP_ERR_INVALID_ARG
     assert call(H=12) == flp.FLP_ERR_UNSUPPORTED

@@ -204,6 +204,33 @@ def test_zero_rows(flp):
     assert torch.all(dW == 7.0)
 
 
+def test_dw_bf16_single_wave(flp):
+    dev = torch.device("cuda")
+    d = case(300, 200, 3001, seed=20)
+    X, W, y = d["X"].to(dev), d["W"].to(dev), d["y"].to(dev)
+    g1, g2 = d["g_lp"].to(dev), d["g_ent"].to(dev)
+    ws = flp.alloc_workspace(300, 200, 3001, True, device=dev)
+    lp, lse, en = flp.forward(X, W, y, workspace=ws)
+    _, dW32 = flp.backward(X, W, y, lse, en, g1, g2, workspace=ws)
+    dX, dW16 = flp.backward(X, W, y, lse, en, g1, g2, dw_dtype=torch.bfloat16, workspace=ws)
+    torch.cuda.synchronize()
+    assert dW16.dtype == torch.bfloat16
+    # the bf16 output is the fp32 accumulator rounded once (RNE)
+    assert torch.equal(dW16, dW32.to(torch.bfloat16))
+    Xb, Wb = inputs.bf16_bits(d["X"]), inputs.bf16_bits(d["W"])
+    _, o_dw = oracle.backward(Xb, Wb, d["y"].numpy(), d["g_lp"].double().numpy(),
+                              d["g_ent"].double().numpy())
+    check_grad(dW16, o_dw, "dW bf16")
+    # several waves, or accumulation, need the fp32 dW
+    small = flp.alloc_workspace(300, 200, 3001, True, chunk_rows=128, device=dev)
+    with pytest.raises(flp.FlpError) as e:
+        flp.backward(X, W, y, lse, en, g1, g2, dw_dtype=torch.bfloat16, workspace=small)
+    assert e.value.status == flp.FLP_ERR_UNSUPPORTED
+    with pytest.raises(flp.FlpError) as e:
+        flp.backward(X, W, y, lse, en, g1, g2, dW=dW16, accumulate_dW=True, workspace=ws)
+    assert e.value.status == flp.FLP_ERR_UNSUPPORTED
+
+
 def test_dx_fp32(flp):
     run_case(flp, case(260, 96, 999, seed=5), dx_dtype=torch.float32)
 
