@@ -51,6 +51,9 @@ def parse():
     ap.add_argument("--chunk-rows", type=int, default=0,
                     help="backward wave size in rows (0: the library default); smaller waves "
                          "trade speed for a smaller workspace")
+    ap.add_argument("--schedule", default="auto", choices=["auto", "split", "fused"],
+                    help="backward tile schedule: per-wave dZ then dX/dW launches (split) or one "
+                         "persistent launch (fused); auto lets the library pick")
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="target CPU time of the oracle baseline sample")
     return ap.parse_args()
@@ -209,10 +212,17 @@ def run_ours(args, world, rank, local):
     dW = torch.empty(V, H, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
     kw = dict(ignore_index=d["ignore_index"], scale=d["scale"], compute_entropy=ent, workspace=ws)
+    bkw = dict(kw, schedule=args.schedule)
+    wave_rows, waves, sched = flp.backward_plan(M, H, V, ws.numel(), args.schedule)
+    # phases the library records (events 2k, 2k+1 around phase k)
+    if sched == "fused":
+        phase_names = {"fwd": 0, "merge": 1, "bwd": 2}
+    else:
+        phase_names = {"fwd": 0, "merge": 1, "bwd_dz": 2, "bwd_gemm": 3}
 
     def step():
         flp.forward(X, W, y, logprob=lp, lse=lse, entropy=en, **kw)
-        flp.backward(X, W, y, lse, en, g_lp, g_ent, dX=dX, dW=dW, **kw)
+        flp.backward(X, W, y, lse, en, g_lp, g_ent, dX=dX, dW=dW, **bkw)
 
     for _ in range(max(args.warmup, 3)):
         step()
@@ -247,7 +257,7 @@ def run_ours(args, world, rank, local):
     ms_total = max_over_ranks(ms_total, world)
     ms_step = ms_total / K
     phase_ms = {}
-    for i, name in enumerate(flp.PHASES):
+    for name, i in phase_names.items():
         vals = [evs[k][2 * i].elapsed_time(evs[k][2 * i + 1]) for k in range(K)]
         phase_ms[name] = statistics.mean(vals)
     if flp.get_error(ws) != flp.FLP_OK:
@@ -256,24 +266,28 @@ def run_ours(args, world, rank, local):
     flops_step = 8.0 * M * H * V
     value = world * flops_step / (ms_step * 1e-3) / 1e12
 
-    # roofline of the dominant kernel (largest mean duration among the phases)
+    # roofline of the dominant kernel launch (largest mean duration among the phases)
     peaks, peak_src = load_peaks()
-    _, bwd_bytes = flp.workspace_query(M, H, V, ent)
-    wave_rows = min(M, ((ws.numel() - 1024) // (((V + 255) // 256) * 256 * 2)) // 128 * 128)
-    phase_flops = {"fwd": 2.0 * M * H * V, "dz": 2.0 * wave_rows * H * V,
-                   "bwd_gemm": 4.0 * wave_rows * H * V}  # dX and dW of the first wave
-    dom = max(phase_flops, key=lambda n: phase_ms[n])
+    first_wave = min(M, wave_rows)
+    phase_flops = {"fwd": 2.0 * M * H * V, "merge": 0.0,
+                   "bwd": 6.0 * M * H * V,                       # fused: every wave in one launch
+                   "bwd_dz": 2.0 * first_wave * H * V,           # split: the first wave's launches
+                   "bwd_gemm": 4.0 * first_wave * H * V}
+    dom = max(phase_ms, key=lambda n: phase_ms[n])
     achieved = phase_flops[dom] / (phase_ms[dom] * 1e-3) / 1e12
     peak = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
-    kname = {"fwd": "flp_tile_kernel<fwd>", "dz": "flp_tile_kernel<dz>",
-             "bwd_gemm": "flp_bwd_gemm_kernel"}[dom]
+    kname = {"fwd": "flp_fwd_kernel", "bwd": "flp_bwd_kernel", "bwd_dz": "flp_bwd_kernel/dz",
+             "bwd_gemm": "flp_bwd_kernel/dx_dw"}[dom]
     roofline = {"bound": "tensor", "kernel": kname, "achieved": round(achieved, 1),
                 "peak": peak, "unit": UNIT, "frac": round(achieved / peak, 4),
                 "traffic": profiled_traffic(kname, w.name),
                 "peak_source": f"bf16_tflops_sustained of {peak_src}"}
 
-    waves = -(-M // wave_rows)
-    launches = K * (2 + 2 * waves)
+    # our kernels per step: forward, merge, and the backward's launches (from the
+    # library's own plan; host arithmetic)
+    pairs = torch.cuda.get_device_properties(dev).multi_processor_count // 2
+    bwd_launches = int(flp.backward_schedule(M, H, V, ws.numel(), args.schedule, pairs)[:, 0].max()) + 1
+    launches = K * (2 + bwd_launches)
 
     result = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": K,
@@ -284,7 +298,8 @@ def run_ours(args, world, rank, local):
                    "scale": d["scale"], "ignore_frac": w.ignore_frac,
                    "parallelism": "replicas" if world > 1 else "single",
                    "l2": "inputs larger than L2 (W is %.2f GiB), no flush" % (V * H * 2 / 2**30),
-                   "wave_rows": wave_rows, "workspace_bytes": int(ws.numel()),
+                   "wave_rows": wave_rows, "waves": waves, "bwd_schedule": sched,
+                   "workspace_bytes": int(ws.numel()),
                    "fwd_bwd_flop_per_step": flops_step},
         "pct_of_bf16_peak": {"measured_burst": round(value / world / float(peaks.get("bf16_tflops", 1900.0)), 4),
                              "measured_sustained": round(value / world / peak, 4),
@@ -297,14 +312,15 @@ def run_ours(args, world, rank, local):
     }
 
     if not args.no_e2e:
-        result["e2e"] = run_e2e(args, d, X.device, W, ws, world, M, H, V, ent, stream, flp)
+        result["e2e"] = run_e2e(args, d, X.device, W, ws, world, M, H, V, ent, stream, flp,
+                                args.schedule)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(d, w, args.cpu_seconds)
     if rank == 0:
         print(json.dumps(result), flush=True)
 
 
-def run_e2e(args, d, dev, W, ws, world, M, H, V, ent, stream, flp):
+def run_e2e(args, d, dev, W, ws, world, M, H, V, ent, stream, flp, schedule):
     """Same step through the public API, with the step's inputs (hidden states,
     targets, upstream grads) copied from pinned host memory each step and the
     per-row log-probs read back.  W is the layer's resident parameter.  As in a
@@ -334,7 +350,7 @@ def run_e2e(args, d, dev, W, ws, world, M, H, V, ent, stream, flp):
         X, y, g1 = bufs[i][0], bufs[i][1], bufs[i][2]
         g2 = bufs[i][3] if geh is not None else None
         lp, lse, en = flp.forward(X, W, y, **kw)
-        flp.backward(X, W, y, lse, en, g1, g2, **kw)
+        flp.backward(X, W, y, lse, en, g1, g2, schedule=schedule, **kw)
         free[i].record(stream)
         out_h.copy_(lp, non_blocking=True)
 

@@ -1,0 +1,595 @@
+// bwd.cuh - the backward of the fused linear log-prob head on CTA pairs.
+//
+// One persistent kernel whose units are 256 x 256 pair tiles of three kinds:
+//   dZ : the logits tile recomputed (K = H), then
+//        dZ = s [g_lp (onehot - p) + g_ent p (sum_j p_j z_j - z)]  in bf16,
+//        TMA-stored to the wave's dZ buffer (rows of the wave x padded V)
+//   dX : dX[wave] tile = dZ W        (K = padded vocabulary; W read MN-major)
+//   dW : dW tile (+)= dZ^T X[wave]   (K = wave rows; both operands MN-major)
+// The leader CTA of each pair takes tickets from a global counter and maps
+// them to units through a schedule of segments that the host lays down, then
+// publishes each unit to both CTAs' roles through a shared-memory ring.
+//
+// Two schedules drive it (the host picks one per call):
+//   split : per row wave, one launch with the wave's dZ tiles, then one launch
+//           with its dX tiles (long, first) and dW tiles (short, filling the
+//           tail); the kernel boundary orders the phases.
+//   fused : every wave in one launch.  A dX tile waits until the dZ tiles of
+//           its rows are stored, a dW tile until those of its vocabulary
+//           column are; from the second wave on, a dZ tile waits until the
+//           previous wave's dX and dW tiles that read its buffer slot are
+//           done, and a dW tile until the previous wave's add into the same
+//           dW rows is.  The counters live in the workspace; every wait is on
+//           a ticket handed out earlier, so the lowest unfinished ticket can
+//           always proceed, and every wait is bounded in time.
+// Both schedules compute every output tile with the same instructions in the
+// same K order, so their results agree bit for bit.
+#pragma once
+#include "kernels.cuh"
+
+namespace flp {
+
+enum UnitKind : int { kUnitDz = 0, kUnitDx = 1, kUnitDw = 2 };
+
+// A segment is a run of consecutive tickets that decode to one pattern:
+//   kSegDz   : dZ tiles of row tiles [a0, a0 + an), vocabulary tiles from b0
+//              on; vocabulary outer, rows inner (the rows share each W tile)
+//   kSegDx   : dX tiles of row tiles [a0, a0 + an); hidden tiles outer
+//   kSegDw   : dW tiles of vocabulary tiles from b0 on; hidden tiles inner
+//   kSegDzDw : blocks of (the an dZ tiles of vocabulary tile b0 + c, then the
+//              Nh dW tiles of vocabulary tile b0 + c - lag), so that a dW
+//              tile reads a dZ column written a few blocks earlier (in L2)
+enum SegKind : int { kSegDz = 0, kSegDx = 1, kSegDw = 2, kSegDzDw = 3 };
+
+struct BwdSeg {
+    int start;  // first ticket
+    int kind;
+    int wave;
+    int a0, an;
+    int b0;
+    int lag;
+};
+
+constexpr int MAX_SEGS = 160;
+
+struct BwdParams {
+    int total;       // tickets of this launch
+    int nseg;
+    int M;           // rows covered by the row tensor maps of this launch
+    int V;           // vocabulary size (column mask)
+    int chunk;       // rows of a full wave; wave w starts at row w * chunk
+    int nwaves;
+    int Mt_full;     // 256-row pair tiles of a full wave
+    int Vt;          // 256-column tiles of the padded vocabulary
+    int Nh;          // 256-column tiles of H
+    int KB_h;        // 64-deep K blocks of H (dZ tiles)
+    int KB_v;        // 64-deep K blocks of the padded vocabulary (dX tiles)
+    int deps;        // 1: the fused schedule's dependency counters are live
+    int dw_add0;     // wave 0 adds into dW (accumulate); later waves always add
+    int dx_f32;      // dX boxes in fp32 (else bf16)
+    int dw_bf16;     // dW boxes in bf16 (one wave, no accumulation; else fp32)
+    int ent;         // the entropy term is part of the upstream gradient
+    long long ignore_index;
+    float scale;     // s
+    float scale2;    // s * log2(e)
+    const long long* y;
+    const float* lse;
+    const float* ent_v;
+    const float* g_lp;
+    const float* g_ent;
+    uint32_t* row_dz;   // [Mt_full] dZ tile stores finished per row tile (2 per tile: one per CTA)
+    uint32_t* col_dz;   // [Vt]      ... per vocabulary tile
+    uint32_t* dx_done;  // [Mt_full] dX tiles finished per row tile (2 per tile)
+    uint32_t* dw_done;  // [Vt]      dW tiles finished per vocabulary tile (2 per tile)
+    unsigned long long* ticket;
+    unsigned long long ticket_base;
+    int* err;
+    unsigned long long wait_limit_ns;
+    BwdSeg seg[MAX_SEGS];
+};
+
+struct BUnit {
+    int kind, wave;
+    int mt;  // dZ, dX: row tile of the wave; dW: vocabulary tile
+    int nt;  // dZ: vocabulary tile; dX, dW: hidden tile
+};
+
+__host__ __device__ __forceinline__ BUnit decode_bwd(const BwdParams& p, int u) {
+    int lo = 0, hi = p.nseg - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (p.seg[mid].start <= u)
+            lo = mid;
+        else
+            hi = mid - 1;
+    }
+    const BwdSeg& s = p.seg[lo];
+    const int off = u - s.start;
+    BUnit t;
+    t.wave = s.wave;
+    if (s.kind == kSegDz) {
+        t.kind = kUnitDz;
+        t.nt = s.b0 + off / s.an;
+        t.mt = s.a0 + off % s.an;
+    } else if (s.kind == kSegDx) {
+        t.kind = kUnitDx;
+        t.nt = off / s.an;
+        t.mt = s.a0 + off % s.an;
+    } else if (s.kind == kSegDw) {
+        t.kind = kUnitDw;
+        t.mt = s.b0 + off / p.Nh;
+        t.nt = off % p.Nh;
+    } else {
+        const int blk = s.an + p.Nh;
+        const int c = off / blk;
+        const int r = off - c * blk;
+        if (r < s.an) {
+            t.kind = kUnitDz;
+            t.nt = s.b0 + c;
+            t.mt = s.a0 + r;
+        } else {
+            t.kind = kUnitDw;
+            t.mt = s.b0 + c - s.lag;
+            t.nt = r - s.an;
+        }
+    }
+    return t;
+}
+
+struct WaveInfo {
+    int r0;     // first row of the wave (in the launch's row tensor maps)
+    int rows;   // rows of the wave
+    int Mt;     // 256-row pair tiles
+    int KB_dw;  // 64-deep K blocks of the dW tiles
+};
+
+__device__ __forceinline__ WaveInfo wave_info(const BwdParams& p, int w) {
+    WaveInfo wi;
+    wi.r0 = w * p.chunk;
+    wi.rows = min(p.chunk, p.M - wi.r0);
+    wi.Mt = (wi.rows + PM - 1) / PM;
+    wi.KB_dw = (wi.rows + BK - 1) / BK;
+    return wi;
+}
+
+// Bounded wait until a device-wide counter reaches `target` (acquire).  Gives
+// up when this pair aborts, when another pair has recorded a timeout, or
+// after `limit_ns`.
+__device__ __forceinline__ bool wait_count(const uint32_t* c, uint32_t target, uint64_t limit_ns,
+                                           volatile int* abort_flag, const int* err) {
+    if (ld_acquire_gpu_u32(c) >= target) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+        __nanosleep(64);
+        if (ld_acquire_gpu_u32(c) >= target) return true;
+        if (*abort_flag) return false;
+        if (ld_volatile_s32(err) & ERR_TIMEOUT) return false;
+        if (globaltimer_ns() - t0 > limit_ns) return false;
+    }
+}
+
+// ------------------------------------------------------------ dZ epilogue
+
+// Per-row constants of dZ = p (K1 + K2 acc) + Bc [column == y], with
+// p = 2^(acc s log2e - lse2).  Rows outside the wave and ignored rows get
+// lse2 = +inf (p = 0) and no target column, hence a zero dZ row.
+struct DzRow {
+    long long y;
+    float lse2, K1, K2, Bc;
+};
+
+__device__ __forceinline__ DzRow dz_row(const BwdParams& p, int grow, bool in_wave) {
+    DzRow d{-1, INFINITY, 0.f, 0.f, 0.f};
+    if (!in_wave) return d;
+    const long long yv = p.y[grow];
+    if (yv == p.ignore_index) return d;
+    const float lse_v = p.lse[grow];
+    const float glp = p.g_lp ? p.g_lp[grow] : 0.f;
+    const float gent = (p.ent && p.g_ent) ? p.g_ent[grow] : 0.f;
+    const float spz = p.ent ? (lse_v - p.ent_v[grow]) : 0.f;  // sum_j p_j z_j
+    const float A = p.scale * gent;
+    d.y = yv;
+    d.Bc = p.scale * glp;
+    d.K1 = A * spz - d.Bc;
+    d.K2 = -A * p.scale;
+    d.lse2 = lse_v * LOG2E;
+    if (yv < 0 || yv >= p.V) atomicOr(p.err, ERR_BAD_TARGET);
+    return d;
+}
+
+// One 256-column dZ tile of this thread's row: 4 store boxes of 64 bf16
+// columns; the accumulator is released after its last TMEM read.
+__device__ __forceinline__ void dz_tile_epilogue(StoreRing& ring, uint8_t* smem, int et, int r,
+                                                 uint32_t tbase, int col0, int V, float scale2,
+                                                 const DzRow& d, const CUtensorMap* out, int out_row,
+                                                 uint32_t tempty) {
+#pragma unroll 1
+    for (int b = 0; b < BN / 64; ++b) {
+        const uint32_t box = store_box_acquire(ring, smem, et);
+        uint32_t w[32];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            uint32_t v[32];
+            tmem_ld_32x32b_x32(tbase + b * 64 + h * 32, v);
+            tmem_wait_ld();
+            if (b == BN / 64 - 1 && h == 1) {
+                tc_fence_before();
+                mbar_arrive_cluster(tempty);
+            }
+            const int cbase = col0 + b * 64 + h * 32;
+            float dz[32];
+            {
+                // packed fp32 pairs: p = 2^(acc s log2e - lse2), dz = p (K1 + K2 acc)
+                const uint64_t sc2 = f2_pack(scale2, scale2);
+                const uint64_t nl = f2_pack(-d.lse2, -d.lse2);
+                const uint64_t k1 = f2_pack(d.K1, d.K1), k2 = f2_pack(d.K2, d.K2);
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const uint64_t a = f2_pack(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
+                    float x0, x1;
+                    f2_unpack(f2_fma(a, sc2, nl), x0, x1);
+                    const uint64_t pp = f2_pack(ex2_approx(x0), ex2_approx(x1));
+                    f2_unpack(f2_mul(pp, f2_fma(a, k2, k1)), dz[2 * j], dz[2 * j + 1]);
+                }
+            }
+            const long long tc = d.y - cbase;
+            if (tc >= 0 && tc < 32) {
+                const uint32_t bit = 1u << static_cast<int>(tc);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) dz[j] += ((bit >> j) & 1u) ? d.Bc : 0.f;
+            }
+            const int nv = V - cbase;
+            if (nv < 32) {
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                    if (j >= nv) dz[j] = 0.f;
+            }
+#pragma unroll
+            for (int j = 0; j < 16; ++j) w[h * 16 + j] = pack_bf16x2(dz[2 * j], dz[2 * j + 1]);
+        }
+        stage_row(box, r, w);
+        store_box_release(ring, smem, et, out, col0 + b * 64, out_row, false);
+    }
+}
+
+// One 256-column dX or dW tile of this thread's row: bf16 boxes of 64 columns
+// or fp32 boxes of 32 columns, stored or added.
+__device__ __forceinline__ void gemm_tile_epilogue(StoreRing& ring, uint8_t* smem, int et, int r,
+                                                   uint32_t tbase, bool bf16_out, bool add,
+                                                   const CUtensorMap* out, int col0, int row0,
+                                                   uint32_t tempty) {
+    if (bf16_out) {
+#pragma unroll 1
+        for (int b = 0; b < BN / 64; ++b) {
+            const uint32_t box = store_box_acquire(ring, smem, et);
+            uint32_t w[32];
+            tmem_row64_to_bf16(tbase + b * 64, w);
+            if (b == BN / 64 - 1) {
+                tc_fence_before();
+                mbar_arrive_cluster(tempty);
+            }
+            stage_row(box, r, w);
+            store_box_release(ring, smem, et, out, col0 + b * 64, row0, false);
+        }
+    } else {
+#pragma unroll 1
+        for (int b = 0; b < BN / 32; ++b) {
+            const uint32_t box = store_box_acquire(ring, smem, et);
+            uint32_t w[32];
+            tmem_ld_32x32b_x32(tbase + b * 32, w);
+            tmem_wait_ld();
+            if (b == BN / 32 - 1) {
+                tc_fence_before();
+                mbar_arrive_cluster(tempty);
+            }
+            stage_row(box, r, w);
+            store_box_release(ring, smem, et, out, col0 + b * 32, row0, add);
+        }
+    }
+}
+
+__device__ __forceinline__ int unit_kblocks(const BwdParams& p, const BUnit& t, const WaveInfo& wi) {
+    return t.kind == kUnitDz ? p.KB_h : (t.kind == kUnitDx ? p.KB_v : wi.KB_dw);
+}
+
+// ------------------------------------------------------------------ kernel
+
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    flp_bwd_kernel(const __grid_constant__ CUtensorMap tmXk,    // X, K-major A of dZ tiles (64 x 128 boxes)
+                   const __grid_constant__ CUtensorMap tmWk,    // W, K-major B of dZ tiles (64 x 128)
+                   const __grid_constant__ CUtensorMap tmDz,    // dZ buffer: dZ store boxes and K-major A of dX (64 x 128)
+                   const __grid_constant__ CUtensorMap tmWmn,   // W, MN-major B of dX (64 x 64)
+                   const __grid_constant__ CUtensorMap tmDzMn,  // dZ buffer, MN-major A of dW (64 x 64)
+                   const __grid_constant__ CUtensorMap tmXmn,   // X, MN-major B of dW (64 x 64)
+                   const __grid_constant__ CUtensorMap tmDx,    // dX store boxes
+                   const __grid_constant__ CUtensorMap tmDw,    // dW store / add boxes
+                   const __grid_constant__ BwdParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    const Smem sm = smem_layout(smem_raw);
+    uint8_t* smem = sm.base;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
+    const bool leader = (rank == 0);
+    const int rofs = static_cast<int>(rank) * BM;  // this CTA's rows / columns inside a pair tile
+
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmXk);
+        tma_prefetch_desc(&tmWk);
+        tma_prefetch_desc(&tmDz);
+        tma_prefetch_desc(&tmWmn);
+        tma_prefetch_desc(&tmDzMn);
+        tma_prefetch_desc(&tmXmn);
+        tma_prefetch_desc(&tmDx);
+        tma_prefetch_desc(&tmDw);
+    }
+    const uint32_t tmem_base = pair_prologue(sm, warp);
+    const uint64_t limit = p.wait_limit_ns;
+    volatile int* abort_flag = sm.abort_flag;
+
+    if (warp == 0) {
+        // ------------------------------------------- scheduler + TMA producer
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            // the leader holds the next ticket one unit ahead, so the global
+            // atomic's latency overlaps the current unit's loads
+            unsigned long long next_tk = leader ? atomicAdd(p.ticket, 1ull) : 0ull;
+            // The leader keeps one unit published ahead of the one it loads, so
+            // the peer finds the next unit in its ring when it needs it.
+            int published = 0;
+            bool ended = false;  // the terminating (-1) unit is in the ring
+            for (int it = 0; ok; ++it) {
+                const int slot = it % SCHED_SLOTS;
+                const uint32_t sph = static_cast<uint32_t>(it / SCHED_SLOTS) & 1u;
+                int u;
+                if (leader) {
+                    while (!ended && published < it + 2) {
+                        const int ps = published % SCHED_SLOTS;
+                        const uint32_t pph = static_cast<uint32_t>(published / SCHED_SLOTS) & 1u;
+                        if (!mbar_wait(&sm.sched_empty[ps], pph ^ 1u, limit, abort_flag)) {
+                            ok = false;
+                            break;
+                        }
+                        const unsigned long long tk = next_tk - p.ticket_base;
+                        const int pu = (tk < static_cast<unsigned long long>(p.total)) ? static_cast<int>(tk) : -1;
+                        if (pu >= 0) next_tk = atomicAdd(p.ticket, 1ull);
+                        sm.sched_val[ps] = pu;
+                        st_shared_cluster_u32(mapa_shared(smem_addr(const_cast<int*>(&sm.sched_val[ps])), 1),
+                                              static_cast<uint32_t>(pu));
+                        mbar_arrive(&sm.sched_full[ps]);
+                        mbar_arrive_cluster(mapa_shared(smem_addr(&sm.sched_full[ps]), 1));
+                        ++published;
+                        if (pu < 0) ended = true;
+                    }
+                    if (!ok) break;
+                    u = sm.sched_val[slot];  // written by this thread; not reused before `published` passes it + 4
+                } else {
+                    if (!mbar_wait<true>(&sm.sched_full[slot], sph, limit, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    u = sm.sched_val[slot];
+                    mbar_arrive_cluster(mapa_shared(smem_addr(&sm.sched_empty[slot]), 0));
+                }
+                if (u < 0) break;
+                const BUnit t = decode_bwd(p, u);
+                const WaveInfo wi = wave_info(p, t.wave);
+                if (p.deps && t.kind != kUnitDz) {
+                    // the dZ tiles this unit reads must be stored first
+                    const bool dep_ok =
+                        (t.kind == kUnitDx)
+                            ? wait_count(p.row_dz + t.mt, 2u * static_cast<uint32_t>(p.Vt) * (t.wave + 1),
+                                         limit, abort_flag, p.err)
+                            : wait_count(p.col_dz + t.mt,
+                                         2u * static_cast<uint32_t>(p.Mt_full * t.wave + wi.Mt), limit,
+                                         abort_flag, p.err);
+                    if (!dep_ok) {
+                        ok = false;
+                        break;
+                    }
+                    fence_proxy_async_global();
+                }
+                const int kbn = unit_kblocks(p, t, wi);
+                for (int kb = 0; kb < kbn; ++kb) {
+                    if (!mbar_wait(&sm.empty[stage], phase ^ 1u, limit, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    if (leader) mbar_arrive_expect_tx(&sm.full[stage], PAIR_STAGE_TX);
+                    const uint32_t bar = mapa_shared(smem_addr(&sm.full[stage]), 0);
+                    uint8_t* a_dst = smem + SMEM_A + stage * A_STAGE_BYTES;
+                    uint8_t* b_dst = smem + SMEM_B + stage * B_STAGE_BYTES;
+                    if (t.kind == kUnitDz) {
+                        tma_load_2d_pair(a_dst, &tmXk, kb * BK, wi.r0 + t.mt * PM + rofs, bar);
+                        tma_load_2d_pair(b_dst, &tmWk, kb * BK, t.nt * BN + rofs, bar);
+                    } else if (t.kind == kUnitDx) {
+                        tma_load_2d_pair(a_dst, &tmDz, kb * BK, t.mt * PM + rofs, bar);
+#pragma unroll
+                        for (int j = 0; j < BNH / 64; ++j)
+                            tma_load_2d_pair(b_dst + j * 8192, &tmWmn, t.nt * BN + rofs + j * 64, kb * BK, bar);
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < BM / 64; ++j)
+                            tma_load_2d_pair(a_dst + j * 8192, &tmDzMn, t.mt * PM + rofs + j * 64, kb * BK, bar);
+#pragma unroll
+                        for (int j = 0; j < BNH / 64; ++j)
+                            tma_load_2d_pair(b_dst + j * 8192, &tmXmn, t.nt * BN + rofs + j * 64,
+                                             wi.r0 + kb * BK, bar);
+                    }
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (!ok) {
+                raise_abort(sm, p.err);
+            }
+        }
+    } else if (warp == 1) {
+        // ---------------------------------------------- MMA issuer (leader)
+        if (lane == 0 && leader) {
+            int stage = 0;
+            uint32_t phase = 0;
+            int acc = 0;
+            uint32_t acc_phase = 0;
+            bool ok = true;
+            constexpr uint32_t idesc_kk = idesc_bf16_f32(PM, BN, 0, 0);  // dZ: X and W K-major
+            constexpr uint32_t idesc_km = idesc_bf16_f32(PM, BN, 0, 1);  // dX: dZ K-major, W MN-major
+            constexpr uint32_t idesc_mm = idesc_bf16_f32(PM, BN, 1, 1);  // dW: dZ^T and X MN-major
+            for (int it = 0; ok; ++it) {
+                const int slot = it % SCHED_SLOTS;
+                const uint32_t sph = static_cast<uint32_t>(it / SCHED_SLOTS) & 1u;
+                if (!mbar_wait(&sm.sched_full[slot], sph, limit, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                const int u = sm.sched_val[slot];
+                mbar_arrive(&sm.sched_empty[slot]);
+                if (u < 0) break;
+                const BUnit t = decode_bwd(p, u);
+                const WaveInfo wi = wave_info(p, t.wave);
+                if (!mbar_wait(&sm.tempty[acc], acc_phase ^ 1u, limit, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+                const int kbn = unit_kblocks(p, t, wi);
+                for (int kb = 0; kb < kbn; ++kb) {
+                    if (!mbar_wait(&sm.full[stage], phase, limit, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a_base = smem_addr(smem + SMEM_A + stage * A_STAGE_BYTES);
+                    const uint32_t b_base = smem_addr(smem + SMEM_B + stage * B_STAGE_BYTES);
+                    if (t.kind == kUnitDz) {
+#pragma unroll
+                        for (int k = 0; k < BK / UMMA_K; ++k)
+                            umma_bf16_pair(d_tmem, operand_desc<0>(a_base, k), operand_desc<0>(b_base, k),
+                                           idesc_kk, (kb > 0 || k > 0) ? 1u : 0u);
+                    } else if (t.kind == kUnitDx) {
+#pragma unroll
+                        for (int k = 0; k < BK / UMMA_K; ++k)
+                            umma_bf16_pair(d_tmem, operand_desc<0>(a_base, k), operand_desc<1>(b_base, k),
+                                           idesc_km, (kb > 0 || k > 0) ? 1u : 0u);
+                    } else {
+#pragma unroll
+                        for (int k = 0; k < BK / UMMA_K; ++k)
+                            umma_bf16_pair(d_tmem, operand_desc<1>(a_base, k), operand_desc<1>(b_base, k),
+                                           idesc_mm, (kb > 0 || k > 0) ? 1u : 0u);
+                    }
+                    umma_commit_pair_mc(&sm.empty[stage], PAIR_MASK);  // stage free in both CTAs
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                umma_commit_pair_mc(&sm.tfull[acc], PAIR_MASK);  // accumulator ready in both CTAs
+                acc ^= 1;
+                if (acc == 0) acc_phase ^= 1u;
+            }
+            if (!ok) {
+                raise_abort(sm, p.err);
+            }
+            umma_commit_pair_mc(sm.drain, 0x1);  // every MMA issued so far has completed
+            volatile int no_abort = 0;
+            mbar_wait(sm.drain, 0, limit, &no_abort);
+        }
+    } else {
+        // --------------------------------------------------------- epilogue
+        const int et = threadIdx.x - 64;  // 0..127; thread 0 issues the bulk stores
+        const int q = warp & 3;           // TMEM lane quadrant of this warp
+        const int r = q * 32 + lane;      // accumulator row == TMEM lane
+        const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
+        const uint32_t tempty_leader0 = mapa_shared(smem_addr(&sm.tempty[0]), 0);
+        const uint32_t tempty_leader1 = mapa_shared(smem_addr(&sm.tempty[1]), 0);
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        bool ok = true;
+        StoreRing ring;
+        for (int it = 0;; ++it) {
+            const int slot = it % SCHED_SLOTS;
+            const uint32_t sph = static_cast<uint32_t>(it / SCHED_SLOTS) & 1u;
+            const bool got = mbar_wait<true>(&sm.sched_full[slot], sph, limit, abort_flag);
+            int u = -1;
+            if (got) {
+                u = sm.sched_val[slot];
+                mbar_arrive_cluster(mapa_shared(smem_addr(&sm.sched_empty[slot]), 0));
+            }
+            BUnit t{};
+            WaveInfo wi{};
+            DzRow d{};
+            bool ready = got;
+            if (got && u >= 0) {
+                t = decode_bwd(p, u);
+                wi = wave_info(p, t.wave);
+                if (t.kind == kUnitDz) {
+                    const int lrow = t.mt * PM + rofs + r;  // row inside the wave
+                    d = dz_row(p, wi.r0 + lrow, lrow < wi.rows);
+                }
+                if (p.deps && t.wave > 0 && t.kind != kUnitDx && et == 0) {
+                    // a dZ tile overwrites a buffer slot the previous wave's dX
+                    // and dW tiles read; a dW tile adds after the previous wave's add
+                    const uint32_t tgt = 2u * static_cast<uint32_t>(p.Nh) * t.wave;
+                    bool dep_ok;
+                    if (t.kind == kUnitDz)
+                        dep_ok = wait_count(p.dx_done + t.mt, tgt, limit, abort_flag, p.err) &&
+                                 wait_count(p.dw_done + t.nt, tgt, limit, abort_flag, p.err);
+                    else
+                        dep_ok = wait_count(p.dw_done + t.mt, tgt, limit, abort_flag, p.err);
+                    if (!dep_ok) raise_abort(sm, p.err);  // the others wait on this thread at the store barriers
+                    fence_proxy_async_global();
+                }
+                ready = mbar_wait(&sm.tfull[acc], acc_phase, limit, abort_flag);
+            }
+            // every epilogue thread takes the same branch (the store barriers
+            // below need all of them)
+            if (!named_bar_all(2, EPI_THREADS, ready)) {
+                ok = false;
+                break;
+            }
+            if (u < 0) break;
+            tc_fence_after();
+            const uint32_t tbase = tmem_base + static_cast<uint32_t>(acc * BN) + lane_off;
+            const uint32_t tempty = acc ? tempty_leader1 : tempty_leader0;
+            if (t.kind == kUnitDz) {
+                dz_tile_epilogue(ring, smem, et, r, tbase, t.nt * BN, p.V, p.scale2, d, &tmDz,
+                                 t.mt * PM + rofs, tempty);
+            } else if (t.kind == kUnitDx) {
+                gemm_tile_epilogue(ring, smem, et, r, tbase, !p.dx_f32, false, &tmDx, t.nt * BN,
+                                   wi.r0 + t.mt * PM + rofs, tempty);
+            } else {
+                gemm_tile_epilogue(ring, smem, et, r, tbase, p.dw_bf16 != 0, t.wave > 0 || p.dw_add0,
+                                   &tmDw, t.nt * BN, t.mt * PM + rofs, tempty);
+            }
+            if (p.deps && et == 0 && (t.kind == kUnitDz || p.nwaves > 1)) {
+                // publish the finished tile: its bulk stores complete, then a release
+                bulk_wait_group<0>();
+                fence_proxy_async_global();
+                if (t.kind == kUnitDz) {
+                    red_release_gpu_add_u32(p.row_dz + t.mt, 1u);
+                    red_release_gpu_add_u32(p.col_dz + t.nt, 1u);
+                } else if (t.kind == kUnitDx) {
+                    red_release_gpu_add_u32(p.dx_done + t.mt, 1u);
+                } else {
+                    red_release_gpu_add_u32(p.dw_done + t.mt, 1u);
+                }
+            }
+            acc ^= 1;
+            if (acc == 0) acc_phase ^= 1u;
+        }
+        if (!ok) {
+            raise_abort(sm, p.err);
+        }
+        if (et == 0) bulk_wait_group<0>();
+    }
+
+    pair_epilogue(sm, warp, tmem_base);
+}
+
+}  // namespace flp

@@ -11,10 +11,12 @@
 #include <cstring>
 #include <mutex>
 #include <string>
+#include <vector>
 
 #include <nvtx3/nvToolsExt.h>
 
 #include "flp.h"
+#include "bwd.cuh"
 #include "kernels.cuh"
 #include "loss.cuh"
 
@@ -190,48 +192,86 @@ FwdPlan plan_forward(int64_t M, int64_t H, int64_t V, int compute_entropy, int p
     return f;
 }
 
-struct BwdPlan {
-    int64_t Vp, chunk;
-    size_t off_dz, bytes;
+// Backward workspace: header (error word, ticket) | tile counters of the
+// fused schedule | one wave of bf16 dZ [chunk, Vp].
+struct BwdLayout {
+    int64_t Vp;
+    int Vt, Mt_max;
+    size_t off_cnt, cnt_bytes, off_dz;
 };
 
-BwdPlan plan_backward(int64_t M, int64_t V, int64_t chunk_rows) {
-    BwdPlan b{};
-    b.Vp = cdiv(V, BN) * BN;
+BwdLayout bwd_layout(int64_t M, int64_t V) {
+    BwdLayout L{};
+    L.Vp = cdiv(V, BN) * BN;
+    L.Vt = static_cast<int>(L.Vp / BN);
+    L.Mt_max = static_cast<int>(std::max<int64_t>(1, cdiv(M, PM)));
+    L.off_cnt = kHeaderBytes;
+    L.cnt_bytes = align_up((2 * static_cast<size_t>(L.Mt_max) + 2 * static_cast<size_t>(L.Vt)) * 4, 1024);
+    L.off_dz = L.off_cnt + L.cnt_bytes;
+    return L;
+}
+
+size_t backward_bytes(int64_t M, int64_t V, int64_t chunk_rows) {
+    const BwdLayout L = bwd_layout(M, V);
     const int64_t mr = std::max<int64_t>(BM, cdiv(M, BM) * BM);
     int64_t c = chunk_rows > 0 ? chunk_rows : kDefaultChunkRows;
     c = std::max<int64_t>(BM, cdiv(c, BM) * BM);
-    b.chunk = std::min(c, mr);
-    b.off_dz = kHeaderBytes;
-    b.bytes = b.off_dz + static_cast<size_t>(b.chunk) * b.Vp * 2;
-    return b;
+    c = std::min(c, mr);
+    return L.off_dz + static_cast<size_t>(c) * L.Vp * 2;
+}
+
+// The wave size and schedule a backward call runs with.  Split waves are any
+// multiple of 128 rows; fused waves are all rows (one wave) or a multiple of
+// 256 rows, so no 256-row pair tile straddles two waves.
+struct BwdChoice {
+    flp_bwd_schedule schedule;
+    int64_t chunk, waves;
+};
+
+flp_status choose_backward(int64_t M, int64_t V, size_t workspace_bytes, flp_bwd_schedule want,
+                           BwdChoice* out) {
+    if (want != FLP_BWD_AUTO && want != FLP_BWD_SPLIT && want != FLP_BWD_FUSED)
+        return fail(FLP_ERR_INVALID_ARG, "schedule must be FLP_BWD_AUTO, FLP_BWD_SPLIT or FLP_BWD_FUSED");
+    const BwdLayout L = bwd_layout(M, V);
+    if (workspace_bytes < L.off_dz) return fail(FLP_ERR_WORKSPACE, "backward workspace too small");
+    const int64_t fit = static_cast<int64_t>((workspace_bytes - L.off_dz) / (static_cast<size_t>(L.Vp) * 2));
+    const int64_t mr = std::max<int64_t>(BM, cdiv(M, BM) * BM);
+    const int64_t split_chunk = std::min(mr, fit / BM * BM);
+    if (split_chunk < BM) return fail(FLP_ERR_WORKSPACE, "backward workspace holds fewer than 128 rows of dZ");
+    const int64_t fused_chunk = fit >= mr ? mr : fit / PM * PM;
+    const int64_t fused_waves = fused_chunk > 0 ? cdiv(std::max<int64_t>(M, 1), fused_chunk) : 0;
+    // the fused counters' cumulative targets must fit 32 bits
+    const bool fused_ok = fused_chunk >= PM || fused_chunk == mr;
+    const bool fused_fits = fused_ok && static_cast<double>(L.Vt) * fused_waves * 2.0 < 4.0e9;
+    // On GB300 the split schedule measured faster at every shape tried: the
+    // chip runs at its power cap, and a launch that mixes dZ tiles (exp-heavy
+    // epilogue) with dX / dW tiles runs at a lower clock for the same cycles
+    // per tile, which costs more than the launch boundaries it removes.
+    const flp_bwd_schedule use = want == FLP_BWD_AUTO ? FLP_BWD_SPLIT : want;
+    if (use == FLP_BWD_FUSED && !fused_fits)
+        return fail(FLP_ERR_UNSUPPORTED,
+                    "the fused backward needs a workspace that holds all rows of dZ or at least 256 rows");
+    out->schedule = use;
+    out->chunk = use == FLP_BWD_FUSED ? fused_chunk : split_chunk;
+    out->waves = M > 0 ? cdiv(M, out->chunk) : 0;
+    return FLP_OK;
 }
 
 bool smem_attrs_done(DevInfo* d) { return d->attrs_set; }
 
-template <int kMode, bool kEnt>
-cudaError_t set_smem_attr() {
-    return cudaFuncSetAttribute(flp_tile_kernel<kMode, kEnt>,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_ALLOC);
-}
-
-template <bool kDxF32, bool kDwBf16>
-cudaError_t set_bwd_smem_attr() {
-    return cudaFuncSetAttribute(flp_bwd_gemm_kernel<kDxF32, kDwBf16>,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_ALLOC);
+template <bool kEnt>
+cudaError_t set_fwd_smem_attr() {
+    return cudaFuncSetAttribute(flp_fwd_kernel<kEnt>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                SMEM_ALLOC);
 }
 
 flp_status ensure_attrs(DevInfo* d) {
     if (smem_attrs_done(d)) return FLP_OK;
     cudaError_t e = cudaSuccess;
-    if (e == cudaSuccess) e = set_smem_attr<kFwd, true>();
-    if (e == cudaSuccess) e = set_smem_attr<kFwd, false>();
-    if (e == cudaSuccess) e = set_smem_attr<kDz, true>();
-    if (e == cudaSuccess) e = set_smem_attr<kDz, false>();
-    if (e == cudaSuccess) e = set_bwd_smem_attr<false, false>();
-    if (e == cudaSuccess) e = set_bwd_smem_attr<true, false>();
-    if (e == cudaSuccess) e = set_bwd_smem_attr<false, true>();
-    if (e == cudaSuccess) e = set_bwd_smem_attr<true, true>();
+    if (e == cudaSuccess) e = set_fwd_smem_attr<true>();
+    if (e == cudaSuccess) e = set_fwd_smem_attr<false>();
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(flp_bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_ALLOC);
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
     // How many clusters of two fit at once (SMs that a cluster cannot pair up
     // stay idle); the persistent grids never exceed it.
@@ -247,7 +287,7 @@ flp_status ensure_attrs(DevInfo* d) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int clusters = 0;
-    e = cudaOccupancyMaxActiveClusters(&clusters, flp_tile_kernel<kFwd, true>, &cfg);
+    e = cudaOccupancyMaxActiveClusters(&clusters, flp_fwd_kernel<true>, &cfg);
     if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveClusters");
     if (clusters < 1) return fail(FLP_ERR_UNSUPPORTED, "no CTA pair fits on the device");
     std::lock_guard<std::mutex> lk(g_mu);
@@ -309,10 +349,10 @@ flp_status launch_pairs(void (*kernel)(KArgs...), int grid, cudaStream_t s, cons
     return FLP_OK;
 }
 
-template <int kMode, bool kEnt>
-flp_status launch_tile(int grid, const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& o,
-                       const TileParams& p, cudaStream_t s) {
-    return launch_pairs(flp_tile_kernel<kMode, kEnt>, grid, s, "flp_tile_kernel launch", a, b, o, p);
+template <bool kEnt>
+flp_status launch_fwd(int grid, const CUtensorMap& a, const CUtensorMap& b, const FwdParams& p,
+                      cudaStream_t s) {
+    return launch_pairs(flp_fwd_kernel<kEnt>, grid, s, "flp_fwd_kernel launch", a, b, p);
 }
 
 flp_status common_checks(const void* X, const void* W, const int64_t* targets, int64_t M,
@@ -364,7 +404,7 @@ flp_status flp_workspace_query(int64_t M, int64_t H, int64_t V, int compute_entr
     flp_status st = check_device(&d);
     if (st != FLP_OK) return st;
     if (fwd_bytes) *fwd_bytes = plan_forward(M, H, V, compute_entropy ? 1 : 0, d->pairs).bytes;
-    if (bwd_bytes) *bwd_bytes = plan_backward(M, V, chunk_rows).bytes;
+    if (bwd_bytes) *bwd_bytes = backward_bytes(M, V, chunk_rows);
     return FLP_OK;
 }
 
@@ -400,7 +440,7 @@ flp_status flp_forward(const void* X, const void* W, const int64_t* targets, int
     st = tmap_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, W, H, V, H * 2, BK, BNH);
     if (st != FLP_OK) return st;
 
-    TileParams p{};
+    FwdParams p{};
     p.units = f.units;
     p.Mt = f.Mt;
     p.Nt = f.Vt;
@@ -410,7 +450,6 @@ flp_status flp_forward(const void* X, const void* W, const int64_t* targets, int
     p.KB = static_cast<int>(cdiv(H, BK));
     p.M = static_cast<int>(M);
     p.V = static_cast<int>(V);
-    p.row0 = 0;
     p.ignore_index = ignore_index;
     p.scale = scale;
     p.scale2 = scale * LOG2E;
@@ -423,8 +462,7 @@ flp_status flp_forward(const void* X, const void* W, const int64_t* targets, int
     p.wait_limit_ns = kWaitLimitNs;
     p.debug_stall_after = -1;
     mark(0, s);
-    st = ent ? launch_tile<kFwd, true>(f.grid, tmX, tmW, tmX, p, s)
-             : launch_tile<kFwd, false>(f.grid, tmX, tmW, tmX, p, s);
+    st = ent ? launch_fwd<true>(f.grid, tmX, tmW, p, s) : launch_fwd<false>(f.grid, tmX, tmW, p, s);
     if (st != FLP_OK) return st;
     mark(1, s);
 
@@ -451,12 +489,234 @@ flp_status flp_forward(const void* X, const void* W, const int64_t* targets, int
     return FLP_OK;
 }
 
+flp_status flp_backward_plan(int64_t M, int64_t H, int64_t V, size_t workspace_bytes,
+                             flp_bwd_schedule schedule, int64_t* wave_rows, int64_t* waves,
+                             flp_bwd_schedule* schedule_used) {
+    if (M < 0 || H < 1 || V < 1) return fail(FLP_ERR_INVALID_ARG, "M >= 0, H >= 1 and V >= 1 required");
+    BwdChoice c{};
+    flp_status st = choose_backward(M, V, workspace_bytes, schedule, &c);
+    if (st != FLP_OK) return st;
+    if (wave_rows) *wave_rows = c.chunk;
+    if (waves) *waves = c.waves;
+    if (schedule_used) *schedule_used = c.schedule;
+    return FLP_OK;
+}
+
 flp_status flp_backward(const void* X, const void* W, const int64_t* targets, int64_t M,
                         int64_t H, int64_t V, int64_t ignore_index, float scale,
                         int compute_entropy, const float* lse, const float* entropy,
                         const float* grad_logprob, const float* grad_entropy, void* dX,
                         flp_dtype dX_dtype, void* dW, flp_dtype dW_dtype, int accumulate_dW,
                         void* workspace, size_t workspace_bytes, void* stream) {
+    return flp_backward_ex(X, W, targets, M, H, V, ignore_index, scale, compute_entropy, lse, entropy,
+                           grad_logprob, grad_entropy, dX, dX_dtype, dW, dW_dtype, accumulate_dW,
+                           workspace, workspace_bytes, FLP_BWD_AUTO, stream);
+}
+
+}  // extern "C"
+
+namespace {
+
+// Appends segments to a launch's schedule (BwdParams::seg).
+struct SegList {
+    BwdParams* p;
+    bool overflow = false;
+    void add(int kind, int wave, int a0, int an, int b0, int lag, int64_t count) {
+        if (count <= 0) return;
+        if (p->nseg >= MAX_SEGS || static_cast<int64_t>(p->total) + count > INT_MAX / 2) {
+            overflow = true;
+            return;
+        }
+        BwdSeg& g = p->seg[p->nseg++];
+        g.start = p->total;
+        g.kind = kind;
+        g.wave = wave;
+        g.a0 = a0;
+        g.an = an;
+        g.b0 = b0;
+        g.lag = lag;
+        p->total += static_cast<int>(count);
+    }
+    // dX tiles of row tiles [m0, m0 + gm) in groups of 8 rows (hidden tiles
+    // outer inside a group): the pairs running together share dZ rows and W
+    // columns in L2.
+    void dx_rows(int wave, int m0, int gm, int Nh) {
+        for (int s = m0; s < m0 + gm; s += 8) {
+            const int n = std::min(8, m0 + gm - s);
+            add(kSegDx, wave, s, n, 0, 0, static_cast<int64_t>(n) * Nh);
+        }
+    }
+};
+
+constexpr int kDwLag = 8;  // vocabulary tiles between a dZ column and the dW column paired with it
+
+// The fused schedule of one wave (see bwd.cuh).  Row tiles are swept in
+// groups of GM (vocabulary outer, so each W tile is shared by the group);
+// the dX tiles of a group follow once a few columns of the next group have
+// been handed out; during the last group's sweep, each dZ column is followed
+// by the dW tiles of the column kDwLag tiles earlier; then come a buffer of
+// dW tiles (time for the sweep's last stores), the last group's dX tiles
+// (long: K = padded vocabulary) and the remaining dW tiles (short), enough of
+// them to even out the end of the dX tiles.
+void fused_wave_schedule(SegList& sl, int w, int Mt, int GM, int Vt, int Nh, int pairs, int KB_v,
+                         int KB_dw, bool more_waves) {
+    const int G = static_cast<int>(cdiv(Mt, GM));
+    const int lead = 3 * pairs;  // tickets handed out before a dependent unit
+    for (int g = 0; g < G; ++g) {
+        const int m0 = g * GM, gm = std::min(GM, Mt - m0);
+        int c = 0;
+        if (g > 0) {
+            const int Lc = static_cast<int>(std::min<int64_t>(Vt, cdiv(lead, gm)));
+            sl.add(kSegDz, w, m0, gm, 0, 0, static_cast<int64_t>(gm) * Lc);
+            sl.dx_rows(w, (g - 1) * GM, GM, Nh);
+            c = Lc;
+        }
+        if (g < G - 1) {
+            sl.add(kSegDz, w, m0, gm, c, 0, static_cast<int64_t>(gm) * (Vt - c));
+            continue;
+        }
+        const double tail_units =
+            static_cast<double>(pairs) * KB_v / std::max(1, KB_dw) * (more_waves ? 1.25 : 1.0);
+        const int Ct = static_cast<int>(std::min<double>(Vt, std::ceil(tail_units / Nh)));
+        const int Cb = static_cast<int>(std::min<int64_t>(Vt - Ct, cdiv(lead, Nh)));
+        const int z0 = std::max(c, Ct + Cb + kDwLag);  // first dZ column paired with a dW column
+        if (z0 < Vt) {
+            sl.add(kSegDz, w, m0, gm, c, 0, static_cast<int64_t>(gm) * (z0 - c));
+            sl.add(kSegDzDw, w, m0, gm, z0, kDwLag, static_cast<int64_t>(gm + Nh) * (Vt - z0));
+            sl.add(kSegDw, w, 0, 0, Ct, 0, static_cast<int64_t>(Cb) * Nh);
+            sl.dx_rows(w, m0, gm, Nh);
+            sl.add(kSegDw, w, 0, 0, 0, 0, static_cast<int64_t>(Ct) * Nh);
+            sl.add(kSegDw, w, 0, 0, Ct + Cb, 0, static_cast<int64_t>(z0 - kDwLag - Ct - Cb) * Nh);
+            sl.add(kSegDw, w, 0, 0, Vt - kDwLag, 0, static_cast<int64_t>(kDwLag) * Nh);
+        } else {
+            sl.add(kSegDz, w, m0, gm, c, 0, static_cast<int64_t>(gm) * (Vt - c));
+            sl.add(kSegDw, w, 0, 0, Ct, 0, static_cast<int64_t>(Cb) * Nh);
+            sl.dx_rows(w, m0, gm, Nh);
+            sl.add(kSegDw, w, 0, 0, 0, 0, static_cast<int64_t>(Ct) * Nh);
+            sl.add(kSegDw, w, 0, 0, Ct + Cb, 0, static_cast<int64_t>(Vt - Ct - Cb) * Nh);
+        }
+    }
+}
+
+// One launch of flp_bwd_kernel: the rows its row tensor maps cover and its
+// schedule (the segment fields of BwdParams; the rest is filled per call).
+struct LaunchSpec {
+    int64_t r0, rows, dz_rows;  // X / dX maps over rows [r0, r0 + rows); dZ buffer rows
+    int mark_begin, mark_end;   // phase events recorded around the launch (-1: none)
+    BwdParams p;
+};
+
+// Every launch of a backward call, in stream order.
+flp_status plan_backward_launches(int64_t M, int64_t H, int64_t V, const BwdChoice& ch, int pairs,
+                                  int accumulate_dW, std::vector<LaunchSpec>& out) {
+    out.clear();
+    const int Vt = static_cast<int>(cdiv(V, BN));
+    const int Nh = static_cast<int>(cdiv(H, BN));
+    const int KB_v = Vt * (BN / BK);
+    const int gm_rows = static_cast<int>(std::max<int64_t>(4, 40ll * 1000 * 1000 / (PM * 2 * H)));
+    const int64_t chunk = ch.chunk;
+    if (ch.schedule == FLP_BWD_SPLIT) {
+        for (int64_t r0 = 0; r0 < M; r0 += chunk) {
+            const int64_t rows = std::min(chunk, M - r0);
+            const bool first = (r0 == 0);
+            LaunchSpec a{};
+            a.r0 = r0;
+            a.rows = rows;
+            a.dz_rows = rows;
+            a.p.Vt = Vt;
+            a.p.Nh = Nh;
+            a.p.M = static_cast<int>(rows);
+            a.p.chunk = static_cast<int>(rows);
+            a.p.nwaves = 1;
+            a.p.Mt_full = static_cast<int>(cdiv(rows, PM));
+            a.p.deps = 0;
+            a.p.dw_add0 = (accumulate_dW || r0 > 0) ? 1 : 0;
+            const int Mt = a.p.Mt_full;
+            const int GM = std::min(Mt, gm_rows);
+            LaunchSpec b = a;
+            a.mark_begin = first ? 4 : -1;
+            a.mark_end = first ? 5 : -1;
+            b.mark_begin = first ? 6 : -1;
+            b.mark_end = first ? 7 : -1;
+            SegList dzs{&a.p};
+            for (int m0 = 0; m0 < Mt; m0 += GM) {
+                const int gm = std::min(GM, Mt - m0);
+                dzs.add(kSegDz, 0, m0, gm, 0, 0, static_cast<int64_t>(gm) * Vt);
+            }
+            SegList gl{&b.p};
+            gl.dx_rows(0, 0, Mt, Nh);
+            gl.add(kSegDw, 0, 0, 0, 0, 0, static_cast<int64_t>(Vt) * Nh);
+            if (dzs.overflow || gl.overflow) return fail(FLP_ERR_UNSUPPORTED, "backward schedule too large");
+            out.push_back(a);
+            out.push_back(b);
+        }
+        return FLP_OK;
+    }
+    // fused: every wave in as few launches as the segment table allows (normally one)
+    const int nwaves = static_cast<int>(ch.waves);
+    const int Mt_full = static_cast<int>(cdiv(chunk, PM));
+    const int GM = std::min(Mt_full, gm_rows);
+    int w = 0;
+    while (w < nwaves) {
+        LaunchSpec L{};
+        L.r0 = 0;
+        L.rows = M;
+        L.dz_rows = chunk;
+        L.mark_begin = (w == 0) ? 4 : -1;
+        L.mark_end = -1;
+        L.p.Vt = Vt;
+        L.p.Nh = Nh;
+        L.p.M = static_cast<int>(M);
+        L.p.chunk = static_cast<int>(chunk);
+        L.p.nwaves = nwaves;
+        L.p.Mt_full = Mt_full;
+        L.p.deps = 1;
+        L.p.dw_add0 = accumulate_dW ? 1 : 0;
+        int w_end = w;
+        while (w_end < nwaves) {
+            const int nseg0 = L.p.nseg, total0 = L.p.total;
+            SegList sl{&L.p};
+            const int64_t rows = std::min(chunk, M - static_cast<int64_t>(w_end) * chunk);
+            fused_wave_schedule(sl, w_end, static_cast<int>(cdiv(rows, PM)), GM, Vt, Nh, pairs, KB_v,
+                                static_cast<int>(cdiv(rows, BK)), w_end + 1 < nwaves);
+            if (sl.overflow) {
+                if (w_end == w) return fail(FLP_ERR_UNSUPPORTED, "backward schedule too large");
+                L.p.nseg = nseg0;  // this wave starts the next launch
+                L.p.total = total0;
+                break;
+            }
+            ++w_end;
+        }
+        if (w_end == nwaves) L.mark_end = 5;
+        out.push_back(L);
+        w = w_end;
+    }
+    return FLP_OK;
+}
+
+struct BwdMaps {
+    CUtensorMap Xk, Wk, Dz, Wmn, DzMn, Xmn, Dx, Dw;
+};
+
+flp_status launch_bwd(int pairs, const BwdMaps& m, const BwdParams& p, unsigned long long* ticket_base,
+                      cudaStream_t s) {
+    const int np = std::min(p.total, pairs);
+    *ticket_base += static_cast<unsigned long long>(p.total) + np;  // every CTA pair draws one past the end
+    return launch_pairs(flp_bwd_kernel, 2 * np, s, "flp_bwd_kernel launch", m.Xk, m.Wk, m.Dz, m.Wmn,
+                        m.DzMn, m.Xmn, m.Dx, m.Dw, p);
+}
+
+}  // namespace
+
+extern "C" {
+
+flp_status flp_backward_ex(const void* X, const void* W, const int64_t* targets, int64_t M,
+                           int64_t H, int64_t V, int64_t ignore_index, float scale,
+                           int compute_entropy, const float* lse, const float* entropy,
+                           const float* grad_logprob, const float* grad_entropy, void* dX,
+                           flp_dtype dX_dtype, void* dW, flp_dtype dW_dtype, int accumulate_dW,
+                           void* workspace, size_t workspace_bytes, flp_bwd_schedule schedule,
+                           void* stream) {
     NvtxRange range("flp_backward");
     flp_status st = common_checks(X, W, targets, M, H, V);
     if (st != FLP_OK) return st;
@@ -479,14 +739,11 @@ flp_status flp_backward(const void* X, const void* W, const int64_t* targets, in
     st = check_device(&d);
     if (st != FLP_OK) return st;
     if (M > 0 && (st = check_on_current_device(X, "X")) != FLP_OK) return st;
-    if (!workspace || !aligned16(workspace) || workspace_bytes < kHeaderBytes)
-        return fail(FLP_ERR_WORKSPACE, "backward workspace null, misaligned or too small");
-    // Largest wave (multiple of 128 rows, at most M rounded up) the workspace holds.
-    const int64_t Vp = cdiv(V, BN) * BN;
-    const int64_t fit = static_cast<int64_t>((workspace_bytes - kHeaderBytes) / (static_cast<size_t>(Vp) * 2));
-    const int64_t mr = std::max<int64_t>(BM, cdiv(M, BM) * BM);
-    const int64_t chunk = std::min(mr, fit / BM * BM);
-    if (chunk < BM) return fail(FLP_ERR_WORKSPACE, "backward workspace holds fewer than 128 rows of dZ");
+    if (!workspace || !aligned16(workspace))
+        return fail(FLP_ERR_WORKSPACE, "backward workspace null or misaligned");
+    BwdChoice ch{};
+    if ((st = choose_backward(M, V, workspace_bytes, schedule, &ch)) != FLP_OK) return st;
+    const int64_t chunk = ch.chunk;
     if (dW_dtype == FLP_BF16 && chunk < M)
         return fail(FLP_ERR_UNSUPPORTED,
                     "a bf16 dW needs the backward in one wave (waves accumulate dW in fp32): pass a "
@@ -504,106 +761,124 @@ flp_status flp_backward(const void* X, const void* W, const int64_t* targets, in
         if (!accumulate_dW) FLP_CUDA(cudaMemsetAsync(dW, 0, static_cast<size_t>(V) * H * dw_es, s));
         return FLP_OK;
     }
-    void* dz = ws + kHeaderBytes;
+    const BwdLayout L = bwd_layout(M, V);
+    uint8_t* dz = ws + L.off_dz;
+    const int64_t Vp = L.Vp;
+    const int pairs = d->pairs;
     unsigned long long ticket_base = 0;
 
-    CUtensorMap tmW_k, tmW_mn, tmDW;
-    st = tmap_2d(&tmW_k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, W, H, V, H * 2, BK, BNH);
-    if (st != FLP_OK) return st;
-    st = tmap_2d(&tmW_mn, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, W, H, V, H * 2, 64, 64);
-    if (st != FLP_OK) return st;
+    BwdMaps m{};
+    if ((st = tmap_2d(&m.Wk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, W, H, V, H * 2, BK, BNH)) != FLP_OK) return st;
+    if ((st = tmap_2d(&m.Wmn, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, W, H, V, H * 2, 64, 64)) != FLP_OK) return st;
     if (dW_dtype == FLP_BF16)
-        st = tmap_2d(&tmDW, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dW, H, V, H * 2, 64, BM);
+        st = tmap_2d(&m.Dw, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dW, H, V, H * 2, 64, BM);
     else
-        st = tmap_2d(&tmDW, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, dW, H, V, H * 4, 32, BM);
+        st = tmap_2d(&m.Dw, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, dW, H, V, H * 4, 32, BM);
     if (st != FLP_OK) return st;
 
-    const int Vt = static_cast<int>(Vp / BN);
-    const int Nt_h = static_cast<int>(cdiv(H, BN));
-    const int pairs = d->pairs;
-    const int64_t gm_rows = std::max<int64_t>(4, 40ll * 1000 * 1000 / (PM * 2 * H));
-
-    for (int64_t r0 = 0; r0 < M; r0 += chunk) {
-        NvtxRange wave_range("flp_backward_wave");
-        const int64_t rows = std::min(chunk, M - r0);
+    // Row tensor maps (X, dX, dZ buffer) over `rows` rows starting at global row r0.
+    auto row_maps = [&](int64_t r0, int64_t rows, int64_t dz_rows) -> flp_status {
         const uint8_t* Xc = static_cast<const uint8_t*>(X) + r0 * H * 2;
         uint8_t* dXc = static_cast<uint8_t*>(dX) + r0 * H * dx_es;
-        CUtensorMap tmXk, tmXmn, tmDZk, tmDZmn, tmDZst, tmDX;
-        if ((st = tmap_2d(&tmXk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Xc, H, rows, H * 2, BK, BM)) != FLP_OK) return st;
-        if ((st = tmap_2d(&tmXmn, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Xc, H, rows, H * 2, 64, 64)) != FLP_OK) return st;
-        if ((st = tmap_2d(&tmDZst, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dz, Vp, rows, Vp * 2, 64, BM)) != FLP_OK) return st;
-        if ((st = tmap_2d(&tmDZk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dz, Vp, rows, Vp * 2, BK, BM)) != FLP_OK) return st;
-        if ((st = tmap_2d(&tmDZmn, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dz, Vp, rows, Vp * 2, 64, 64)) != FLP_OK) return st;
+        flp_status e;
+        if ((e = tmap_2d(&m.Xk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Xc, H, rows, H * 2, BK, BM)) != FLP_OK) return e;
+        if ((e = tmap_2d(&m.Xmn, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Xc, H, rows, H * 2, 64, 64)) != FLP_OK) return e;
+        if ((e = tmap_2d(&m.Dz, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dz, Vp, dz_rows, Vp * 2, BK, BM)) != FLP_OK) return e;
+        if ((e = tmap_2d(&m.DzMn, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dz, Vp, dz_rows, Vp * 2, 64, 64)) != FLP_OK) return e;
         if (dX_dtype == FLP_F32)
-            st = tmap_2d(&tmDX, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, dXc, H, rows, H * 4, 32, BM);
-        else
-            st = tmap_2d(&tmDX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dXc, H, rows, H * 2, 64, BM);
-        if (st != FLP_OK) return st;
+            return tmap_2d(&m.Dx, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, dXc, H, rows, H * 4, 32, BM);
+        return tmap_2d(&m.Dx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dXc, H, rows, H * 2, 64, BM);
+    };
 
-        // (1) recompute logits tiles -> bf16 dZ for this wave
-        TileParams p{};
-        p.Mt = static_cast<int>(cdiv(rows, PM));
-        p.Nt = Vt;
-        p.S = Vt;
-        p.tps = 1;
-        p.GM = static_cast<int>(std::min<int64_t>(p.Mt, gm_rows));
-        p.units = p.Mt * p.Nt;
-        p.KB = static_cast<int>(cdiv(H, BK));
-        p.M = static_cast<int>(rows);
-        p.V = static_cast<int>(V);
-        p.row0 = static_cast<int>(r0);
-        p.ignore_index = ignore_index;
-        p.scale = scale;
-        p.scale2 = scale * LOG2E;
-            p.y = reinterpret_cast<const long long*>(targets);
-        p.lse = lse;
-        p.ent = ent ? entropy : nullptr;
-        p.g_lp = grad_logprob;
-        p.g_ent = ent ? grad_entropy : nullptr;
-        p.err = err;
-        p.wait_limit_ns = kWaitLimitNs;
-        p.debug_stall_after = -1;
-        const int grid_dz = 2 * std::min(p.units, pairs);
-        const bool first = (r0 == 0);
-        if (first) mark(4, s);
-        st = ent ? launch_tile<kDz, true>(grid_dz, tmXk, tmW_k, tmDZst, p, s)
-                 : launch_tile<kDz, false>(grid_dz, tmXk, tmW_k, tmDZst, p, s);
-        if (st != FLP_OK) return st;
-        if (first) mark(5, s);
+    std::vector<LaunchSpec> plan;
+    if ((st = plan_backward_launches(M, H, V, ch, pairs, accumulate_dW, plan)) != FLP_OK) return st;
 
-        // (2) dX[wave] = dZ W (K = Vp) and dW (+)= dZ^T X[wave] (K = wave rows),
-        // one persistent launch of CTA pairs; the ticket counter lives in the
-        // zeroed header and every launch consumes units + pairs tickets.
-        BwdParams q{};
-        q.Mt_dx = static_cast<int>(cdiv(rows, PM));
-        q.GM_dx = std::min(q.Mt_dx, 8);
-        q.Nt = Nt_h;
-        q.units_dx = q.Mt_dx * Nt_h;
-        q.units_dw = Vt * Nt_h;
-        q.KB_dx = static_cast<int>(Vp / BK);
-        q.KB_dw = static_cast<int>(cdiv(rows, BK));
-        q.dw_add = (accumulate_dW || r0 > 0) ? 1 : 0;
-        q.ticket = reinterpret_cast<unsigned long long*>(ws + kTicketOffset);
-        q.ticket_base = ticket_base;
-        q.err = err;
-        q.wait_limit_ns = kWaitLimitNs;
-        const int total = q.units_dx + q.units_dw;
-        const int pairs_bw = std::min(total, pairs);
-        ticket_base += static_cast<unsigned long long>(total) + pairs_bw;
-        if (first) mark(6, s);
-        const char* what = "flp_bwd_gemm_kernel launch";
-        const int g = 2 * pairs_bw;
-        if (dX_dtype == FLP_F32)
-            st = (dW_dtype == FLP_BF16)
-                     ? launch_pairs(flp_bwd_gemm_kernel<true, true>, g, s, what, tmDZk, tmW_mn, tmDZmn, tmXmn, tmDX, tmDW, q)
-                     : launch_pairs(flp_bwd_gemm_kernel<true, false>, g, s, what, tmDZk, tmW_mn, tmDZmn, tmXmn, tmDX, tmDW, q);
-        else
-            st = (dW_dtype == FLP_BF16)
-                     ? launch_pairs(flp_bwd_gemm_kernel<false, true>, g, s, what, tmDZk, tmW_mn, tmDZmn, tmXmn, tmDX, tmDW, q)
-                     : launch_pairs(flp_bwd_gemm_kernel<false, false>, g, s, what, tmDZk, tmW_mn, tmDZmn, tmXmn, tmDX, tmDW, q);
-        if (st != FLP_OK) return st;
-        if (first) mark(7, s);
+    BwdParams base{};
+    base.V = static_cast<int>(V);
+    base.KB_h = static_cast<int>(cdiv(H, BK));
+    base.KB_v = static_cast<int>(Vp / BK);
+    base.dx_f32 = dX_dtype == FLP_F32;
+    base.dw_bf16 = dW_dtype == FLP_BF16;
+    base.ent = ent;
+    base.ignore_index = ignore_index;
+    base.scale = scale;
+    base.scale2 = scale * LOG2E;
+    uint32_t* cnt = reinterpret_cast<uint32_t*>(ws + L.off_cnt);
+    base.row_dz = cnt;
+    base.col_dz = cnt + L.Mt_max;
+    base.dx_done = cnt + L.Mt_max + L.Vt;
+    base.dw_done = cnt + 2 * L.Mt_max + L.Vt;
+    base.ticket = reinterpret_cast<unsigned long long*>(ws + kTicketOffset);
+    base.err = err;
+    base.wait_limit_ns = kWaitLimitNs;
+    // the fused schedule's tile counters start at zero and only grow
+    if (ch.schedule == FLP_BWD_FUSED) FLP_CUDA(cudaMemsetAsync(ws + L.off_cnt, 0, L.cnt_bytes, s));
+
+    int64_t mapped_r0 = -1, mapped_rows = -1;
+    for (LaunchSpec& spec : plan) {
+        NvtxRange launch_range("flp_backward_launch");
+        if (spec.r0 != mapped_r0 || spec.rows != mapped_rows) {
+            if ((st = row_maps(spec.r0, spec.rows, spec.dz_rows)) != FLP_OK) return st;
+            mapped_r0 = spec.r0;
+            mapped_rows = spec.rows;
+        }
+        BwdParams& p = spec.p;
+        const int64_t r0 = spec.r0;
+        p.V = base.V;
+        p.KB_h = base.KB_h;
+        p.KB_v = base.KB_v;
+        p.dx_f32 = base.dx_f32;
+        p.dw_bf16 = base.dw_bf16;
+        p.ent = base.ent;
+        p.ignore_index = base.ignore_index;
+        p.scale = base.scale;
+        p.scale2 = base.scale2;
+        p.y = reinterpret_cast<const long long*>(targets) + r0;
+        p.lse = lse + r0;
+        p.ent_v = ent ? entropy + r0 : nullptr;
+        p.g_lp = grad_logprob ? grad_logprob + r0 : nullptr;
+        p.g_ent = (ent && grad_entropy) ? grad_entropy + r0 : nullptr;
+        p.row_dz = base.row_dz;
+        p.col_dz = base.col_dz;
+        p.dx_done = base.dx_done;
+        p.dw_done = base.dw_done;
+        p.ticket = base.ticket;
+        p.ticket_base = ticket_base;
+        p.err = base.err;
+        p.wait_limit_ns = base.wait_limit_ns;
+        if (spec.mark_begin >= 0) mark(spec.mark_begin, s);
+        if ((st = launch_bwd(pairs, m, p, &ticket_base, s)) != FLP_OK) return st;
+        if (spec.mark_end >= 0) mark(spec.mark_end, s);
     }
+    return FLP_OK;
+}
+
+flp_status flp_backward_schedule(int64_t M, int64_t H, int64_t V, size_t workspace_bytes,
+                                 flp_bwd_schedule schedule, int pairs, int32_t* units,
+                                 int64_t capacity, int64_t* count) {
+    if (M < 0 || H < 1 || V < 1 || pairs < 1 || capacity < 0 || !count)
+        return fail(FLP_ERR_INVALID_ARG, "M >= 0, H >= 1, V >= 1, pairs >= 1 and count required");
+    BwdChoice ch{};
+    flp_status st = choose_backward(M, V, workspace_bytes, schedule, &ch);
+    if (st != FLP_OK) return st;
+    std::vector<LaunchSpec> plan;
+    if (M > 0 && (st = plan_backward_launches(M, H, V, ch, pairs, 0, plan)) != FLP_OK) return st;
+    int64_t n = 0;
+    for (size_t li = 0; li < plan.size(); ++li) {
+        const BwdParams& p = plan[li].p;
+        const int w0 = static_cast<int>(plan[li].r0 / std::max<int64_t>(1, ch.chunk));
+        for (int u = 0; u < p.total; ++u, ++n) {
+            if (!units || n >= capacity) continue;
+            const BUnit t = decode_bwd(p, u);
+            int32_t* e = units + 5 * n;
+            e[0] = static_cast<int32_t>(li);
+            e[1] = t.kind;
+            e[2] = t.wave + w0;  // split launches number their one wave 0
+            e[3] = t.mt;
+            e[4] = t.nt;
+        }
+    }
+    *count = n;
     return FLP_OK;
 }
 
@@ -690,7 +965,7 @@ extern "C" flp_status flp_forward_noalloc(const void* X, const void* W, const in
     st = tmap_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, W, H, V, H * 2, BK, BNH);
     if (st != FLP_OK) return st;
 
-    TileParams p{};
+    FwdParams p{};
     p.units = f.units;
     p.Mt = f.Mt;
     p.Nt = f.Vt;
@@ -700,7 +975,6 @@ extern "C" flp_status flp_forward_noalloc(const void* X, const void* W, const in
     p.KB = static_cast<int>(cdiv(H, BK));
     p.M = static_cast<int>(M);
     p.V = static_cast<int>(V);
-    p.row0 = 0;
     p.ignore_index = ignore_index;
     p.scale = scale;
     p.scale2 = scale * LOG2E;
@@ -712,8 +986,7 @@ extern "C" flp_status flp_forward_noalloc(const void* X, const void* W, const in
     p.err = err;
     p.wait_limit_ns = kWaitLimitNs;
     p.debug_stall_after = -1;
-    st = ent ? launch_tile<kFwd, true>(f.grid, tmX, tmW, tmX, p, s)
-             : launch_tile<kFwd, false>(f.grid, tmX, tmW, tmX, p, s);
+    st = ent ? launch_fwd<true>(f.grid, tmX, tmW, p, s) : launch_fwd<false>(f.grid, tmX, tmW, p, s);
     if (st != FLP_OK) return st;
 
     MergeParams mp{};
@@ -765,7 +1038,7 @@ extern "C" flp_status flp_selftest_wait_timeout(void* workspace, size_t workspac
     if (st != FLP_OK) return st;
     st = tmap_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, ws + off_w, H, V, H * 2, BK, BNH);
     if (st != FLP_OK) return st;
-    TileParams p{};
+    FwdParams p{};
     p.units = f.units;
     p.Mt = f.Mt;
     p.Nt = f.Vt;
@@ -786,7 +1059,7 @@ extern "C" flp_status flp_selftest_wait_timeout(void* workspace, size_t workspac
     p.err = reinterpret_cast<int*>(ws);
     p.wait_limit_ns = static_cast<unsigned long long>(wait_limit_ns);
     p.debug_stall_after = stall_after < 0 ? -1 : stall_after;
-    st = launch_tile<kFwd, true>(f.grid, tmX, tmW, tmX, p, s);
+    st = launch_fwd<true>(f.grid, tmX, tmW, p, s);
     if (st != FLP_OK) return st;
     return flp_get_error(workspace, stream);
 }

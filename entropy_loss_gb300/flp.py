@@ -27,11 +27,19 @@ FLP_BF16 = 1
 
 EXPORTS = ("flp_workspace_query", "flp_forward", "flp_backward", "flp_get_error",
            "flp_set_phase_events", "flp_status_string", "flp_last_error_message",
-           "flp_forward_noalloc", "flp_selftest_wait_timeout", "flp_loss")
+           "flp_forward_noalloc", "flp_selftest_wait_timeout", "flp_loss", "flp_backward_ex",
+           "flp_backward_plan", "flp_backward_schedule")
 FLP_LOSS_NLL_MEAN = 1
 FLP_LOSS_CLIPPED_SURROGATE = 2
 SELFTEST_WORKSPACE_BYTES = 1 << 20
 STATIC_SCRATCH_BYTES = 16 << 20
+FLP_BWD_AUTO = 0
+FLP_BWD_SPLIT = 1
+FLP_BWD_FUSED = 2
+SCHEDULES = {"auto": FLP_BWD_AUTO, "split": FLP_BWD_SPLIT, "fused": FLP_BWD_FUSED}
+# phase k of flp_set_phase_events is recorded around events 2k, 2k+1; the
+# backward records phase 2 (split: first wave's dZ launch; fused: the whole
+# backward launch) and, split only, phase 3 (first wave's dX and dW launch)
 PHASES = ("fwd", "merge", "dz", "bwd_gemm")
 
 
@@ -59,6 +67,17 @@ def load(path: str = LIB_PATH):
                                 ctypes.c_size_t, p]
     lib.flp_backward.argtypes = [p, p, p, i64, i64, i64, i64, ctypes.c_float, i32, p, p, p, p, p,
                                  i32, p, i32, i32, p, ctypes.c_size_t, p]
+    lib.flp_backward_ex.argtypes = [p, p, p, i64, i64, i64, i64, ctypes.c_float, i32, p, p, p, p,
+                                    p, i32, p, i32, i32, p, ctypes.c_size_t, i32, p]
+    lib.flp_backward_ex.restype = i32
+    lib.flp_backward_plan.argtypes = [i64, i64, i64, ctypes.c_size_t, i32,
+                                      ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_int64),
+                                      ctypes.POINTER(ctypes.c_int)]
+    lib.flp_backward_plan.restype = i32
+    lib.flp_backward_schedule.argtypes = [i64, i64, i64, ctypes.c_size_t, i32, i32,
+                                          ctypes.POINTER(ctypes.c_int32), i64,
+                                          ctypes.POINTER(ctypes.c_int64)]
+    lib.flp_backward_schedule.restype = i32
     lib.flp_forward_noalloc.argtypes = [p, p, p, i64, i64, i64, i64, ctypes.c_float, i32, p, p, p,
                                         p]
     lib.flp_forward_noalloc.restype = i32
@@ -161,12 +180,43 @@ def forward_noalloc(X, W, y, logprob, lse, entropy=None, *, ignore_index: int = 
     return logprob, lse, entropy
 
 
+def backward_plan(M: int, H: int, V: int, workspace_bytes: int, schedule: str = "auto"):
+    """(wave rows, waves, schedule name) that `backward` runs with for this
+    workspace size; host arithmetic only."""
+    rows = ctypes.c_int64(0)
+    waves = ctypes.c_int64(0)
+    used = ctypes.c_int(0)
+    _check(load().flp_backward_plan(M, H, V, workspace_bytes, SCHEDULES[schedule],
+                                    ctypes.byref(rows), ctypes.byref(waves), ctypes.byref(used)),
+           "flp_backward_plan")
+    name = {v: k for k, v in SCHEDULES.items()}[used.value]
+    return rows.value, waves.value, name
+
+
+def backward_schedule(M: int, H: int, V: int, workspace_bytes: int, schedule: str = "auto",
+                      pairs: int = 76):
+    """The backward's units in ticket order as an int32 array of rows
+    (launch, kind, wave, a, b); kind 0 dZ, 1 dX, 2 dW (see include/flp.h)."""
+    import numpy as np
+    lib = load()
+    n = ctypes.c_int64(0)
+    _check(lib.flp_backward_schedule(M, H, V, workspace_bytes, SCHEDULES[schedule], pairs, None, 0,
+                                     ctypes.byref(n)), "flp_backward_schedule")
+    out = np.zeros((n.value, 5), dtype=np.int32)
+    _check(lib.flp_backward_schedule(M, H, V, workspace_bytes, SCHEDULES[schedule], pairs,
+                                     out.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)), n.value,
+                                     ctypes.byref(n)), "flp_backward_schedule")
+    return out
+
+
 def backward(X, W, y, lse, entropy, grad_logprob, grad_entropy, *, ignore_index: int = -100,
              scale: float = 1.0, compute_entropy: bool = True, dX=None, dW=None,
              dx_dtype=torch.bfloat16, dw_dtype=torch.float32, accumulate_dW: bool = False,
-             workspace=None, stream=None):
+             workspace=None, schedule: str = "auto", stream=None):
     """(dX, dW) for upstream gradients of logprob and entropy (None = zero).
-    dW may be fp32 (accumulated in fp32 across waves) or bf16 (one wave only)."""
+    dW may be fp32 (accumulated in fp32 across waves) or bf16 (one wave only).
+    schedule: "auto", "split" (per wave a dZ launch, then a dX/dW launch) or
+    "fused" (one persistent launch for every wave)."""
     M, H = X.shape
     V = W.shape[0]
     dev = X.device
@@ -178,12 +228,13 @@ def backward(X, W, y, lse, entropy, grad_logprob, grad_entropy, *, ignore_index:
     dwt = FLP_F32 if dW.dtype == torch.float32 else FLP_BF16
     if workspace is None:
         workspace = alloc_workspace(M, H, V, compute_entropy, device=dev)
-    _check(load().flp_backward(_ptr(X), _ptr(W), _ptr(y), M, H, V, ignore_index, float(scale),
-                               int(compute_entropy), _ptr(lse),
-                               _ptr(entropy if compute_entropy else None), _ptr(grad_logprob),
-                               _ptr(grad_entropy if compute_entropy else None), _ptr(dX), dxt,
-                               _ptr(dW), dwt, int(accumulate_dW), _ptr(workspace),
-                               workspace.numel(), _stream(stream)), "flp_backward")
+    _check(load().flp_backward_ex(_ptr(X), _ptr(W), _ptr(y), M, H, V, ignore_index, float(scale),
+                                  int(compute_entropy), _ptr(lse),
+                                  _ptr(entropy if compute_entropy else None), _ptr(grad_logprob),
+                                  _ptr(grad_entropy if compute_entropy else None), _ptr(dX), dxt,
+                                  _ptr(dW), dwt, int(accumulate_dW), _ptr(workspace),
+                                  workspace.numel(), SCHEDULES[schedule], _stream(stream)),
+           "flp_backward_ex")
     return dX, dW
 
 
@@ -252,8 +303,8 @@ class FusedLinearLogprob(torch.autograd.Function):
         g_ent = None if (g_ent is None or not compute_entropy) else g_ent.contiguous().float()
         # a bf16 weight gets its bf16 gradient straight from the epilogue when
         # one backward wave covers every row; otherwise fp32 waves, then a cast
-        M, V = X.shape[0], W.shape[0]
-        wave_rows = (workspace.numel() - 1024) // (((V + 255) // 256) * 256 * 2) // 128 * 128
+        M, H, V = X.shape[0], X.shape[1], W.shape[0]
+        wave_rows, _, _ = backward_plan(M, H, V, workspace.numel())
         direct = W.dtype == torch.bfloat16 and wave_rows >= M
         dX, dW = backward(X, W, y, lse, ent if compute_entropy else None, g_lp, g_ent,
                           ignore_index=ignore_index, scale=scale, compute_entropy=compute_entropy,

@@ -82,10 +82,11 @@ typedef enum { FLP_F32 = 0, FLP_BF16 = 1 } flp_dtype;
  *               results in separate buffers, and so does this library).
  *   bwd_bytes : needed by flp_backward when it processes the rows in waves of
  *               `chunk_rows` rows (chunk_rows <= 0 selects 8192); one wave's
- *               bf16 dZ, [chunk, ceil(V/256)*256], dominates.  The Liger-Kernel
- *               native commit's "Memory" section reports the same kind of
- *               reusable workspace, and pull request 1294's "Kernel design
- *               notes" a reusable per-chunk grad_logits buffer.
+ *               bf16 dZ, [chunk, ceil(V/256)*256], dominates, beside a few
+ *               KiB of tile counters.  The Liger-Kernel native commit's
+ *               "Memory" section reports the same kind of reusable workspace,
+ *               and pull request 1294's "Kernel design notes" a reusable
+ *               per-chunk grad_logits buffer.
  * Either output pointer may be NULL.  The same buffer may serve both calls.
  * Returns FLP_ERR_INVALID_ARG for negative sizes, FLP_ERR_CUDA if the device
  * cannot be queried.
@@ -122,7 +123,8 @@ flp_status flp_forward(const void* X, const void* W, const int64_t* targets, int
  * Rows are processed in waves of as many rows as the workspace holds (at most
  * M, at least 128): each wave recomputes its logits tiles, writes bf16 dZ to
  * the workspace, and runs the dX and dW contractions; dW accumulates in fp32
- * across waves in stream order.
+ * across waves in a fixed order.  flp_backward picks the schedule
+ * (FLP_BWD_AUTO of flp_backward_ex).
  */
 flp_status flp_backward(const void* X, const void* W, const int64_t* targets, int64_t M,
                         int64_t H, int64_t V, int64_t ignore_index, float scale,
@@ -130,6 +132,67 @@ flp_status flp_backward(const void* X, const void* W, const int64_t* targets, in
                         const float* grad_logprob, const float* grad_entropy, void* dX,
                         flp_dtype dX_dtype, void* dW, flp_dtype dW_dtype, int accumulate_dW,
                         void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * How the backward's tiles are scheduled (the Liger-Kernel native commit,
+ * "Implementation > Backward": persistent kernels over token waves).
+ *   FLP_BWD_SPLIT : per wave, one launch of the wave's dZ tiles, then one
+ *                   launch of its dX and dW tiles.  Waves may be any multiple
+ *                   of 128 rows.
+ *   FLP_BWD_FUSED : one persistent launch for every wave: dX and dW tiles
+ *                   start as soon as the dZ tiles they read are stored (tile
+ *                   counters in the workspace), most dW tiles run interleaved
+ *                   with the dZ sweep while their dZ column is still in L2,
+ *                   and a wave's last dW tiles overlap the next wave's dZ
+ *                   tiles.  With more than one wave, waves are multiples of
+ *                   256 rows.
+ *   FLP_BWD_AUTO  : the faster one on GB300, FLP_BWD_SPLIT: at every shape
+ *                   measured the fused launch ran 0.6-2% slower.  The chip
+ *                   runs at its power cap, and mixing dZ tiles (exp-heavy
+ *                   epilogue) with dX / dW tiles lowers the clock while the
+ *                   cycles per tile stay the same.
+ * Both schedules compute every output tile with the same instructions in the
+ * same order: their results are bit-identical.
+ */
+typedef enum { FLP_BWD_AUTO = 0, FLP_BWD_SPLIT = 1, FLP_BWD_FUSED = 2 } flp_bwd_schedule;
+
+/*
+ * flp_backward with an explicit schedule.  FLP_BWD_FUSED returns
+ * FLP_ERR_UNSUPPORTED when the workspace holds fewer than 256 rows of dZ but
+ * not all M rows; other arguments and errors are those of flp_backward.
+ */
+flp_status flp_backward_ex(const void* X, const void* W, const int64_t* targets, int64_t M,
+                           int64_t H, int64_t V, int64_t ignore_index, float scale,
+                           int compute_entropy, const float* lse, const float* entropy,
+                           const float* grad_logprob, const float* grad_entropy, void* dX,
+                           flp_dtype dX_dtype, void* dW, flp_dtype dW_dtype, int accumulate_dW,
+                           void* workspace, size_t workspace_bytes, flp_bwd_schedule schedule,
+                           void* stream);
+
+/*
+ * The wave size, wave count and schedule (FLP_BWD_SPLIT or FLP_BWD_FUSED)
+ * that flp_backward_ex would use for this problem, workspace size and
+ * requested schedule.  Host arithmetic only: touches no device.  Any output
+ * pointer may be NULL.  Returns FLP_ERR_WORKSPACE / FLP_ERR_UNSUPPORTED
+ * exactly when the backward call would.
+ */
+flp_status flp_backward_plan(int64_t M, int64_t H, int64_t V, size_t workspace_bytes,
+                             flp_bwd_schedule schedule, int64_t* wave_rows, int64_t* waves,
+                             flp_bwd_schedule* schedule_used);
+
+/*
+ * The backward's tile schedule, for inspection (a diagnostic; host arithmetic
+ * only, touches no device): the units that flp_backward_ex would hand out, in
+ * ticket order over its launches, for `pairs` resident CTA pairs.  Entry n is
+ * units[5n .. 5n+4] = (launch, kind, wave, a, b), kind 0 = dZ tile (a = row
+ * tile of the wave, b = vocabulary tile), 1 = dX tile (a = row tile, b =
+ * hidden tile), 2 = dW tile (a = vocabulary tile, b = hidden tile); tiles are
+ * 256 x 256.  At most `capacity` entries are written; *count receives the
+ * total.  units may be NULL to query the count.
+ */
+flp_status flp_backward_schedule(int64_t M, int64_t H, int64_t V, size_t workspace_bytes,
+                                 flp_bwd_schedule schedule, int pairs, int32_t* units,
+                                 int64_t capacity, int64_t* count);
 
 /*
  * Forward that allocates nothing and takes no workspace.  The pages have no
@@ -196,7 +259,10 @@ flp_status flp_get_error(const void* workspace, void* stream);
  * before and events[2k+1] immediately after kernel phase k, on the call's
  * stream:
  *   k = 0  forward tile kernel          k = 1  split merge
- *   k = 2  dZ recompute (first wave)    k = 3  dX and dW contractions (first wave)
+ *   k = 2  FLP_BWD_SPLIT: the first wave's dZ launch;
+ *          FLP_BWD_FUSED: the one backward launch (every wave)
+ *   k = 3  FLP_BWD_SPLIT: the first wave's dX and dW launch (not recorded
+ *          by FLP_BWD_FUSED)
  *   k = 4  reserved (never recorded)
  * `events` holds `count` (<= 10) caller-created cudaEvent_t handles passed as
  * void*; NULL entries are skipped.  events == NULL or count == 0 turns the

@@ -56,7 +56,7 @@ def check_grad(got, want, name, rtol=RTOL_GRAD):
 
 
 def run_case(flp, d, *, chunk_rows=0, dx_dtype=torch.bfloat16, check_backward=True, rows=None,
-             dw_rows=None):
+             dw_rows=None, schedule="auto"):
     dev = torch.device("cuda")
     X, W, y = d["X"].to(dev), d["W"].to(dev), d["y"].to(dev)
     M, H = X.shape
@@ -87,7 +87,7 @@ def run_case(flp, d, *, chunk_rows=0, dx_dtype=torch.bfloat16, check_backward=Tr
         g2 = None if g2 is None else g2 * mask
     dX, dW = flp.backward(X, W, y, lse, en, g1.to(dev), None if g2 is None else g2.to(dev),
                           ignore_index=d["ignore_index"], scale=d["scale"], compute_entropy=ent,
-                          dx_dtype=dx_dtype, workspace=ws)
+                          dx_dtype=dx_dtype, workspace=ws, schedule=schedule)
     torch.cuda.synchronize()
     assert flp.get_error(ws) == flp.FLP_OK
     g1n = g1.double().numpy()
@@ -148,6 +148,50 @@ def test_waves_and_ragged_tail(flp):
     # 700 rows in 256-row waves: three waves, the last one ragged; dW accumulates
     # across waves in fp32.
     run_case(flp, case(700, 136, 2100, seed=4), chunk_rows=256)
+
+
+@pytest.mark.parametrize("schedule", ["split", "fused"])
+@pytest.mark.parametrize("M,H,V,chunk", [
+    (700, 136, 2100, 256),   # three 256-row waves, the last ragged
+    (5000, 64, 1000, 512),   # ten waves
+    (1200, 264, 3001, 0),    # one wave
+    (257, 136, 513, 256),    # two waves, the second a single row
+    (2600, 72, 5000, 1024),  # fused: dZ tiles of a wave wait on the previous wave's dX / dW tiles
+])
+def test_schedules_match_oracle(flp, schedule, M, H, V, chunk):
+    run_case(flp, case(M, H, V, seed=22), chunk_rows=chunk, schedule=schedule)
+
+
+@pytest.mark.parametrize("M,H,V,chunk,ent,dx_f32,dw_bf16,acc", [
+    (700, 136, 2100, 256, True, False, False, False),
+    (700, 136, 2100, 256, False, True, False, True),
+    (1200, 264, 3001, 0, True, False, True, False),
+    (2600, 72, 5000, 1024, True, True, False, False),
+    (4096, 512, 16384, 0, True, False, False, False),
+])
+def test_fused_and_split_bit_identical(flp, M, H, V, chunk, ent, dx_f32, dw_bf16, acc):
+    """Both schedules run every output tile with the same instructions in the
+    same K order (and waves in the same order), so dX and dW agree bit for bit."""
+    dev = torch.device("cuda")
+    d = case(M, H, V, seed=23, compute_entropy=ent)
+    X, W, y = d["X"].to(dev), d["W"].to(dev), d["y"].to(dev)
+    g1 = d["g_lp"].to(dev)
+    g2 = d["g_ent"].to(dev) if ent else None
+    ws = flp.alloc_workspace(M, H, V, ent, chunk_rows=chunk, device=dev)
+    lp, lse, en = flp.forward(X, W, y, compute_entropy=ent, workspace=ws)
+    base = torch.randn(V, H, device=dev)
+    outs = {}
+    for sched in ("split", "fused"):
+        dW = (base.clone() if acc else None)
+        dX, dW = flp.backward(X, W, y, lse, en, g1, g2, compute_entropy=ent, workspace=ws,
+                              dx_dtype=torch.float32 if dx_f32 else torch.bfloat16,
+                              dw_dtype=torch.bfloat16 if dw_bf16 else torch.float32, dW=dW,
+                              accumulate_dW=acc, schedule=sched)
+        torch.cuda.synchronize()
+        assert flp.get_error(ws) == flp.FLP_OK
+        outs[sched] = (dX.clone(), dW.clone())
+    assert torch.equal(outs["split"][0], outs["fused"][0])
+    assert torch.equal(outs["split"][1], outs["fused"][1])
 
 
 @pytest.mark.parametrize("M", [4097, 5000])

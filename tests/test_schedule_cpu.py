@@ -1,0 +1,172 @@
+"""The backward's tile schedules, checked on the host (no GPU): every dZ, dX
+and dW tile is handed out exactly once, the split schedule keeps each wave's
+dZ tiles in a launch before its dX/dW launch, and in the fused schedule every
+tile that waits (dX on its dZ rows, dW on its dZ column, a later wave's dZ on
+the previous wave's readers of its buffer slot) only waits on tiles with an
+earlier ticket, which is what rules out a deadlock of the persistent launch."""
+import numpy as np
+import pytest
+
+DZ, DX, DW = 0, 1, 2
+
+
+@pytest.fixture(scope="module")
+def flp():
+    from entropy_loss_gb300 import build, flp
+    build.build()
+    flp.load()
+    return flp
+
+
+def cdiv(a, b):
+    return -(-a // b)
+
+
+def workspace_for(flp, M, H, V, chunk):
+    """Smallest workspace whose split-schedule wave holds `chunk` rows."""
+    lo, hi = 0, 1 << 42
+    while lo < hi:
+        mid = (lo + hi) // 2
+        try:
+            rows = flp.backward_plan(M, H, V, mid, "split")[0]
+        except flp.FlpError:
+            rows = 0
+        if rows >= min(chunk, cdiv(M, 128) * 128):
+            hi = mid
+        else:
+            lo = mid + 1
+    return lo
+
+
+def expected_units(M, H, V, chunk):
+    Vt, Nh = cdiv(V, 256), cdiv(H, 256)
+    out = []
+    for w, r0 in enumerate(range(0, M, chunk)):
+        Mt = cdiv(min(chunk, M - r0), 256)
+        out += [(DZ, w, m, v) for m in range(Mt) for v in range(Vt)]
+        out += [(DX, w, m, h) for m in range(Mt) for h in range(Nh)]
+        out += [(DW, w, v, h) for v in range(Vt) for h in range(Nh)]
+    return sorted(out)
+
+
+SHAPES = [
+    # M, H, V, wave rows, pairs
+    (256, 256, 4096, 8192, 76),
+    (4096, 4096, 131072, 8192, 76),
+    (4096, 4096, 131072, 8192, 1),
+    (4096, 4096, 131072, 2048, 74),
+    (20001, 4096, 128257, 20096, 76),
+    (20001, 4096, 128257, 4096, 76),
+    (32768, 5120, 152064, 8192, 76),
+    (8192, 2048, 151936, 8192, 76),
+    (700, 136, 2100, 256, 2),
+    (300, 200, 3001, 256, 76),
+    (5000, 64, 1000, 512, 5),
+    (1, 8, 1, 128, 76),
+]
+
+
+@pytest.mark.parametrize("schedule", ["split", "fused"])
+@pytest.mark.parametrize("M,H,V,chunk,pairs", SHAPES)
+def test_every_tile_exactly_once(flp, schedule, M, H, V, chunk, pairs):
+    ws = workspace_for(flp, M, H, V, chunk)
+    rows, waves, used = flp.backward_plan(M, H, V, ws, schedule)
+    assert used == schedule
+    u = flp.backward_schedule(M, H, V, ws, schedule, pairs)
+    got = sorted(map(tuple, u[:, 1:].tolist()))
+    assert got == expected_units(M, H, V, rows)
+    assert waves == cdiv(M, rows)
+
+
+@pytest.mark.parametrize("M,H,V,chunk,pairs", SHAPES)
+def test_split_schedule_orders_phases_by_launch(flp, M, H, V, chunk, pairs):
+    ws = workspace_for(flp, M, H, V, chunk)
+    rows, waves, _ = flp.backward_plan(M, H, V, ws, "split")
+    u = flp.backward_schedule(M, H, V, ws, "split", pairs)
+    launch, kind, wave = u[:, 0], u[:, 1], u[:, 2]
+    assert launch.max() + 1 == 2 * waves
+    for li in range(2 * waves):
+        sel = launch == li
+        assert np.all(wave[sel] == li // 2)
+        if li % 2 == 0:
+            assert np.all(kind[sel] == DZ)
+        else:
+            assert np.all(kind[sel] != DZ)
+            # the long dX tiles first, the short dW tiles fill the tail
+            k = kind[sel]
+            assert np.all(np.diff(k) >= 0)
+
+
+@pytest.mark.parametrize("M,H,V,chunk,pairs", SHAPES)
+def test_fused_waits_only_on_earlier_tickets(flp, M, H, V, chunk, pairs):
+    ws = workspace_for(flp, M, H, V, chunk)
+    rows, waves, used = flp.backward_plan(M, H, V, ws, "fused")
+    assert used == "fused"
+    u = flp.backward_schedule(M, H, V, ws, "fused", pairs)
+    kind, wave, a, b = u[:, 1], u[:, 2], u[:, 3], u[:, 4]
+    pos = np.arange(len(u))
+    Vt, Nh, Mt_full = cdiv(V, 256), cdiv(H, 256), cdiv(rows, 256)
+    last_dz_row = np.full((waves, Mt_full), -1)
+    last_dz_col = np.full((waves, Vt), -1)
+    last_dx_row = np.full((waves, Mt_full), -1)
+    last_dw_col = np.full((waves, Vt), -1)
+    s = kind == DZ
+    np.maximum.at(last_dz_row, (wave[s], a[s]), pos[s])
+    np.maximum.at(last_dz_col, (wave[s], b[s]), pos[s])
+    s = kind == DX
+    np.maximum.at(last_dx_row, (wave[s], a[s]), pos[s])
+    s = kind == DW
+    np.maximum.at(last_dw_col, (wave[s], a[s]), pos[s])
+    # dX on every dZ tile of its rows, dW on every dZ tile of its column
+    s = kind == DX
+    assert np.all(last_dz_row[wave[s], a[s]] < pos[s])
+    s = kind == DW
+    assert np.all(last_dz_col[wave[s], a[s]] < pos[s])
+    # a later wave's dZ tile after the previous wave's readers of its slot,
+    # a later wave's dW add after the previous wave's
+    s = (kind == DZ) & (wave > 0)
+    assert np.all(last_dx_row[wave[s] - 1, a[s]] < pos[s])
+    assert np.all(last_dw_col[wave[s] - 1, b[s]] < pos[s])
+    s = (kind == DW) & (wave > 0)
+    assert np.all(last_dw_col[wave[s] - 1, a[s]] < pos[s])
+
+
+def test_fused_interleaves_dw_with_the_dz_sweep(flp):
+    """At the headline shape most dW tiles are handed out during the dZ sweep,
+    a few columns behind it, and the dX tiles are followed by enough dW tiles
+    to even out their end."""
+    M, H, V = 4096, 4096, 131072
+    ws = workspace_for(flp, M, H, V, M)
+    u = flp.backward_schedule(M, H, V, ws, "fused", 76)
+    kind = u[:, 1]
+    last_dz = np.nonzero(kind == DZ)[0].max()
+    first_dx = np.nonzero(kind == DX)[0].min()
+    last_dx = np.nonzero(kind == DX)[0].max()
+    dw_pos = np.nonzero(kind == DW)[0]
+    assert (dw_pos < last_dz).sum() > 0.6 * len(dw_pos)
+    assert first_dx > last_dz
+    assert (dw_pos > last_dx).sum() >= 76 * (131072 // 64) // (4096 // 64)
+
+
+def test_plan_picks_and_rejects(flp):
+    M, H, V = 5000, 64, 1000
+    # a 384-row wave is a multiple of 128 but not 256: fused waves round down
+    ws = workspace_for(flp, M, H, V, 384)
+    assert flp.backward_plan(M, H, V, ws, "split")[0] == 384
+    assert flp.backward_plan(M, H, V, ws, "fused")[0] == 256
+    # auto runs the split schedule (the faster one on GB300)
+    for rows in (384, 512, M):
+        ws = workspace_for(flp, M, H, V, rows)
+        assert flp.backward_plan(M, H, V, ws, "auto") == flp.backward_plan(M, H, V, ws, "split")
+        assert flp.backward_plan(M, H, V, ws, "auto")[2] == "split"
+    ws = workspace_for(flp, M, H, V, M)
+    assert flp.backward_plan(M, H, V, ws, "fused")[:3] == (cdiv(M, 128) * 128, 1, "fused")
+    # 128 rows of dZ: split only
+    ws = workspace_for(flp, M, H, V, 128)
+    assert flp.backward_plan(M, H, V, ws, "auto")[2] == "split"
+    with pytest.raises(flp.FlpError) as e:
+        flp.backward_plan(M, H, V, ws, "fused")
+    assert e.value.status == flp.FLP_ERR_UNSUPPORTED
+    with pytest.raises(flp.FlpError) as e:
+        flp.backward_plan(M, H, V, 1024, "auto")
+    assert e.value.status == flp.FLP_ERR_WORKSPACE
