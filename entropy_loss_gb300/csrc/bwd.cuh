@@ -8,7 +8,9 @@
 //   dW : dW tile (+)= dZ^T X[wave]   (K = wave rows; both operands MN-major)
 // The leader CTA of each pair takes tickets from a global counter and maps
 // them to units through a schedule of segments that the host lays down, then
-// publishes each unit to both CTAs' roles through a shared-memory ring.
+// publishes each unit to both CTAs' roles through a shared-memory ring.  A
+// launch of equal-length units (the split schedule's dZ launch) instead runs
+// a static round-robin that every role computes for itself.
 //
 // Two schedules drive it (the host picks one per call):
 //   split : per row wave, one launch with the wave's dZ tiles, then one launch
@@ -65,6 +67,7 @@ struct BwdParams {
     int KB_h;        // 64-deep K blocks of H (dZ tiles)
     int KB_v;        // 64-deep K blocks of the padded vocabulary (dX tiles)
     int deps;        // 1: the fused schedule's dependency counters are live
+    int static_order;  // 1: pair p runs units p, p + pairs, ... (no tickets, no hand-off ring)
     int dw_add0;     // wave 0 adds into dW (accumulate); later waves always add
     int dx_f32;      // dX boxes in fp32 (else bf16)
     int dw_bf16;     // dW boxes in bf16 (one wave, no accumulation; else fp32)
@@ -312,6 +315,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint32_t rank = cluster_ctarank();
     const bool leader = (rank == 0);
     const int rofs = static_cast<int>(rank) * BM;  // this CTA's rows / columns inside a pair tile
+    const int pair = blockIdx.x >> 1;
+    const int npairs = gridDim.x >> 1;
 
     if (warp == 0 && lane == 0) {
         tma_prefetch_desc(&tmXk);
@@ -335,7 +340,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             bool ok = true;
             // the leader holds the next ticket one unit ahead, so the global
             // atomic's latency overlaps the current unit's loads
-            unsigned long long next_tk = leader ? atomicAdd(p.ticket, 1ull) : 0ull;
+            unsigned long long next_tk = (leader && !p.static_order) ? atomicAdd(p.ticket, 1ull) : 0ull;
             // The leader keeps one unit published ahead of the one it loads, so
             // the peer finds the next unit in its ring when it needs it.
             int published = 0;
@@ -344,7 +349,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 const int slot = it % SCHED_SLOTS;
                 const uint32_t sph = static_cast<uint32_t>(it / SCHED_SLOTS) & 1u;
                 int u;
-                if (leader) {
+                if (p.static_order) {
+                    u = pair + it * npairs;
+                    if (u >= p.total) u = -1;
+                } else if (leader) {
                     while (!ended && published < it + 2) {
                         const int ps = published % SCHED_SLOTS;
                         const uint32_t pph = static_cast<uint32_t>(published / SCHED_SLOTS) & 1u;
@@ -442,13 +450,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             for (int it = 0; ok; ++it) {
                 const int slot = it % SCHED_SLOTS;
                 const uint32_t sph = static_cast<uint32_t>(it / SCHED_SLOTS) & 1u;
-                if (!mbar_wait(&sm.sched_full[slot], sph, limit, abort_flag)) {
-                    ok = false;
-                    break;
+                int u;
+                if (p.static_order) {
+                    u = pair + it * npairs;
+                    if (u >= p.total) break;
+                } else {
+                    if (!mbar_wait(&sm.sched_full[slot], sph, limit, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    u = sm.sched_val[slot];
+                    mbar_arrive(&sm.sched_empty[slot]);
+                    if (u < 0) break;
                 }
-                const int u = sm.sched_val[slot];
-                mbar_arrive(&sm.sched_empty[slot]);
-                if (u < 0) break;
                 const BUnit t = decode_bwd(p, u);
                 const WaveInfo wi = wave_info(p, t.wave);
                 if (!mbar_wait(&sm.tempty[acc], acc_phase ^ 1u, limit, abort_flag)) {
@@ -515,11 +529,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         for (int it = 0;; ++it) {
             const int slot = it % SCHED_SLOTS;
             const uint32_t sph = static_cast<uint32_t>(it / SCHED_SLOTS) & 1u;
-            const bool got = mbar_wait<true>(&sm.sched_full[slot], sph, limit, abort_flag);
+            bool got = true;
             int u = -1;
-            if (got) {
-                u = sm.sched_val[slot];
-                mbar_arrive_cluster(mapa_shared(smem_addr(&sm.sched_empty[slot]), 0));
+            if (p.static_order) {
+                u = pair + it * npairs;
+                if (u >= p.total) u = -1;
+            } else {
+                got = mbar_wait<true>(&sm.sched_full[slot], sph, limit, abort_flag);
+                if (got) {
+                    u = sm.sched_val[slot];
+                    mbar_arrive_cluster(mapa_shared(smem_addr(&sm.sched_empty[slot]), 0));
+                }
             }
             BUnit t{};
             WaveInfo wi{};

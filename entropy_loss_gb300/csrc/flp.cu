@@ -634,6 +634,7 @@ flp_status plan_backward_launches(int64_t M, int64_t H, int64_t V, const BwdChoi
             const int Mt = a.p.Mt_full;
             const int GM = std::min(Mt, gm_rows);
             LaunchSpec b = a;
+            a.p.static_order = 1;  // equal-length dZ tiles: static round-robin
             a.mark_begin = first ? 4 : -1;
             a.mark_end = first ? 5 : -1;
             b.mark_begin = first ? 6 : -1;
@@ -701,7 +702,9 @@ struct BwdMaps {
 flp_status launch_bwd(int pairs, const BwdMaps& m, const BwdParams& p, unsigned long long* ticket_base,
                       cudaStream_t s) {
     const int np = std::min(p.total, pairs);
-    *ticket_base += static_cast<unsigned long long>(p.total) + np;  // every CTA pair draws one past the end
+    // a ticketed launch draws every unit plus one past the end per CTA pair;
+    // a static round-robin draws none
+    if (!p.static_order) *ticket_base += static_cast<unsigned long long>(p.total) + np;
     return launch_pairs(flp_bwd_kernel, 2 * np, s, "flp_bwd_kernel launch", m.Xk, m.Wk, m.Dz, m.Wmn,
                         m.DzMn, m.Xmn, m.Dx, m.Dw, p);
 }
