@@ -1067,6 +1067,82 @@ extern "C" flp_status flp_selftest_wait_timeout(void* workspace, size_t workspac
     return flp_get_error(workspace, stream);
 }
 
+// A fused-schedule launch on a small internal all-zero problem (M = H = V =
+// 256: one tile of each kind) laid out in the workspace.  broken != 0 drops
+// the dZ tiles from the schedule, so the dX tile's dependency wait can never
+// be met and has to give up after wait_limit_ns.
+extern "C" flp_status flp_selftest_dependency_timeout(void* workspace, size_t workspace_bytes,
+                                                      int broken, int64_t wait_limit_ns,
+                                                      void* stream) {
+    if (!workspace || !aligned16(workspace) || workspace_bytes < FLP_SELFTEST_WORKSPACE_BYTES)
+        return fail(FLP_ERR_WORKSPACE, "self-test needs FLP_SELFTEST_WORKSPACE_BYTES of workspace");
+    if (wait_limit_ns <= 0 || wait_limit_ns > 60ll * 1000 * 1000 * 1000)
+        return fail(FLP_ERR_INVALID_ARG, "wait_limit_ns must be in (0, 60 s]");
+    DevInfo* d;
+    flp_status st = check_device(&d);
+    if (st != FLP_OK) return st;
+    constexpr int64_t M = 256, H = 256, V = 256;
+    const BwdLayout L = bwd_layout(M, V);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    const size_t off_x = align_up(L.off_dz + M * L.Vp * 2, 1024);
+    const size_t off_w = off_x + align_up(M * H * 2, 1024);
+    const size_t off_y = off_w + align_up(V * H * 2, 1024);
+    const size_t off_f = off_y + align_up(M * 8, 1024);  // lse, g_lp: fp32 [M] each
+    const size_t off_dx = off_f + align_up(2 * M * 4, 1024);
+    const size_t off_dw = off_dx + align_up(M * H * 2, 1024);
+    const size_t end = off_dw + V * H * 4;
+    if (end > FLP_SELFTEST_WORKSPACE_BYTES)
+        return fail(FLP_ERR_UNSUPPORTED, "self-test layout exceeds its workspace");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    FLP_CUDA(cudaMemsetAsync(ws, 0, end, s));  // header, counters, inputs (zeros), targets (0)
+
+    BwdMaps m{};
+    const void* X = ws + off_x;
+    const void* W = ws + off_w;
+    void* dz = ws + L.off_dz;
+    if ((st = tmap_2d(&m.Xk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, X, H, M, H * 2, BK, BM)) != FLP_OK) return st;
+    if ((st = tmap_2d(&m.Xmn, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, X, H, M, H * 2, 64, 64)) != FLP_OK) return st;
+    if ((st = tmap_2d(&m.Wk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, W, H, V, H * 2, BK, BNH)) != FLP_OK) return st;
+    if ((st = tmap_2d(&m.Wmn, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, W, H, V, H * 2, 64, 64)) != FLP_OK) return st;
+    if ((st = tmap_2d(&m.Dz, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dz, L.Vp, M, L.Vp * 2, BK, BM)) != FLP_OK) return st;
+    if ((st = tmap_2d(&m.DzMn, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dz, L.Vp, M, L.Vp * 2, 64, 64)) != FLP_OK) return st;
+    if ((st = tmap_2d(&m.Dx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, ws + off_dx, H, M, H * 2, 64, BM)) != FLP_OK) return st;
+    if ((st = tmap_2d(&m.Dw, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, ws + off_dw, H, V, H * 4, 32, BM)) != FLP_OK) return st;
+
+    BwdChoice ch{FLP_BWD_FUSED, M, 1};
+    std::vector<LaunchSpec> plan;
+    if ((st = plan_backward_launches(M, H, V, ch, d->pairs, 0, plan)) != FLP_OK) return st;
+    if (plan.size() != 1) return fail(FLP_ERR_UNSUPPORTED, "self-test schedule is not one launch");
+    BwdParams& p = plan[0].p;
+    if (broken) {
+        p.nseg = 0;
+        p.total = 0;
+        SegList sl{&p};
+        sl.add(kSegDx, 0, 0, 1, 0, 0, 1);  // the dX tile alone: its dZ tile never comes
+    }
+    uint32_t* cnt = reinterpret_cast<uint32_t*>(ws + L.off_cnt);
+    p.V = static_cast<int>(V);
+    p.KB_h = static_cast<int>(H / BK);
+    p.KB_v = static_cast<int>(L.Vp / BK);
+    p.ignore_index = -100;
+    p.scale = 1.f;
+    p.scale2 = LOG2E;
+    p.y = reinterpret_cast<const long long*>(ws + off_y);
+    p.lse = reinterpret_cast<const float*>(ws + off_f);
+    p.g_lp = reinterpret_cast<const float*>(ws + off_f + M * 4);
+    p.row_dz = cnt;
+    p.col_dz = cnt + L.Mt_max;
+    p.dx_done = cnt + L.Mt_max + L.Vt;
+    p.dw_done = cnt + 2 * L.Mt_max + L.Vt;
+    p.ticket = reinterpret_cast<unsigned long long*>(ws + kTicketOffset);
+    p.ticket_base = 0;
+    p.err = reinterpret_cast<int*>(ws);
+    p.wait_limit_ns = static_cast<unsigned long long>(wait_limit_ns);
+    unsigned long long tb = 0;
+    if ((st = launch_bwd(d->pairs, m, p, &tb, s)) != FLP_OK) return st;
+    return flp_get_error(workspace, stream);
+}
+
 // ============================================================ loss heads
 
 extern "C" flp_status flp_loss(const float* logprob, const int64_t* targets, int64_t M,

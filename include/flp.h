@@ -288,6 +288,21 @@ flp_status flp_set_phase_events(void* const* events, int count);
 flp_status flp_selftest_wait_timeout(void* workspace, size_t workspace_bytes, int stall_after,
                                      int64_t wait_limit_ns, void* stream);
 
+/*
+ * Self-test of the fused backward schedule's dependency waits (a diagnostic;
+ * the pages have no counterpart).  Runs one fused-schedule launch of the
+ * backward kernel on a small internal all-zero problem (M = H = V = 256)
+ * laid out in `workspace` (at least FLP_SELFTEST_WORKSPACE_BYTES).  With
+ * broken != 0 the schedule holds only the dX tile, whose wait for its dZ tile
+ * can never be met: the wait gives up after wait_limit_ns, the kernel records
+ * FLP_ERR_TIMEOUT, winds down (bounded) and returns; nothing faults and the
+ * context stays usable.  With broken == 0 the full schedule runs normally.
+ * Synchronises `stream` and returns the error word (FLP_ERR_TIMEOUT or
+ * FLP_OK), or an argument / CUDA error.
+ */
+flp_status flp_selftest_dependency_timeout(void* workspace, size_t workspace_bytes, int broken,
+                                           int64_t wait_limit_ns, void* stream);
+
 /* Static description of a status code. */
 const char* flp_status_string(flp_status status);
 

@@ -1,10 +1,11 @@
 """GPU runtime behaviour: bounded waits that run out, CUDA-graph capture.
 
-The wait test makes a kernel wait for data that never comes (its TMA
-producers are told to stop early) and checks that the wait gives up after its
-limit with FLP_ERR_TIMEOUT in the error word, that the kernel returns on its
-own, and that the CUDA context keeps working afterwards.  Nothing faults,
-traps or hangs the GPU.
+The wait tests make a kernel wait for something that never comes (the
+forward's TMA producers are told to stop early; a fused-schedule backward
+launch whose dX tile depends on a dZ tile that is not scheduled) and check
+that the wait gives up after its limit with FLP_ERR_TIMEOUT in the error
+word, that the kernel returns on its own, and that the CUDA context keeps
+working afterwards.  Nothing faults, traps or hangs the GPU.
 """
 import time
 
@@ -47,7 +48,35 @@ def test_bounded_wait_times_out_and_context_survives(flp):
     assert np.abs(en.cpu().double().numpy() - o_en).max() < 2e-3
 
 
-def test_cuda_graph_capture_and_replay(flp):
+def test_fused_dependency_wait_times_out_and_context_survives(flp):
+    limit_ns = 200_000_000
+    assert flp.selftest_dependency_timeout(False, limit_ns) == flp.FLP_OK  # full schedule
+    t0 = time.perf_counter()
+    st = flp.selftest_dependency_timeout(True, limit_ns)
+    elapsed = time.perf_counter() - t0
+    assert st == flp.FLP_ERR_TIMEOUT
+    assert elapsed < 5.0, f"timed-out kernel took {elapsed:.2f} s to return"
+    assert flp.selftest_dependency_timeout(False, limit_ns) == flp.FLP_OK
+    # the context still runs the real fused backward correctly
+    M, H, V = 300, 64, 1000
+    d = inputs.make_inputs(inputs.custom("after_dep", M, H, V, w_std=0.05, seed=43))
+    dev = torch.device("cuda")
+    X, W, y = d["X"].to(dev), d["W"].to(dev), d["y"].to(dev)
+    ws = flp.alloc_workspace(M, H, V, True, chunk_rows=256, device=dev)
+    lp, lse, en = flp.forward(X, W, y, workspace=ws)
+    dX, dW = flp.backward(X, W, y, lse, en, d["g_lp"].to(dev), d["g_ent"].to(dev), workspace=ws,
+                          schedule="fused")
+    torch.cuda.synchronize()
+    assert flp.get_error(ws) == flp.FLP_OK
+    o_dx, o_dw = oracle.backward(inputs.bf16_bits(d["X"]), inputs.bf16_bits(d["W"]), d["y"].numpy(),
+                                 d["g_lp"].double().numpy(), d["g_ent"].double().numpy())
+    for got, want in ((dX, o_dx), (dW, o_dw)):
+        g = got.float().cpu().double().numpy()
+        assert np.linalg.norm(g - want) / np.linalg.norm(want) < 1e-2
+
+
+@pytest.mark.parametrize("schedule", ["split", "fused"])
+def test_cuda_graph_capture_and_replay(flp, schedule):
     dev = torch.device("cuda")
     d = inputs.make_inputs(inputs.custom("graph", 700, 136, 2100, w_std=0.05, ignore_frac=0.1,
                                          seed=42))
@@ -63,7 +92,7 @@ def test_cuda_graph_capture_and_replay(flp):
 
     def step():
         flp.forward(X, W, y, logprob=lp, lse=lse, entropy=en, workspace=ws)
-        flp.backward(X, W, y, lse, en, g1, g2, dX=dX, dW=dW, workspace=ws)
+        flp.backward(X, W, y, lse, en, g1, g2, dX=dX, dW=dW, workspace=ws, schedule=schedule)
 
     step()
     torch.cuda.synchronize()
