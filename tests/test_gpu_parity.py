@@ -168,6 +168,7 @@ def test_schedules_match_oracle(flp, schedule, M, H, V, chunk):
     (1200, 264, 3001, 0, True, False, True, False),
     (2600, 72, 5000, 1024, True, True, False, False),
     (4096, 512, 16384, 0, True, False, False, False),
+    (16384, 64, 1000, 256, True, False, False, True),  # 64 waves: the fused schedule spans two launches
 ])
 def test_fused_and_split_bit_identical(flp, M, H, V, chunk, ent, dx_f32, dw_bf16, acc):
     """Both schedules run every output tile with the same instructions in the

@@ -63,6 +63,7 @@ SHAPES = [
     (300, 200, 3001, 256, 76),
     (5000, 64, 1000, 512, 5),
     (1, 8, 1, 128, 76),
+    (32768, 64, 1000, 256, 76),   # 128 waves: the fused segment table spans three launches
 ]
 
 
@@ -129,6 +130,19 @@ def test_fused_waits_only_on_earlier_tickets(flp, M, H, V, chunk, pairs):
     assert np.all(last_dw_col[wave[s] - 1, b[s]] < pos[s])
     s = (kind == DW) & (wave > 0)
     assert np.all(last_dw_col[wave[s] - 1, a[s]] < pos[s])
+
+
+def test_fused_schedule_splits_into_launches_when_the_table_overflows(flp):
+    """Up to 160 segments fit one launch's table; more waves start another
+    launch, at a wave boundary (a wave never spans two launches)."""
+    M, H, V = 32768, 64, 1000
+    ws = workspace_for(flp, M, H, V, 256)
+    u = flp.backward_schedule(M, H, V, ws, "fused", 76)
+    launch, wave = u[:, 0], u[:, 2]
+    assert launch.max() + 1 == 3
+    assert np.all(np.diff(launch) >= 0)
+    for w in np.unique(wave):
+        assert len(np.unique(launch[wave == w])) == 1
 
 
 def test_fused_interleaves_dw_with_the_dz_sweep(flp):
