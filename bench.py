@@ -397,6 +397,20 @@ def _oracle_sample_time(d, rows, oracle):
     return time.perf_counter() - t0
 
 
+def _calibrate(d, w, oracle, g, n_lo, n_hi):
+    """Fit t(n) = a + b n (a: the fp64 dW buffer and other fixed costs) to two
+    row samples, after one discarded call that pays the first call's page-in
+    and buffer set-up (else the small sample can time slower than the large
+    one).  b is at least half the large sample's mean cost per row."""
+    _oracle_sample_time(d, g.choice(w.M, 1, replace=False), oracle)
+    n_lo, n_hi = min(n_lo, w.M), min(n_hi, w.M)
+    t_lo = _oracle_sample_time(d, g.choice(w.M, n_lo, replace=False), oracle)
+    t_hi = _oracle_sample_time(d, g.choice(w.M, n_hi, replace=False), oracle)
+    b = max((t_hi - t_lo) / max(n_hi - n_lo, 1), 0.5 * t_hi / n_hi, 1e-6)
+    a = max(t_lo - b * n_lo, 0.0)
+    return a, b
+
+
 def cpu_baseline(d, w, seconds):
     """The oracle as it stands, on a seeded row sample: forward of the rows, then
     their backward (logit recompute, dX rows, and their dW contribution over the
@@ -406,13 +420,8 @@ def cpu_baseline(d, w, seconds):
     import oracle
     oracle.build()
     g = np.random.default_rng(0)
-    # two-point calibration t(n) = a + b n (a: the dW buffer and other fixed
-    # costs) on 8 and 64 rows, where the per-row cost has settled
-    n_lo, n_hi = min(8, w.M), min(64, w.M)
-    t_lo = _oracle_sample_time(d, g.choice(w.M, n_lo, replace=False), oracle)
-    t_hi = _oracle_sample_time(d, g.choice(w.M, n_hi, replace=False), oracle)
-    b = max((t_hi - t_lo) / max(n_hi - n_lo, 1), 1e-6)
-    a = max(t_lo - b * n_lo, 0.0)
+    # two-point calibration on 8 and 64 rows, where the per-row cost has settled
+    a, b = _calibrate(d, w, oracle, g, 8, 64)
     n = int(max(1, min(w.M, (seconds - a) / b)))
     rows = g.choice(w.M, n, replace=False)
     t = _oracle_sample_time(d, rows, oracle)
@@ -434,16 +443,15 @@ def run_reference(args, world, rank):
     d = inputs.make_inputs(w)
     g = np.random.default_rng(1)
     steps, warm = args.steps, max(args.warmup, 3)
-    # two-point calibration t(n) = a + b n (a: the fp64 dW buffer and other
-    # fixed costs), then rows per step so the whole run takes about `budget`
-    t1 = _oracle_sample_time(d, g.choice(w.M, 1, replace=False), oracle)
-    t8 = _oracle_sample_time(d, g.choice(w.M, 8, replace=False), oracle)
-    b = max((t8 - t1) / 7.0, 1e-6)
-    a = max(t1 - b, 0.0)
+    # two-point calibration, then rows per step so the whole run takes about `budget`
+    a, b = _calibrate(d, w, oracle, g, 1, 8)
     budget = 150.0  # seconds for the whole run
-    n = int(max(1, min(w.M, (budget / (steps + warm) - a) / b)))
+    per_step = budget / (steps + warm)
+    n = int(max(1, min(w.M, (per_step - a) / b)))
     for _ in range(warm):
-        _oracle_sample_time(d, g.choice(w.M, n, replace=False), oracle)
+        t = _oracle_sample_time(d, g.choice(w.M, n, replace=False), oracle)
+        # the warm-up steps refine the rows per step before any timed step
+        n = int(max(1, min(w.M, n * per_step / max(t, 1e-3))))
     times = [_oracle_sample_time(d, g.choice(w.M, n, replace=False), oracle) for _ in range(steps)]
     t = sum(times)
     value = 8.0 * w.H * w.V * n * steps / t / 1e12
