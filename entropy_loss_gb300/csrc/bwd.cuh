@@ -4,7 +4,10 @@
 //   dZ : the logits tile recomputed (K = H), then
 //        dZ = s [g_lp (onehot - p) + g_ent p (sum_j p_j z_j - z)]  in bf16,
 //        TMA-stored to the wave's dZ buffer (rows of the wave x padded V)
-//   dX : dX[wave] tile = dZ W        (K = padded vocabulary; W read MN-major)
+//   dX : dX[wave] tile = dZ W        (K = padded vocabulary; W read MN-major),
+//        256 x 512 when H allows: two N = 256 MMAs share each A stage, so
+//        an SM loads 48 KiB per 64-deep K step for twice the MACs (the
+//        mainloops are bound by how fast an SM ingests operands from L2)
 //   dW : dW tile (+)= dZ^T X[wave]   (K = wave rows; both operands MN-major)
 // The leader CTA of each pair takes tickets from a global counter and maps
 // them to units through a schedule of segments that the host lays down, then
@@ -41,7 +44,24 @@ enum UnitKind : int { kUnitDz = 0, kUnitDx = 1, kUnitDw = 2 };
 //   kSegDzDw : blocks of (the an dZ tiles of vocabulary tile b0 + c, then the
 //              Nh dW tiles of vocabulary tile b0 + c - lag), so that a dW
 //              tile reads a dZ column written a few blocks earlier (in L2)
-enum SegKind : int { kSegDz = 0, kSegDx = 1, kSegDw = 2, kSegDzDw = 3 };
+//   kSegDx2  : wide (256 x 512) dX tiles of row tiles [a0, a0 + an); 512-column
+//              hidden tiles outer
+enum SegKind : int { kSegDz = 0, kSegDx = 1, kSegDw = 2, kSegDzDw = 3, kSegDx2 = 4 };
+
+// Shared-memory slots.  Normal tiles: STAGES slots of 16 KiB of A and 16 KiB
+// of B (A slots first, then B slots).  Wide dX tiles: STAGES_W slots of 48 KiB
+// (A, then the B halves of the two 256-column sub-tiles), over the same bytes.
+constexpr int STAGES_W = 4;
+constexpr uint32_t STAGE_W_BYTES = A_STAGE_BYTES + 2 * B_STAGE_BYTES;
+constexpr uint32_t PAIR_STAGE_TX_W = 2 * STAGE_W_BYTES;
+static_assert(STAGES_W * STAGE_W_BYTES <= SMEM_STG, "wide slots must fit the pipeline region");
+
+__device__ __forceinline__ uint32_t slot_a(bool wide, int s) {
+    return wide ? s * STAGE_W_BYTES : SMEM_A + s * A_STAGE_BYTES;
+}
+__device__ __forceinline__ uint32_t slot_b(bool wide, int s) {
+    return wide ? s * STAGE_W_BYTES + A_STAGE_BYTES : SMEM_B + s * B_STAGE_BYTES;
+}
 
 struct BwdSeg {
     int start;  // first ticket
@@ -64,6 +84,7 @@ struct BwdParams {
     int Mt_full;     // 256-row pair tiles of a full wave
     int Vt;          // 256-column tiles of the padded vocabulary
     int Nh;          // 256-column tiles of H
+    int Ndx;         // dX tiles per row tile (Nh, or Nh / 2 wide tiles)
     int KB_h;        // 64-deep K blocks of H (dZ tiles)
     int KB_v;        // 64-deep K blocks of the padded vocabulary (dX tiles)
     int deps;        // 1: the fused schedule's dependency counters are live
@@ -82,7 +103,7 @@ struct BwdParams {
     const float* g_ent;
     uint32_t* row_dz;   // [Mt_full] dZ tile stores finished per row tile (2 per tile: one per CTA)
     uint32_t* col_dz;   // [Vt]      ... per vocabulary tile
-    uint32_t* dx_done;  // [Mt_full] dX tiles finished per row tile (2 per tile)
+    uint32_t* dx_done;  // [Mt_full] dX tiles finished per row tile (2 per tile: one per CTA)
     uint32_t* dw_done;  // [Vt]      dW tiles finished per vocabulary tile (2 per tile)
     unsigned long long* ticket;
     unsigned long long ticket_base;
@@ -93,8 +114,9 @@ struct BwdParams {
 
 struct BUnit {
     int kind, wave;
-    int mt;  // dZ, dX: row tile of the wave; dW: vocabulary tile
-    int nt;  // dZ: vocabulary tile; dX, dW: hidden tile
+    int mt;    // dZ, dX: row tile of the wave; dW: vocabulary tile
+    int nt;    // dZ: vocabulary tile; dX, dW: hidden tile (of 512 columns for a wide dX tile)
+    int wide;  // a 256 x 512 dX tile
 };
 
 __host__ __device__ __forceinline__ BUnit decode_bwd(const BwdParams& p, int u) {
@@ -110,6 +132,7 @@ __host__ __device__ __forceinline__ BUnit decode_bwd(const BwdParams& p, int u) 
     const int off = u - s.start;
     BUnit t;
     t.wave = s.wave;
+    t.wide = 0;
     if (s.kind == kSegDz) {
         t.kind = kUnitDz;
         t.nt = s.b0 + off / s.an;
@@ -122,6 +145,11 @@ __host__ __device__ __forceinline__ BUnit decode_bwd(const BwdParams& p, int u) 
         t.kind = kUnitDw;
         t.mt = s.b0 + off / p.Nh;
         t.nt = off % p.Nh;
+    } else if (s.kind == kSegDx2) {
+        t.kind = kUnitDx;
+        t.wide = 1;
+        t.nt = off / s.an;
+        t.mt = s.a0 + off % s.an;
     } else {
         const int blk = s.an + p.Nh;
         const int c = off / blk;
@@ -291,12 +319,31 @@ __device__ __forceinline__ void gemm_tile_epilogue(StoreRing& ring, uint8_t* sme
     }
 }
 
-__device__ __forceinline__ int unit_kblocks(const BwdParams& p, const BUnit& t, const WaveInfo& wi) {
-    return t.kind == kUnitDz ? p.KB_h : (t.kind == kUnitDx ? p.KB_v : wi.KB_dw);
+// The kernel is instantiated per set of tile kinds a launch holds, so a
+// launch of dZ tiles alone (or of dX and dW tiles alone) carries no code for
+// the others.
+constexpr int kHasDz = 1, kHasDx = 2, kHasDw = 4;
+
+struct UnitClass {
+    bool dz, dx, wide;  // dW when neither dz nor dx
+};
+
+template <int kKinds>
+__device__ __forceinline__ UnitClass classify(const BUnit& t) {
+    UnitClass c;
+    c.dz = (kKinds == kHasDz) || ((kKinds & kHasDz) && t.kind == kUnitDz);
+    c.dx = (kKinds == kHasDx) || ((kKinds & kHasDx) && !c.dz && t.kind == kUnitDx);
+    c.wide = (kKinds & kHasDx) && c.dx && t.wide;
+    return c;
+}
+
+__device__ __forceinline__ int unit_kblocks(const BwdParams& p, const UnitClass& c, const WaveInfo& wi) {
+    return c.dz ? p.KB_h : (c.dx ? p.KB_v : wi.KB_dw);
 }
 
 // ------------------------------------------------------------------ kernel
 
+template <int kKinds>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     flp_bwd_kernel(const __grid_constant__ CUtensorMap tmXk,    // X, K-major A of dZ tiles (64 x 128 boxes)
                    const __grid_constant__ CUtensorMap tmWk,    // W, K-major B of dZ tiles (64 x 128)
@@ -336,7 +383,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // ------------------------------------------- scheduler + TMA producer
         if (lane == 0) {
             int stage = 0;
-            uint32_t phase = 0;
+            uint32_t fill_par = 0;  // bit i: parity of the fills of slot i so far
+            bool wide_mode = false; // slot layout in use (normal or wide)
             bool ok = true;
             // the leader holds the next ticket one unit ahead, so the global
             // atomic's latency overlaps the current unit's loads
@@ -383,11 +431,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
                 if (u < 0) break;
                 const BUnit t = decode_bwd(p, u);
+                const UnitClass c = classify<kKinds>(t);
                 const WaveInfo wi = wave_info(p, t.wave);
-                if (p.deps && t.kind != kUnitDz) {
+                if (p.deps && !c.dz) {
                     // the dZ tiles this unit reads must be stored first
                     const bool dep_ok =
-                        (t.kind == kUnitDx)
+                        c.dx
                             ? wait_count(p.row_dz + t.mt, 2u * static_cast<uint32_t>(p.Vt) * (t.wave + 1),
                                          limit, abort_flag, p.err)
                             : wait_count(p.col_dz + t.mt,
@@ -399,24 +448,38 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     }
                     fence_proxy_async_global();
                 }
-                const int kbn = unit_kblocks(p, t, wi);
+                if (c.wide != wide_mode) {
+                    // the two slot layouts overlap: every fill of the old one
+                    // must have been consumed before the new one is written
+                    for (int i = 0; i < STAGES && ok; ++i)
+                        ok = mbar_wait(&sm.empty[i], ((fill_par >> i) & 1u) ^ 1u, limit, abort_flag);
+                    if (!ok) break;
+                    wide_mode = c.wide;
+                    stage = 0;
+                }
+                const int nslots = wide_mode ? STAGES_W : STAGES;
+                const int kbn = unit_kblocks(p, c, wi);
                 for (int kb = 0; kb < kbn; ++kb) {
-                    if (!mbar_wait(&sm.empty[stage], phase ^ 1u, limit, abort_flag)) {
+                    if (!mbar_wait(&sm.empty[stage], ((fill_par >> stage) & 1u) ^ 1u, limit, abort_flag)) {
                         ok = false;
                         break;
                     }
-                    if (leader) mbar_arrive_expect_tx(&sm.full[stage], PAIR_STAGE_TX);
+                    if (leader) mbar_arrive_expect_tx(&sm.full[stage], wide_mode ? PAIR_STAGE_TX_W : PAIR_STAGE_TX);
                     const uint32_t bar = mapa_shared(smem_addr(&sm.full[stage]), 0);
-                    uint8_t* a_dst = smem + SMEM_A + stage * A_STAGE_BYTES;
-                    uint8_t* b_dst = smem + SMEM_B + stage * B_STAGE_BYTES;
-                    if (t.kind == kUnitDz) {
+                    uint8_t* a_dst = smem + slot_a(wide_mode, stage);
+                    uint8_t* b_dst = smem + slot_b(wide_mode, stage);
+                    if (c.dz) {
                         tma_load_2d_pair(a_dst, &tmXk, kb * BK, wi.r0 + t.mt * PM + rofs, bar);
                         tma_load_2d_pair(b_dst, &tmWk, kb * BK, t.nt * BN + rofs, bar);
-                    } else if (t.kind == kUnitDx) {
+                    } else if (c.dx) {
                         tma_load_2d_pair(a_dst, &tmDz, kb * BK, t.mt * PM + rofs, bar);
+                        const int nsub = c.wide ? 2 : 1;
+                        for (int h = 0; h < nsub; ++h) {
 #pragma unroll
-                        for (int j = 0; j < BNH / 64; ++j)
-                            tma_load_2d_pair(b_dst + j * 8192, &tmWmn, t.nt * BN + rofs + j * 64, kb * BK, bar);
+                            for (int j = 0; j < BNH / 64; ++j)
+                                tma_load_2d_pair(b_dst + h * B_STAGE_BYTES + j * 8192, &tmWmn,
+                                                 (t.nt * nsub + h) * BN + rofs + j * 64, kb * BK, bar);
+                        }
                     } else {
 #pragma unroll
                         for (int j = 0; j < BM / 64; ++j)
@@ -426,10 +489,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                             tma_load_2d_pair(b_dst + j * 8192, &tmXmn, t.nt * BN + rofs + j * 64,
                                              wi.r0 + kb * BK, bar);
                     }
-                    if (++stage == STAGES) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
+                    fill_par ^= 1u << stage;
+                    if (++stage == nslots) stage = 0;
                 }
             }
             if (!ok) {
@@ -440,9 +501,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // ---------------------------------------------- MMA issuer (leader)
         if (lane == 0 && leader) {
             int stage = 0;
-            uint32_t phase = 0;
-            int acc = 0;
-            uint32_t acc_phase = 0;
+            uint32_t full_par = 0;   // bit i: parity of the consumptions of slot i so far
+            bool wide_mode = false;  // slot layout in use, switched at the same units as the producer's
+            int acc = 0;             // next accumulator (a wide dX tile takes both, starting here)
+            uint32_t tpar = 0;       // bit a: parity of the uses of accumulator a so far
             bool ok = true;
             constexpr uint32_t idesc_kk = idesc_bf16_f32(PM, BN, 0, 0);  // dZ: X and W K-major
             constexpr uint32_t idesc_km = idesc_bf16_f32(PM, BN, 0, 1);  // dX: dZ K-major, W MN-major
@@ -464,32 +526,46 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     if (u < 0) break;
                 }
                 const BUnit t = decode_bwd(p, u);
+                const UnitClass c = classify<kKinds>(t);
                 const WaveInfo wi = wave_info(p, t.wave);
-                if (!mbar_wait(&sm.tempty[acc], acc_phase ^ 1u, limit, abort_flag)) {
-                    ok = false;
-                    break;
+                if (c.wide != wide_mode) {
+                    wide_mode = c.wide;
+                    stage = 0;
                 }
+                const int nslots = wide_mode ? STAGES_W : STAGES;
+                const int nacc = c.wide ? 2 : 1;
+                for (int h = 0; h < nacc && ok; ++h) {
+                    const int a = acc ^ h;
+                    ok = mbar_wait(&sm.tempty[a], ((tpar >> a) & 1u) ^ 1u, limit, abort_flag);
+                }
+                if (!ok) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
-                const int kbn = unit_kblocks(p, t, wi);
+                const int kbn = unit_kblocks(p, c, wi);
                 for (int kb = 0; kb < kbn; ++kb) {
-                    if (!mbar_wait(&sm.full[stage], phase, limit, abort_flag)) {
+                    if (!mbar_wait(&sm.full[stage], (full_par >> stage) & 1u, limit, abort_flag)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t a_base = smem_addr(smem + SMEM_A + stage * A_STAGE_BYTES);
-                    const uint32_t b_base = smem_addr(smem + SMEM_B + stage * B_STAGE_BYTES);
-                    if (t.kind == kUnitDz) {
+                    const uint32_t a_base = smem_addr(smem + slot_a(wide_mode, stage));
+                    const uint32_t b_base = smem_addr(smem + slot_b(wide_mode, stage));
+                    if (c.dz) {
 #pragma unroll
                         for (int k = 0; k < BK / UMMA_K; ++k)
                             umma_bf16_pair(d_tmem, operand_desc<0>(a_base, k), operand_desc<0>(b_base, k),
                                            idesc_kk, (kb > 0 || k > 0) ? 1u : 0u);
-                    } else if (t.kind == kUnitDx) {
+                    } else if (c.dx) {
+                        // a wide tile: the same A stage against both sub-tiles' B halves,
+                        // into accumulators acc and acc ^ 1
+                        for (int h = 0; h < nacc; ++h) {
+                            const uint32_t d_h = tmem_base + static_cast<uint32_t>((acc ^ h) * BN);
 #pragma unroll
-                        for (int k = 0; k < BK / UMMA_K; ++k)
-                            umma_bf16_pair(d_tmem, operand_desc<0>(a_base, k), operand_desc<1>(b_base, k),
-                                           idesc_km, (kb > 0 || k > 0) ? 1u : 0u);
+                            for (int k = 0; k < BK / UMMA_K; ++k)
+                                umma_bf16_pair(d_h, operand_desc<0>(a_base, k),
+                                               operand_desc<1>(b_base + h * B_STAGE_BYTES, k), idesc_km,
+                                               (kb > 0 || k > 0) ? 1u : 0u);
+                        }
                     } else {
 #pragma unroll
                         for (int k = 0; k < BK / UMMA_K; ++k)
@@ -497,15 +573,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                                            idesc_mm, (kb > 0 || k > 0) ? 1u : 0u);
                     }
                     umma_commit_pair_mc(&sm.empty[stage], PAIR_MASK);  // stage free in both CTAs
-                    if (++stage == STAGES) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
+                    full_par ^= 1u << stage;
+                    if (++stage == nslots) stage = 0;
                 }
                 if (!ok) break;
-                umma_commit_pair_mc(&sm.tfull[acc], PAIR_MASK);  // accumulator ready in both CTAs
-                acc ^= 1;
-                if (acc == 0) acc_phase ^= 1u;
+                for (int h = 0; h < nacc; ++h) {
+                    const int a = acc ^ h;
+                    umma_commit_pair_mc(&sm.tfull[a], PAIR_MASK);  // accumulator ready in both CTAs
+                    tpar ^= 1u << a;
+                }
+                if (nacc == 1) acc ^= 1;
             }
             if (!ok) {
                 raise_abort(sm, p.err);
@@ -522,8 +599,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
         const uint32_t tempty_leader0 = mapa_shared(smem_addr(&sm.tempty[0]), 0);
         const uint32_t tempty_leader1 = mapa_shared(smem_addr(&sm.tempty[1]), 0);
-        int acc = 0;
-        uint32_t acc_phase = 0;
+        int acc = 0;        // next accumulator (a wide dX tile drains acc, then acc ^ 1)
+        uint32_t tpar = 0;  // bit a: parity of the uses of accumulator a so far
         bool ok = true;
         StoreRing ring;
         for (int it = 0;; ++it) {
@@ -542,30 +619,38 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
             }
             BUnit t{};
+            UnitClass c{};
             WaveInfo wi{};
             DzRow d{};
             bool ready = got;
+            int nacc = 1;
             if (got && u >= 0) {
                 t = decode_bwd(p, u);
+                c = classify<kKinds>(t);
                 wi = wave_info(p, t.wave);
-                if (t.kind == kUnitDz) {
+                if (c.dz) {
                     const int lrow = t.mt * PM + rofs + r;  // row inside the wave
                     d = dz_row(p, wi.r0 + lrow, lrow < wi.rows);
                 }
-                if (p.deps && t.wave > 0 && t.kind != kUnitDx && et == 0) {
+                if (p.deps && t.wave > 0 && !c.dx && et == 0) {
                     // a dZ tile overwrites a buffer slot the previous wave's dX
                     // and dW tiles read; a dW tile adds after the previous wave's add
-                    const uint32_t tgt = 2u * static_cast<uint32_t>(p.Nh) * t.wave;
+                    const uint32_t tgt_dx = 2u * static_cast<uint32_t>(p.Ndx) * t.wave;
+                    const uint32_t tgt_dw = 2u * static_cast<uint32_t>(p.Nh) * t.wave;
                     bool dep_ok;
-                    if (t.kind == kUnitDz)
-                        dep_ok = wait_count(p.dx_done + t.mt, tgt, limit, abort_flag, p.err) &&
-                                 wait_count(p.dw_done + t.nt, tgt, limit, abort_flag, p.err);
+                    if (c.dz)
+                        dep_ok = wait_count(p.dx_done + t.mt, tgt_dx, limit, abort_flag, p.err) &&
+                                 wait_count(p.dw_done + t.nt, tgt_dw, limit, abort_flag, p.err);
                     else
-                        dep_ok = wait_count(p.dw_done + t.mt, tgt, limit, abort_flag, p.err);
+                        dep_ok = wait_count(p.dw_done + t.mt, tgt_dw, limit, abort_flag, p.err);
                     if (!dep_ok) raise_abort(sm, p.err);  // the others wait on this thread at the store barriers
                     fence_proxy_async_global();
                 }
-                ready = mbar_wait(&sm.tfull[acc], acc_phase, limit, abort_flag);
+                nacc = c.wide ? 2 : 1;
+                for (int h = 0; h < nacc && ready; ++h) {
+                    const int a = acc ^ h;
+                    ready = mbar_wait(&sm.tfull[a], (tpar >> a) & 1u, limit, abort_flag);
+                }
             }
             // every epilogue thread takes the same branch (the store barriers
             // below need all of them)
@@ -575,33 +660,36 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
             if (u < 0) break;
             tc_fence_after();
-            const uint32_t tbase = tmem_base + static_cast<uint32_t>(acc * BN) + lane_off;
-            const uint32_t tempty = acc ? tempty_leader1 : tempty_leader0;
-            if (t.kind == kUnitDz) {
-                dz_tile_epilogue(ring, smem, et, r, tbase, t.nt * BN, p.V, p.scale2, d, &tmDz,
-                                 t.mt * PM + rofs, tempty);
-            } else if (t.kind == kUnitDx) {
-                gemm_tile_epilogue(ring, smem, et, r, tbase, !p.dx_f32, false, &tmDx, t.nt * BN,
-                                   wi.r0 + t.mt * PM + rofs, tempty);
-            } else {
-                gemm_tile_epilogue(ring, smem, et, r, tbase, p.dw_bf16 != 0, t.wave > 0 || p.dw_add0,
-                                   &tmDw, t.nt * BN, t.mt * PM + rofs, tempty);
+            for (int h = 0; h < nacc; ++h) {
+                const int a = acc ^ h;
+                const uint32_t tbase = tmem_base + static_cast<uint32_t>(a * BN) + lane_off;
+                const uint32_t tempty = a ? tempty_leader1 : tempty_leader0;
+                if (c.dz) {
+                    dz_tile_epilogue(ring, smem, et, r, tbase, t.nt * BN, p.V, p.scale2, d, &tmDz,
+                                     t.mt * PM + rofs, tempty);
+                } else if (c.dx) {
+                    gemm_tile_epilogue(ring, smem, et, r, tbase, !p.dx_f32, false, &tmDx,
+                                       (t.nt * nacc + h) * BN, wi.r0 + t.mt * PM + rofs, tempty);
+                } else {
+                    gemm_tile_epilogue(ring, smem, et, r, tbase, p.dw_bf16 != 0, t.wave > 0 || p.dw_add0,
+                                       &tmDw, t.nt * BN, t.mt * PM + rofs, tempty);
+                }
+                tpar ^= 1u << a;
             }
-            if (p.deps && et == 0 && (t.kind == kUnitDz || p.nwaves > 1)) {
+            if (p.deps && et == 0 && (c.dz || p.nwaves > 1)) {
                 // publish the finished tile: its bulk stores complete, then a release
                 bulk_wait_group<0>();
                 fence_proxy_async_global();
-                if (t.kind == kUnitDz) {
+                if (c.dz) {
                     red_release_gpu_add_u32(p.row_dz + t.mt, 1u);
                     red_release_gpu_add_u32(p.col_dz + t.nt, 1u);
-                } else if (t.kind == kUnitDx) {
+                } else if (c.dx) {
                     red_release_gpu_add_u32(p.dx_done + t.mt, 1u);
                 } else {
                     red_release_gpu_add_u32(p.dw_done + t.mt, 1u);
                 }
             }
-            acc ^= 1;
-            if (acc == 0) acc_phase ^= 1u;
+            if (nacc == 1) acc ^= 1;
         }
         if (!ok) {
             raise_abort(sm, p.err);

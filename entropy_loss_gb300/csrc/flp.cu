@@ -271,7 +271,13 @@ flp_status ensure_attrs(DevInfo* d) {
     if (e == cudaSuccess) e = set_fwd_smem_attr<true>();
     if (e == cudaSuccess) e = set_fwd_smem_attr<false>();
     if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(flp_bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_ALLOC);
+        e = cudaFuncSetAttribute(flp_bwd_kernel<kHasDz>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_ALLOC);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(flp_bwd_kernel<kHasDx | kHasDw>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 SMEM_ALLOC);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(flp_bwd_kernel<kHasDz | kHasDx | kHasDw>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_ALLOC);
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
     // How many clusters of two fit at once (SMs that a cluster cannot pair up
     // stay idle); the persistent grids never exceed it.
@@ -539,13 +545,17 @@ struct SegList {
     }
     // dX tiles of row tiles [m0, m0 + gm) in groups of 8 rows (hidden tiles
     // outer inside a group): the pairs running together share dZ rows and W
-    // columns in L2.
+    // columns in L2.  When H spans an even number of 256-column tiles the
+    // tiles are wide (256 x 512).
     void dx_rows(int wave, int m0, int gm, int Nh) {
+        const bool wide = dx_wide(Nh);
         for (int s = m0; s < m0 + gm; s += 8) {
             const int n = std::min(8, m0 + gm - s);
-            add(kSegDx, wave, s, n, 0, 0, static_cast<int64_t>(n) * Nh);
+            add(wide ? kSegDx2 : kSegDx, wave, s, n, 0, 0, static_cast<int64_t>(n) * dx_per_row(Nh));
         }
     }
+    static bool dx_wide(int Nh) { return Nh % 2 == 0; }
+    static int dx_per_row(int Nh) { return dx_wide(Nh) ? Nh / 2 : Nh; }
 };
 
 constexpr int kDwLag = 8;  // vocabulary tiles between a dZ column and the dW column paired with it
@@ -575,8 +585,9 @@ void fused_wave_schedule(SegList& sl, int w, int Mt, int GM, int Vt, int Nh, int
             sl.add(kSegDz, w, m0, gm, c, 0, static_cast<int64_t>(gm) * (Vt - c));
             continue;
         }
+        const int dx_len = KB_v * (SegList::dx_wide(Nh) ? 2 : 1);  // K blocks x sub-tiles of a dX tile
         const double tail_units =
-            static_cast<double>(pairs) * KB_v / std::max(1, KB_dw) * (more_waves ? 1.25 : 1.0);
+            static_cast<double>(pairs) * dx_len / std::max(1, KB_dw) * (more_waves ? 1.25 : 1.0);
         const int Ct = static_cast<int>(std::min<double>(Vt, std::ceil(tail_units / Nh)));
         const int Cb = static_cast<int>(std::min<int64_t>(Vt - Ct, cdiv(lead, Nh)));
         const int z0 = std::max(c, Ct + Cb + kDwLag);  // first dZ column paired with a dW column
@@ -625,6 +636,7 @@ flp_status plan_backward_launches(int64_t M, int64_t H, int64_t V, const BwdChoi
             a.dz_rows = rows;
             a.p.Vt = Vt;
             a.p.Nh = Nh;
+            a.p.Ndx = SegList::dx_per_row(Nh);
             a.p.M = static_cast<int>(rows);
             a.p.chunk = static_cast<int>(rows);
             a.p.nwaves = 1;
@@ -667,6 +679,7 @@ flp_status plan_backward_launches(int64_t M, int64_t H, int64_t V, const BwdChoi
         L.mark_end = -1;
         L.p.Vt = Vt;
         L.p.Nh = Nh;
+        L.p.Ndx = SegList::dx_per_row(Nh);
         L.p.M = static_cast<int>(M);
         L.p.chunk = static_cast<int>(chunk);
         L.p.nwaves = nwaves;
@@ -699,14 +712,39 @@ struct BwdMaps {
     CUtensorMap Xk, Wk, Dz, Wmn, DzMn, Xmn, Dx, Dw;
 };
 
+// The tile kinds (kHasDz | kHasDx | kHasDw) a launch's segments hold.
+int launch_kinds(const BwdParams& p) {
+    int k = 0;
+    for (int i = 0; i < p.nseg; ++i) {
+        switch (p.seg[i].kind) {
+            case kSegDz: k |= kHasDz; break;
+            case kSegDx:
+            case kSegDx2: k |= kHasDx; break;
+            case kSegDw: k |= kHasDw; break;
+            default: k |= kHasDz | kHasDw; break;
+        }
+    }
+    return k;
+}
+
 flp_status launch_bwd(int pairs, const BwdMaps& m, const BwdParams& p, unsigned long long* ticket_base,
                       cudaStream_t s) {
     const int np = std::min(p.total, pairs);
     // a ticketed launch draws every unit plus one past the end per CTA pair;
     // a static round-robin draws none
     if (!p.static_order) *ticket_base += static_cast<unsigned long long>(p.total) + np;
-    return launch_pairs(flp_bwd_kernel, 2 * np, s, "flp_bwd_kernel launch", m.Xk, m.Wk, m.Dz, m.Wmn,
-                        m.DzMn, m.Xmn, m.Dx, m.Dw, p);
+    const char* what = "flp_bwd_kernel launch";
+    switch (launch_kinds(p)) {
+        case kHasDz:
+            return launch_pairs(flp_bwd_kernel<kHasDz>, 2 * np, s, what, m.Xk, m.Wk, m.Dz, m.Wmn, m.DzMn,
+                                m.Xmn, m.Dx, m.Dw, p);
+        case kHasDx | kHasDw:
+            return launch_pairs(flp_bwd_kernel<kHasDx | kHasDw>, 2 * np, s, what, m.Xk, m.Wk, m.Dz, m.Wmn,
+                                m.DzMn, m.Xmn, m.Dx, m.Dw, p);
+        default:
+            return launch_pairs(flp_bwd_kernel<kHasDz | kHasDx | kHasDw>, 2 * np, s, what, m.Xk, m.Wk, m.Dz,
+                                m.Wmn, m.DzMn, m.Xmn, m.Dx, m.Dw, p);
+    }
 }
 
 }  // namespace
@@ -875,7 +913,7 @@ flp_status flp_backward_schedule(int64_t M, int64_t H, int64_t V, size_t workspa
             const BUnit t = decode_bwd(p, u);
             int32_t* e = units + 5 * n;
             e[0] = static_cast<int32_t>(li);
-            e[1] = t.kind;
+            e[1] = t.wide ? 3 : t.kind;
             e[2] = t.wave + w0;  // split launches number their one wave 0
             e[3] = t.mt;
             e[4] = t.nt;

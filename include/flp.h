@@ -186,8 +186,9 @@ flp_status flp_backward_plan(int64_t M, int64_t H, int64_t V, size_t workspace_b
  * ticket order over its launches, for `pairs` resident CTA pairs.  Entry n is
  * units[5n .. 5n+4] = (launch, kind, wave, a, b), kind 0 = dZ tile (a = row
  * tile of the wave, b = vocabulary tile), 1 = dX tile (a = row tile, b =
- * hidden tile), 2 = dW tile (a = vocabulary tile, b = hidden tile); tiles are
- * 256 x 256.  At most `capacity` entries are written; *count receives the
+ * hidden tile), 2 = dW tile (a = vocabulary tile, b = hidden tile), 3 = wide
+ * dX tile (a = row tile, b = 512-column hidden tile: the hidden tiles 2b and
+ * 2b + 1); tiles are 256 x 256 except the wide ones.  At most `capacity` entries are written; *count receives the
  * total.  units may be NULL to query the count.
  */
 flp_status flp_backward_schedule(int64_t M, int64_t H, int64_t V, size_t workspace_bytes,
