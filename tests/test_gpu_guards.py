@@ -37,8 +37,16 @@ class Guarded:
             torch.all(self.raw[GUARD + self.n:] == PATTERN))
 
 
-@pytest.mark.parametrize("M,H,V,chunk", [(300, 200, 3001, 128), (257, 72, 513, 0), (700, 136, 2100, 256)])
-def test_no_writes_outside_buffers(flp, M, H, V, chunk):
+@pytest.mark.parametrize("schedule", ["split", "fused"])
+@pytest.mark.parametrize("M,H,V,chunk", [
+    (300, 200, 3001, 128), (257, 72, 513, 0), (700, 136, 2100, 256),
+    # wide dX tiles whose second 256-column half is mostly (H = 264) or
+    # entirely inside H (H = 512), over several waves
+    (300, 264, 3001, 256), (700, 512, 2100, 256),
+])
+def test_no_writes_outside_buffers(flp, M, H, V, chunk, schedule):
+    if schedule == "fused" and chunk == 128:
+        pytest.skip("fused waves are multiples of 256 rows")
     dev = torch.device("cuda")
     d = inputs.make_inputs(inputs.custom("guard", M, H, V, w_std=0.05, ignore_frac=0.1, seed=61))
     X, W, y = d["X"].to(dev), d["W"].to(dev), d["y"].to(dev)
@@ -51,10 +59,11 @@ def test_no_writes_outside_buffers(flp, M, H, V, chunk):
     flp.forward(X, W, y, logprob=lp, lse=lse, entropy=en, workspace=ws)
     dX = dx_g.view(torch.bfloat16, (M, H))
     dW = dw_g.view(torch.float32, (V, H))
-    flp.backward(X, W, y, lse, en, d["g_lp"].to(dev), d["g_ent"].to(dev), dX=dX, dW=dW, workspace=ws)
+    flp.backward(X, W, y, lse, en, d["g_lp"].to(dev), d["g_ent"].to(dev), dX=dX, dW=dW, workspace=ws,
+                 schedule=schedule)
     dXf = dxf_g.view(torch.float32, (M, H))
     flp.backward(X, W, y, lse, en, d["g_lp"].to(dev), d["g_ent"].to(dev), dX=dXf, dW=dW,
-                 accumulate_dW=True, workspace=ws)
+                 accumulate_dW=True, workspace=ws, schedule=schedule)
     torch.cuda.synchronize()
     assert flp.get_error(ws) == flp.FLP_OK
     for name, g in (("workspace", ws_g), ("logprob", lp_g), ("lse", lse_g), ("entropy", en_g),

@@ -157,6 +157,7 @@ def test_waves_and_ragged_tail(flp):
     (1200, 264, 3001, 0),    # one wave
     (257, 136, 513, 256),    # two waves, the second a single row
     (2600, 72, 5000, 1024),  # fused: dZ tiles of a wave wait on the previous wave's dX / dW tiles
+    (2600, 512, 5000, 1024), # wide (256 x 512) dX tiles in three waves
 ])
 def test_schedules_match_oracle(flp, schedule, M, H, V, chunk):
     run_case(flp, case(M, H, V, seed=22), chunk_rows=chunk, schedule=schedule)
@@ -169,6 +170,8 @@ def test_schedules_match_oracle(flp, schedule, M, H, V, chunk):
     (2600, 72, 5000, 1024, True, True, False, False),
     (4096, 512, 16384, 0, True, False, False, False),
     (16384, 64, 1000, 256, True, False, False, True),  # 64 waves: the fused schedule spans two launches
+    (2600, 512, 5000, 1024, True, True, False, True),   # wide dX tiles, three waves, slot layouts switching
+    (1000, 1024, 3000, 512, False, False, False, False),
 ])
 def test_fused_and_split_bit_identical(flp, M, H, V, chunk, ent, dx_f32, dw_bf16, acc):
     """Both schedules run every output tile with the same instructions in the
