@@ -51,7 +51,7 @@ def parse():
     ap.add_argument("--chunk-rows", type=int, default=0,
                     help="backward wave size in rows (0: the library default); smaller waves "
                          "trade speed for a smaller workspace")
-    ap.add_argument("--schedule", default="auto", choices=["auto", "split", "fused"],
+    ap.add_argument("--schedule", default="auto", choices=["auto", "split", "fused", "vsplit"],
                     help="backward tile schedule: per-wave dZ then dX/dW launches (split) or one "
                          "persistent launch (fused); auto lets the library pick")
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
@@ -217,6 +217,8 @@ def run_ours(args, world, rank, local):
     # phases the library records (events 2k, 2k+1 around phase k)
     if sched == "fused":
         phase_names = {"fwd": 0, "merge": 1, "bwd": 2}
+    elif sched == "vsplit":
+        phase_names = {"fwd": 0, "merge": 1, "bwd_dz": 2, "bwd_gemm": 3}  # first vocabulary chunk
     else:
         phase_names = {"fwd": 0, "merge": 1, "bwd_dz": 2, "bwd_gemm": 3}
 
@@ -269,10 +271,15 @@ def run_ours(args, world, rank, local):
     # roofline of the dominant kernel launch (largest mean duration among the phases)
     peaks, peak_src = load_peaks()
     first_wave = min(M, wave_rows)
+    share = first_wave * 1.0  # rows x vocabulary share covered by the first wave's (or chunk's) launches
+    if sched == "vsplit":
+        units = flp.backward_schedule(M, H, V, ws.numel(), "vsplit", 76)
+        Vt, Mt = -(-V // 256), -(-M // 256)
+        share = M * (int((units[:, 0] == 0).sum()) // Mt) / Vt
     phase_flops = {"fwd": 2.0 * M * H * V, "merge": 0.0,
                    "bwd": 6.0 * M * H * V,                       # fused: every wave in one launch
-                   "bwd_dz": 2.0 * first_wave * H * V,           # split: the first wave's launches
-                   "bwd_gemm": 4.0 * first_wave * H * V}
+                   "bwd_dz": 2.0 * share * H * V,                # split / vsplit: the first wave's / chunk's launches
+                   "bwd_gemm": 4.0 * share * H * V}
     dom = max(phase_ms, key=lambda n: phase_ms[n])
     achieved = phase_flops[dom] / (phase_ms[dom] * 1e-3) / 1e12
     peak = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))

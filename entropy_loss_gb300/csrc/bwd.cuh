@@ -1,6 +1,7 @@
 // bwd.cuh - the backward of the fused linear log-prob head on CTA pairs.
 //
-// One persistent kernel whose units are 256 x 256 pair tiles of three kinds:
+// One persistent kernel (instantiated per set of tile kinds a launch holds)
+// whose units are pair tiles of three kinds, 256 x 256 unless noted:
 //   dZ : the logits tile recomputed (K = H), then
 //        dZ = s [g_lp (onehot - p) + g_ent p (sum_j p_j z_j - z)]  in bf16,
 //        TMA-stored to the wave's dZ buffer (rows of the wave x padded V)
@@ -19,6 +20,9 @@
 //   split : per row wave, one launch with the wave's dZ tiles, then one launch
 //           with its dX tiles (long, first) and dW tiles (short, filling the
 //           tail); the kernel boundary orders the phases.
+//   vsplit: all rows in one wave and the vocabulary in chunks: per chunk the
+//           same two launches over the chunk's columns; dX accumulates over
+//           the chunks in fp32, each dW tile is written once (K = all rows).
 //   fused : every wave in one launch.  A dX tile waits until the dZ tiles of
 //           its rows are stored, a dW tile until those of its vocabulary
 //           column are; from the second wave on, a dZ tile waits until the
@@ -86,10 +90,12 @@ struct BwdParams {
     int Nh;          // 256-column tiles of H
     int Ndx;         // dX tiles per row tile (Nh, or Nh / 2 wide tiles)
     int KB_h;        // 64-deep K blocks of H (dZ tiles)
-    int KB_v;        // 64-deep K blocks of the padded vocabulary (dX tiles)
+    int KB_v;        // 64-deep K blocks of the padded vocabulary chunk (dX tiles)
     int deps;        // 1: the fused schedule's dependency counters are live
     int static_order;  // 1: pair p runs units p, p + pairs, ... (no tickets, no hand-off ring)
     int dw_add0;     // wave 0 adds into dW (accumulate); later waves always add
+    int vt0;         // first vocabulary tile of this launch's vocabulary chunk (0: all of V)
+    int dx_add;      // dX tiles add into their (fp32) output (later vocabulary chunks)
     int dx_f32;      // dX boxes in fp32 (else bf16)
     int dw_bf16;     // dW boxes in bf16 (one wave, no accumulation; else fp32)
     int ent;         // the entropy term is part of the upstream gradient
@@ -231,9 +237,9 @@ __device__ __forceinline__ DzRow dz_row(const BwdParams& p, int grow, bool in_wa
 // One 256-column dZ tile of this thread's row: 4 store boxes of 64 bf16
 // columns; the accumulator is released after its last TMEM read.
 __device__ __forceinline__ void dz_tile_epilogue(StoreRing& ring, uint8_t* smem, int et, int r,
-                                                 uint32_t tbase, int col0, int V, float scale2,
-                                                 const DzRow& d, const CUtensorMap* out, int out_row,
-                                                 uint32_t tempty) {
+                                                 uint32_t tbase, int col0, int out_col0, int V,
+                                                 float scale2, const DzRow& d, const CUtensorMap* out,
+                                                 int out_row, uint32_t tempty) {
 #pragma unroll 1
     for (int b = 0; b < BN / 64; ++b) {
         const uint32_t box = store_box_acquire(ring, smem, et);
@@ -279,7 +285,7 @@ __device__ __forceinline__ void dz_tile_epilogue(StoreRing& ring, uint8_t* smem,
             for (int j = 0; j < 16; ++j) w[h * 16 + j] = pack_bf16x2(dz[2 * j], dz[2 * j + 1]);
         }
         stage_row(box, r, w);
-        store_box_release(ring, smem, et, out, col0 + b * 64, out_row, false);
+        store_box_release(ring, smem, et, out, out_col0 + b * 64, out_row, false);
     }
 }
 
@@ -472,18 +478,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         tma_load_2d_pair(a_dst, &tmXk, kb * BK, wi.r0 + t.mt * PM + rofs, bar);
                         tma_load_2d_pair(b_dst, &tmWk, kb * BK, t.nt * BN + rofs, bar);
                     } else if (c.dx) {
-                        tma_load_2d_pair(a_dst, &tmDz, kb * BK, t.mt * PM + rofs, bar);
+                        tma_load_2d_pair(a_dst, &tmDz, kb * BK, t.mt * PM + rofs, bar);  // chunk column kb * BK
                         const int nsub = c.wide ? 2 : 1;
                         for (int h = 0; h < nsub; ++h) {
 #pragma unroll
                             for (int j = 0; j < BNH / 64; ++j)
                                 tma_load_2d_pair(b_dst + h * B_STAGE_BYTES + j * 8192, &tmWmn,
-                                                 (t.nt * nsub + h) * BN + rofs + j * 64, kb * BK, bar);
+                                                 (t.nt * nsub + h) * BN + rofs + j * 64, p.vt0 * BN + kb * BK,
+                                                 bar);
                         }
                     } else {
 #pragma unroll
                         for (int j = 0; j < BM / 64; ++j)
-                            tma_load_2d_pair(a_dst + j * 8192, &tmDzMn, t.mt * PM + rofs + j * 64, kb * BK, bar);
+                            tma_load_2d_pair(a_dst + j * 8192, &tmDzMn, (t.mt - p.vt0) * PM + rofs + j * 64,
+                                             kb * BK, bar);
 #pragma unroll
                         for (int j = 0; j < BNH / 64; ++j)
                             tma_load_2d_pair(b_dst + j * 8192, &tmXmn, t.nt * BN + rofs + j * 64,
@@ -665,10 +673,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 const uint32_t tbase = tmem_base + static_cast<uint32_t>(a * BN) + lane_off;
                 const uint32_t tempty = a ? tempty_leader1 : tempty_leader0;
                 if (c.dz) {
-                    dz_tile_epilogue(ring, smem, et, r, tbase, t.nt * BN, p.V, p.scale2, d, &tmDz,
-                                     t.mt * PM + rofs, tempty);
+                    dz_tile_epilogue(ring, smem, et, r, tbase, t.nt * BN, (t.nt - p.vt0) * BN, p.V,
+                                     p.scale2, d, &tmDz, t.mt * PM + rofs, tempty);
                 } else if (c.dx) {
-                    gemm_tile_epilogue(ring, smem, et, r, tbase, !p.dx_f32, false, &tmDx,
+                    gemm_tile_epilogue(ring, smem, et, r, tbase, !p.dx_f32, p.dx_add != 0, &tmDx,
                                        (t.nt * nacc + h) * BN, wi.r0 + t.mt * PM + rofs, tempty);
                 } else {
                     gemm_tile_epilogue(ring, smem, et, r, tbase, p.dw_bf16 != 0, t.wave > 0 || p.dw_add0,

@@ -225,18 +225,54 @@ size_t backward_bytes(int64_t M, int64_t V, int64_t chunk_rows) {
 // 256 rows, so no 256-row pair tile straddles two waves.
 struct BwdChoice {
     flp_bwd_schedule schedule;
-    int64_t chunk, waves;
+    int64_t chunk;   // rows of a row wave (all rows, rounded up to 128, for FLP_BWD_VSPLIT)
+    int64_t waves;   // row waves, or vocabulary chunks for FLP_BWD_VSPLIT
+    int64_t vc;      // padded vocabulary columns per chunk (all of them unless FLP_BWD_VSPLIT)
+    size_t off_scr;  // FLP_BWD_VSPLIT: fp32 dX scratch [M, H] (0: none)
+    size_t off_dz;   // the bf16 dZ buffer [chunk rows, vc]
 };
 
-flp_status choose_backward(int64_t M, int64_t V, size_t workspace_bytes, flp_bwd_schedule want,
+flp_status choose_backward(int64_t M, int64_t H, int64_t V, size_t workspace_bytes, flp_bwd_schedule want,
                            BwdChoice* out) {
-    if (want != FLP_BWD_AUTO && want != FLP_BWD_SPLIT && want != FLP_BWD_FUSED)
-        return fail(FLP_ERR_INVALID_ARG, "schedule must be FLP_BWD_AUTO, FLP_BWD_SPLIT or FLP_BWD_FUSED");
+    if (want != FLP_BWD_AUTO && want != FLP_BWD_SPLIT && want != FLP_BWD_FUSED && want != FLP_BWD_VSPLIT)
+        return fail(FLP_ERR_INVALID_ARG,
+                    "schedule must be FLP_BWD_AUTO, FLP_BWD_SPLIT, FLP_BWD_FUSED or FLP_BWD_VSPLIT");
     const BwdLayout L = bwd_layout(M, V);
     if (workspace_bytes < L.off_dz) return fail(FLP_ERR_WORKSPACE, "backward workspace too small");
-    const int64_t fit = static_cast<int64_t>((workspace_bytes - L.off_dz) / (static_cast<size_t>(L.Vp) * 2));
     const int64_t mr = std::max<int64_t>(BM, cdiv(M, BM) * BM);
+    // the vocabulary-split plan: all rows in one wave, the vocabulary in
+    // chunks of vc columns; dX accumulates over the chunks in an fp32 scratch
+    const size_t scr = align_up(static_cast<size_t>(std::max<int64_t>(M, 1)) * H * 4, 1024);
+    const size_t vs_off_dz = L.off_dz + scr;
+    const int64_t vs_vc =
+        workspace_bytes < vs_off_dz
+            ? 0
+            : std::min<int64_t>(L.Vp, static_cast<int64_t>((workspace_bytes - vs_off_dz) /
+                                                             (static_cast<size_t>(mr) * 2)) / BN * BN);
+    auto take_vsplit = [&]() {
+        out->schedule = FLP_BWD_VSPLIT;
+        out->chunk = mr;
+        out->waves = M > 0 ? cdiv(L.Vp, vs_vc) : 0;
+        out->vc = vs_vc;
+        out->off_scr = L.off_dz;
+        out->off_dz = vs_off_dz;
+        return FLP_OK;
+    };
+    if (want == FLP_BWD_VSPLIT) {
+        if (workspace_bytes < vs_off_dz)
+            return fail(FLP_ERR_WORKSPACE, "backward workspace has no room for the fp32 dX scratch");
+        if (vs_vc < BN)
+            return fail(FLP_ERR_WORKSPACE, "backward workspace holds fewer than 256 vocabulary columns of dZ");
+        return take_vsplit();
+    }
+    const int64_t fit = static_cast<int64_t>((workspace_bytes - L.off_dz) / (static_cast<size_t>(L.Vp) * 2));
     const int64_t split_chunk = std::min(mr, fit / BM * BM);
+    // Short row waves make every dW tile short (K = wave rows) and re-add dW
+    // once per wave; below 2048-row waves the vocabulary-split plan measured
+    // faster on GB300 (+10 % at 1024-row waves, +50 % at 512), above it the
+    // split schedule (its dX tiles run the whole vocabulary as K).
+    const bool short_waves = fit / BM * BM < std::min<int64_t>(mr, 2048);
+    if (want == FLP_BWD_AUTO && short_waves && vs_vc >= BN) return take_vsplit();
     if (split_chunk < BM) return fail(FLP_ERR_WORKSPACE, "backward workspace holds fewer than 128 rows of dZ");
     const int64_t fused_chunk = fit >= mr ? mr : fit / PM * PM;
     const int64_t fused_waves = fused_chunk > 0 ? cdiv(std::max<int64_t>(M, 1), fused_chunk) : 0;
@@ -254,6 +290,9 @@ flp_status choose_backward(int64_t M, int64_t V, size_t workspace_bytes, flp_bwd
     out->schedule = use;
     out->chunk = use == FLP_BWD_FUSED ? fused_chunk : split_chunk;
     out->waves = M > 0 ? cdiv(M, out->chunk) : 0;
+    out->vc = L.Vp;
+    out->off_scr = 0;
+    out->off_dz = L.off_dz;
     return FLP_OK;
 }
 
@@ -500,7 +539,7 @@ flp_status flp_backward_plan(int64_t M, int64_t H, int64_t V, size_t workspace_b
                              flp_bwd_schedule* schedule_used) {
     if (M < 0 || H < 1 || V < 1) return fail(FLP_ERR_INVALID_ARG, "M >= 0, H >= 1 and V >= 1 required");
     BwdChoice c{};
-    flp_status st = choose_backward(M, V, workspace_bytes, schedule, &c);
+    flp_status st = choose_backward(M, H, V, workspace_bytes, schedule, &c);
     if (st != FLP_OK) return st;
     if (wave_rows) *wave_rows = c.chunk;
     if (waves) *waves = c.waves;
@@ -613,6 +652,7 @@ void fused_wave_schedule(SegList& sl, int w, int Mt, int GM, int Vt, int Nh, int
 // schedule (the segment fields of BwdParams; the rest is filled per call).
 struct LaunchSpec {
     int64_t r0, rows, dz_rows;  // X / dX maps over rows [r0, r0 + rows); dZ buffer rows
+    int64_t dz_cols;            // dZ buffer columns (the padded vocabulary, or one chunk of it)
     int mark_begin, mark_end;   // phase events recorded around the launch (-1: none)
     BwdParams p;
 };
@@ -626,42 +666,63 @@ flp_status plan_backward_launches(int64_t M, int64_t H, int64_t V, const BwdChoi
     const int KB_v = Vt * (BN / BK);
     const int gm_rows = static_cast<int>(std::max<int64_t>(4, 40ll * 1000 * 1000 / (PM * 2 * H)));
     const int64_t chunk = ch.chunk;
+    // One wave's two launches over vocabulary tiles [vt0, vt1): its dZ tiles
+    // (static order), then its dX and dW tiles.
+    auto add_pair = [&](int64_t r0, int64_t rows, int64_t dz_rows, int vt0, int vt1, bool first,
+                        bool dx_add, bool dw_add) -> flp_status {
+        LaunchSpec a{};
+        a.r0 = r0;
+        a.rows = rows;
+        a.dz_rows = dz_rows;
+        a.dz_cols = ch.vc;
+        a.p.Vt = Vt;
+        a.p.Nh = Nh;
+        a.p.Ndx = SegList::dx_per_row(Nh);
+        a.p.KB_v = (vt1 - vt0) * (BN / BK);
+        a.p.vt0 = vt0;
+        a.p.M = static_cast<int>(rows);
+        a.p.chunk = static_cast<int>(rows);
+        a.p.nwaves = 1;
+        a.p.Mt_full = static_cast<int>(cdiv(rows, PM));
+        a.p.deps = 0;
+        a.p.dw_add0 = dw_add ? 1 : 0;
+        const int Mt = a.p.Mt_full;
+        const int GM = std::min(Mt, gm_rows);
+        LaunchSpec b = a;
+        b.p.dx_add = dx_add ? 1 : 0;
+        a.p.static_order = 1;  // equal-length dZ tiles: static round-robin
+        a.mark_begin = first ? 4 : -1;
+        a.mark_end = first ? 5 : -1;
+        b.mark_begin = first ? 6 : -1;
+        b.mark_end = first ? 7 : -1;
+        SegList dzs{&a.p};
+        for (int m0 = 0; m0 < Mt; m0 += GM) {
+            const int gm = std::min(GM, Mt - m0);
+            dzs.add(kSegDz, 0, m0, gm, vt0, 0, static_cast<int64_t>(gm) * (vt1 - vt0));
+        }
+        SegList gl{&b.p};
+        gl.dx_rows(0, 0, Mt, Nh);
+        gl.add(kSegDw, 0, 0, 0, vt0, 0, static_cast<int64_t>(vt1 - vt0) * Nh);
+        if (dzs.overflow || gl.overflow) return fail(FLP_ERR_UNSUPPORTED, "backward schedule too large");
+        out.push_back(a);
+        out.push_back(b);
+        return FLP_OK;
+    };
     if (ch.schedule == FLP_BWD_SPLIT) {
         for (int64_t r0 = 0; r0 < M; r0 += chunk) {
             const int64_t rows = std::min(chunk, M - r0);
-            const bool first = (r0 == 0);
-            LaunchSpec a{};
-            a.r0 = r0;
-            a.rows = rows;
-            a.dz_rows = rows;
-            a.p.Vt = Vt;
-            a.p.Nh = Nh;
-            a.p.Ndx = SegList::dx_per_row(Nh);
-            a.p.M = static_cast<int>(rows);
-            a.p.chunk = static_cast<int>(rows);
-            a.p.nwaves = 1;
-            a.p.Mt_full = static_cast<int>(cdiv(rows, PM));
-            a.p.deps = 0;
-            a.p.dw_add0 = (accumulate_dW || r0 > 0) ? 1 : 0;
-            const int Mt = a.p.Mt_full;
-            const int GM = std::min(Mt, gm_rows);
-            LaunchSpec b = a;
-            a.p.static_order = 1;  // equal-length dZ tiles: static round-robin
-            a.mark_begin = first ? 4 : -1;
-            a.mark_end = first ? 5 : -1;
-            b.mark_begin = first ? 6 : -1;
-            b.mark_end = first ? 7 : -1;
-            SegList dzs{&a.p};
-            for (int m0 = 0; m0 < Mt; m0 += GM) {
-                const int gm = std::min(GM, Mt - m0);
-                dzs.add(kSegDz, 0, m0, gm, 0, 0, static_cast<int64_t>(gm) * Vt);
-            }
-            SegList gl{&b.p};
-            gl.dx_rows(0, 0, Mt, Nh);
-            gl.add(kSegDw, 0, 0, 0, 0, 0, static_cast<int64_t>(Vt) * Nh);
-            if (dzs.overflow || gl.overflow) return fail(FLP_ERR_UNSUPPORTED, "backward schedule too large");
-            out.push_back(a);
-            out.push_back(b);
+            flp_status st = add_pair(r0, rows, rows, 0, Vt, r0 == 0, false, accumulate_dW || r0 > 0);
+            if (st != FLP_OK) return st;
+        }
+        return FLP_OK;
+    }
+    if (ch.schedule == FLP_BWD_VSPLIT) {
+        // one wave of all rows; each dW tile is written once (its chunk holds all its K)
+        const int tpc = static_cast<int>(ch.vc / BN);  // vocabulary tiles per chunk
+        for (int vt0 = 0; vt0 < Vt; vt0 += tpc) {
+            flp_status st = add_pair(0, M, chunk, vt0, std::min(Vt, vt0 + tpc), vt0 == 0, vt0 > 0,
+                                     accumulate_dW != 0);
+            if (st != FLP_OK) return st;
         }
         return FLP_OK;
     }
@@ -675,11 +736,13 @@ flp_status plan_backward_launches(int64_t M, int64_t H, int64_t V, const BwdChoi
         L.r0 = 0;
         L.rows = M;
         L.dz_rows = chunk;
+        L.dz_cols = ch.vc;
         L.mark_begin = (w == 0) ? 4 : -1;
         L.mark_end = -1;
         L.p.Vt = Vt;
         L.p.Nh = Nh;
         L.p.Ndx = SegList::dx_per_row(Nh);
+        L.p.KB_v = KB_v;
         L.p.M = static_cast<int>(M);
         L.p.chunk = static_cast<int>(chunk);
         L.p.nwaves = nwaves;
@@ -783,7 +846,7 @@ flp_status flp_backward_ex(const void* X, const void* W, const int64_t* targets,
     if (!workspace || !aligned16(workspace))
         return fail(FLP_ERR_WORKSPACE, "backward workspace null or misaligned");
     BwdChoice ch{};
-    if ((st = choose_backward(M, V, workspace_bytes, schedule, &ch)) != FLP_OK) return st;
+    if ((st = choose_backward(M, H, V, workspace_bytes, schedule, &ch)) != FLP_OK) return st;
     const int64_t chunk = ch.chunk;
     if (dW_dtype == FLP_BF16 && chunk < M)
         return fail(FLP_ERR_UNSUPPORTED,
@@ -803,10 +866,13 @@ flp_status flp_backward_ex(const void* X, const void* W, const int64_t* targets,
         return FLP_OK;
     }
     const BwdLayout L = bwd_layout(M, V);
-    uint8_t* dz = ws + L.off_dz;
-    const int64_t Vp = L.Vp;
+    uint8_t* dz = ws + ch.off_dz;
     const int pairs = d->pairs;
     unsigned long long ticket_base = 0;
+    // The vocabulary-split schedule accumulates a bf16 dX over its chunks in
+    // the fp32 scratch, then rounds it once.
+    const bool dx_scratch = ch.schedule == FLP_BWD_VSPLIT && ch.waves > 1 && dX_dtype == FLP_BF16;
+    float* scr = dx_scratch ? reinterpret_cast<float*>(ws + ch.off_scr) : nullptr;
 
     BwdMaps m{};
     if ((st = tmap_2d(&m.Wk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, W, H, V, H * 2, BK, BNH)) != FLP_OK) return st;
@@ -817,15 +883,20 @@ flp_status flp_backward_ex(const void* X, const void* W, const int64_t* targets,
         st = tmap_2d(&m.Dw, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, dW, H, V, H * 4, 32, BM);
     if (st != FLP_OK) return st;
 
-    // Row tensor maps (X, dX, dZ buffer) over `rows` rows starting at global row r0.
-    auto row_maps = [&](int64_t r0, int64_t rows, int64_t dz_rows) -> flp_status {
+    // Row tensor maps (X, dX, dZ buffer) over `rows` rows starting at global
+    // row r0; the dZ buffer is dz_rows x dz_cols.
+    auto row_maps = [&](int64_t r0, int64_t rows, int64_t dz_rows, int64_t dz_cols) -> flp_status {
         const uint8_t* Xc = static_cast<const uint8_t*>(X) + r0 * H * 2;
-        uint8_t* dXc = static_cast<uint8_t*>(dX) + r0 * H * dx_es;
         flp_status e;
         if ((e = tmap_2d(&m.Xk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Xc, H, rows, H * 2, BK, BM)) != FLP_OK) return e;
         if ((e = tmap_2d(&m.Xmn, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Xc, H, rows, H * 2, 64, 64)) != FLP_OK) return e;
-        if ((e = tmap_2d(&m.Dz, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dz, Vp, dz_rows, Vp * 2, BK, BM)) != FLP_OK) return e;
-        if ((e = tmap_2d(&m.DzMn, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dz, Vp, dz_rows, Vp * 2, 64, 64)) != FLP_OK) return e;
+        if ((e = tmap_2d(&m.Dz, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dz, dz_cols, dz_rows, dz_cols * 2, BK, BM)) != FLP_OK)
+            return e;
+        if ((e = tmap_2d(&m.DzMn, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dz, dz_cols, dz_rows, dz_cols * 2, 64, 64)) != FLP_OK)
+            return e;
+        if (dx_scratch)
+            return tmap_2d(&m.Dx, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, scr + r0 * H, H, rows, H * 4, 32, BM);
+        uint8_t* dXc = static_cast<uint8_t*>(dX) + r0 * H * dx_es;
         if (dX_dtype == FLP_F32)
             return tmap_2d(&m.Dx, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, dXc, H, rows, H * 4, 32, BM);
         return tmap_2d(&m.Dx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dXc, H, rows, H * 2, 64, BM);
@@ -837,8 +908,7 @@ flp_status flp_backward_ex(const void* X, const void* W, const int64_t* targets,
     BwdParams base{};
     base.V = static_cast<int>(V);
     base.KB_h = static_cast<int>(cdiv(H, BK));
-    base.KB_v = static_cast<int>(Vp / BK);
-    base.dx_f32 = dX_dtype == FLP_F32;
+    base.dx_f32 = (dX_dtype == FLP_F32 || dx_scratch) ? 1 : 0;
     base.dw_bf16 = dW_dtype == FLP_BF16;
     base.ent = ent;
     base.ignore_index = ignore_index;
@@ -859,7 +929,7 @@ flp_status flp_backward_ex(const void* X, const void* W, const int64_t* targets,
     for (LaunchSpec& spec : plan) {
         NvtxRange launch_range("flp_backward_launch");
         if (spec.r0 != mapped_r0 || spec.rows != mapped_rows) {
-            if ((st = row_maps(spec.r0, spec.rows, spec.dz_rows)) != FLP_OK) return st;
+            if ((st = row_maps(spec.r0, spec.rows, spec.dz_rows, spec.dz_cols)) != FLP_OK) return st;
             mapped_r0 = spec.r0;
             mapped_rows = spec.rows;
         }
@@ -867,7 +937,6 @@ flp_status flp_backward_ex(const void* X, const void* W, const int64_t* targets,
         const int64_t r0 = spec.r0;
         p.V = base.V;
         p.KB_h = base.KB_h;
-        p.KB_v = base.KB_v;
         p.dx_f32 = base.dx_f32;
         p.dw_bf16 = base.dw_bf16;
         p.ent = base.ent;
@@ -891,6 +960,13 @@ flp_status flp_backward_ex(const void* X, const void* W, const int64_t* targets,
         if ((st = launch_bwd(pairs, m, p, &ticket_base, s)) != FLP_OK) return st;
         if (spec.mark_end >= 0) mark(spec.mark_end, s);
     }
+    if (dx_scratch) {
+        const int64_t n = M * H;
+        const int blocks = static_cast<int>(std::min<int64_t>(cdiv(n, 8 * 256), 8 * d->sm_count));
+        flp_round_bf16_kernel<<<blocks, 256, 0, s>>>(scr, static_cast<uint16_t*>(dX), n);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return cuda_fail(e, "flp_round_bf16_kernel launch");
+    }
     return FLP_OK;
 }
 
@@ -900,7 +976,7 @@ flp_status flp_backward_schedule(int64_t M, int64_t H, int64_t V, size_t workspa
     if (M < 0 || H < 1 || V < 1 || pairs < 1 || capacity < 0 || !count)
         return fail(FLP_ERR_INVALID_ARG, "M >= 0, H >= 1, V >= 1, pairs >= 1 and count required");
     BwdChoice ch{};
-    flp_status st = choose_backward(M, V, workspace_bytes, schedule, &ch);
+    flp_status st = choose_backward(M, H, V, workspace_bytes, schedule, &ch);
     if (st != FLP_OK) return st;
     std::vector<LaunchSpec> plan;
     if (M > 0 && (st = plan_backward_launches(M, H, V, ch, pairs, 0, plan)) != FLP_OK) return st;
@@ -1147,7 +1223,7 @@ extern "C" flp_status flp_selftest_dependency_timeout(void* workspace, size_t wo
     if ((st = tmap_2d(&m.Dx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, ws + off_dx, H, M, H * 2, 64, BM)) != FLP_OK) return st;
     if ((st = tmap_2d(&m.Dw, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, ws + off_dw, H, V, H * 4, 32, BM)) != FLP_OK) return st;
 
-    BwdChoice ch{FLP_BWD_FUSED, M, 1};
+    BwdChoice ch{FLP_BWD_FUSED, M, 1, L.Vp, 0, L.off_dz};
     std::vector<LaunchSpec> plan;
     if ((st = plan_backward_launches(M, H, V, ch, d->pairs, 0, plan)) != FLP_OK) return st;
     if (plan.size() != 1) return fail(FLP_ERR_UNSUPPORTED, "self-test schedule is not one launch");

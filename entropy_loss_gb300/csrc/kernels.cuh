@@ -527,6 +527,30 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     pair_epilogue(sm, warp, tmem_base);
 }
 
+// ---------------------------------------------------------- fp32 -> bf16
+
+// dst[i] = bf16(src[i]) (round to nearest even): the vocabulary-split
+// backward's fp32 dX, accumulated over the chunks, rounded once.  n may be
+// any size; the 16-byte vector path runs while 8 elements remain.
+__global__ void __launch_bounds__(256) flp_round_bf16_kernel(const float* __restrict__ src,
+                                                             uint16_t* __restrict__ dst, int64_t n) {
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x * 8;
+    for (int64_t i = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) * 8; i < n; i += stride) {
+        if (i + 8 <= n) {
+            const float4 a = *reinterpret_cast<const float4*>(src + i);
+            const float4 b = *reinterpret_cast<const float4*>(src + i + 4);
+            uint4 o;
+            o.x = pack_bf16x2(a.x, a.y);
+            o.y = pack_bf16x2(a.z, a.w);
+            o.z = pack_bf16x2(b.x, b.y);
+            o.w = pack_bf16x2(b.z, b.w);
+            *reinterpret_cast<uint4*>(dst + i) = o;
+        } else {
+            for (int64_t j = i; j < n; ++j) dst[j] = static_cast<uint16_t>(pack_bf16x2(src[j], 0.f) & 0xFFFFu);
+        }
+    }
+}
+
 // ------------------------------------------------------------- split merge
 
 struct MergeParams {

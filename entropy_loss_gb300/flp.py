@@ -36,7 +36,9 @@ STATIC_SCRATCH_BYTES = 16 << 20
 FLP_BWD_AUTO = 0
 FLP_BWD_SPLIT = 1
 FLP_BWD_FUSED = 2
-SCHEDULES = {"auto": FLP_BWD_AUTO, "split": FLP_BWD_SPLIT, "fused": FLP_BWD_FUSED}
+FLP_BWD_VSPLIT = 3
+SCHEDULES = {"auto": FLP_BWD_AUTO, "split": FLP_BWD_SPLIT, "fused": FLP_BWD_FUSED,
+             "vsplit": FLP_BWD_VSPLIT}
 # phase k of flp_set_phase_events is recorded around events 2k, 2k+1; the
 # backward records phase 2 (split: first wave's dZ launch; fused: the whole
 # backward launch) and, split only, phase 3 (first wave's dX and dW launch)
@@ -184,7 +186,8 @@ def forward_noalloc(X, W, y, logprob, lse, entropy=None, *, ignore_index: int = 
 
 def backward_plan(M: int, H: int, V: int, workspace_bytes: int, schedule: str = "auto"):
     """(wave rows, waves, schedule name) that `backward` runs with for this
-    workspace size; host arithmetic only."""
+    workspace size (for "vsplit", waves counts vocabulary chunks); host
+    arithmetic only."""
     rows = ctypes.c_int64(0)
     waves = ctypes.c_int64(0)
     used = ctypes.c_int(0)
@@ -217,8 +220,9 @@ def backward(X, W, y, lse, entropy, grad_logprob, grad_entropy, *, ignore_index:
              workspace=None, schedule: str = "auto", stream=None):
     """(dX, dW) for upstream gradients of logprob and entropy (None = zero).
     dW may be fp32 (accumulated in fp32 across waves) or bf16 (one wave only).
-    schedule: "auto", "split" (per wave a dZ launch, then a dX/dW launch) or
-    "fused" (one persistent launch for every wave)."""
+    schedule: "auto", "split" (per wave a dZ launch, then a dX/dW launch),
+    "fused" (one persistent launch for every wave) or "vsplit" (all rows at
+    once, the vocabulary in chunks: dX accumulates over the chunks in fp32)."""
     M, H = X.shape
     V = W.shape[0]
     dev = X.device

@@ -146,15 +146,27 @@ flp_status flp_backward(const void* X, const void* W, const int64_t* targets, in
  *                   and a wave's last dW tiles overlap the next wave's dZ
  *                   tiles.  With more than one wave, waves are multiples of
  *                   256 rows.
- *   FLP_BWD_AUTO  : the faster one on GB300, FLP_BWD_SPLIT: at every shape
- *                   measured the fused launch ran 0.6-2% slower.  The chip
- *                   runs at its power cap, and mixing dZ tiles (exp-heavy
- *                   epilogue) with dX / dW tiles lowers the clock while the
- *                   cycles per tile stay the same.
+ *   FLP_BWD_VSPLIT: all rows in one wave and the vocabulary in chunks of as
+ *                   many columns as the workspace holds after an fp32 [M, H]
+ *                   dX scratch: per chunk, one launch of its dZ tiles and one
+ *                   of its dX and dW tiles.  dX accumulates over the chunks
+ *                   in fp32 (in the scratch when dX is bf16, rounded once at
+ *                   the end), and every dW tile is written once with K = all
+ *                   rows, so a small workspace keeps long dW contractions and
+ *                   a bf16 dW stays possible.  dW is bit-identical to a
+ *                   one-wave run of the other schedules; dX differs from it
+ *                   by the fp32 summation order over the chunks.
+ *   FLP_BWD_AUTO  : the faster one on GB300: FLP_BWD_SPLIT when its waves
+ *                   hold all rows or at least 2048 rows, else FLP_BWD_VSPLIT
+ *                   when the workspace allows it (else FLP_BWD_SPLIT).  The
+ *                   fused launch ran 0.6-2% slower than the split schedule at
+ *                   every shape measured: the chip runs at its power cap, and
+ *                   mixing dZ tiles (exp-heavy epilogue) with dX / dW tiles
+ *                   lowers the clock while the cycles per tile stay the same.
  * Both schedules compute every output tile with the same instructions in the
  * same order: their results are bit-identical.
  */
-typedef enum { FLP_BWD_AUTO = 0, FLP_BWD_SPLIT = 1, FLP_BWD_FUSED = 2 } flp_bwd_schedule;
+typedef enum { FLP_BWD_AUTO = 0, FLP_BWD_SPLIT = 1, FLP_BWD_FUSED = 2, FLP_BWD_VSPLIT = 3 } flp_bwd_schedule;
 
 /*
  * flp_backward with an explicit schedule.  FLP_BWD_FUSED returns
@@ -170,9 +182,10 @@ flp_status flp_backward_ex(const void* X, const void* W, const int64_t* targets,
                            void* stream);
 
 /*
- * The wave size, wave count and schedule (FLP_BWD_SPLIT or FLP_BWD_FUSED)
- * that flp_backward_ex would use for this problem, workspace size and
- * requested schedule.  Host arithmetic only: touches no device.  Any output
+ * The wave size, wave count and schedule (FLP_BWD_SPLIT, FLP_BWD_FUSED or
+ * FLP_BWD_VSPLIT) that flp_backward_ex would use for this problem, workspace
+ * size and requested schedule; for FLP_BWD_VSPLIT *waves counts vocabulary
+ * chunks.  Host arithmetic only: touches no device.  Any output
  * pointer may be NULL.  Returns FLP_ERR_WORKSPACE / FLP_ERR_UNSUPPORTED
  * exactly when the backward call would.
  */

@@ -37,7 +37,7 @@ class Guarded:
             torch.all(self.raw[GUARD + self.n:] == PATTERN))
 
 
-@pytest.mark.parametrize("schedule", ["split", "fused"])
+@pytest.mark.parametrize("schedule", ["split", "fused", "vsplit"])
 @pytest.mark.parametrize("M,H,V,chunk", [
     (300, 200, 3001, 128), (257, 72, 513, 0), (700, 136, 2100, 256),
     # wide dX tiles whose second 256-column half is mostly (H = 264) or
@@ -47,6 +47,11 @@ class Guarded:
 def test_no_writes_outside_buffers(flp, M, H, V, chunk, schedule):
     if schedule == "fused" and chunk == 128:
         pytest.skip("fused waves are multiples of 256 rows")
+    if schedule == "vsplit":
+        try:
+            flp.backward_plan(M, H, V, max(flp.workspace_query(M, H, V, True, chunk)), "vsplit")
+        except flp.FlpError:
+            pytest.skip("the workspace does not hold the vocabulary split's dX scratch and a dZ chunk")
     dev = torch.device("cuda")
     d = inputs.make_inputs(inputs.custom("guard", M, H, V, w_std=0.05, ignore_frac=0.1, seed=61))
     X, W, y = d["X"].to(dev), d["W"].to(dev), d["y"].to(dev)

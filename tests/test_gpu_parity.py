@@ -144,10 +144,11 @@ def test_scale_and_entropy_flag(flp, ent, scale):
     run_case(flp, case(200, 128, 1500, seed=3, scale=scale, compute_entropy=ent))
 
 
-def test_waves_and_ragged_tail(flp):
+@pytest.mark.parametrize("schedule", ["split", "auto"])
+def test_waves_and_ragged_tail(flp, schedule):
     # 700 rows in 256-row waves: three waves, the last one ragged; dW accumulates
-    # across waves in fp32.
-    run_case(flp, case(700, 136, 2100, seed=4), chunk_rows=256)
+    # across waves in fp32.  (auto takes the vocabulary split for such short waves.)
+    run_case(flp, case(700, 136, 2100, seed=4), chunk_rows=256, schedule=schedule)
 
 
 @pytest.mark.parametrize("schedule", ["split", "fused"])
@@ -196,6 +197,59 @@ def test_fused_and_split_bit_identical(flp, M, H, V, chunk, ent, dx_f32, dw_bf16
         outs[sched] = (dX.clone(), dW.clone())
     assert torch.equal(outs["split"][0], outs["fused"][0])
     assert torch.equal(outs["split"][1], outs["fused"][1])
+
+
+def _vsplit_workspace(flp, M, H, V, cols, dev):
+    """Smallest workspace whose vocabulary-split chunks are `cols` columns wide."""
+    Vp = -(-V // 256) * 256
+    want = -(-Vp // cols)
+    lo, hi = 0, 1 << 40
+    while lo < hi:
+        mid = (lo + hi) // 2
+        try:
+            ok = flp.backward_plan(M, H, V, mid, "vsplit")[1] <= want
+        except flp.FlpError:
+            ok = False
+        hi, lo = (mid, lo) if ok else (hi, mid + 1)
+    return torch.empty(lo, dtype=torch.uint8, device=dev)
+
+
+@pytest.mark.parametrize("M,H,V,cols,dx_f32,dw_bf16,acc", [
+    (700, 136, 2100, 768, False, False, False),   # 3 chunks; bf16 dX through the fp32 scratch
+    (700, 512, 2100, 512, True, False, True),     # 5 chunks; fp32 dX added in place; wide dX tiles
+    (1200, 264, 3001, 1024, False, True, False),  # bf16 dW, each tile written once
+    (257, 72, 513, 256, False, False, False),     # three one-tile chunks
+])
+def test_vsplit_matches_oracle(flp, M, H, V, cols, dx_f32, dw_bf16, acc):
+    """The vocabulary-split backward against the oracle; its dW against a
+    one-wave split backward bit for bit (every dW tile has all rows as K in
+    both), its dX within the tolerance (fp32 sums over the chunks)."""
+    dev = torch.device("cuda")
+    d = case(M, H, V, seed=24)
+    X, W, y = d["X"].to(dev), d["W"].to(dev), d["y"].to(dev)
+    g1, g2 = d["g_lp"].to(dev), d["g_ent"].to(dev)
+    big = flp.alloc_workspace(M, H, V, True, device=dev)
+    lp, lse, en = flp.forward(X, W, y, workspace=big)
+    ws = _vsplit_workspace(flp, M, H, V, cols, dev)
+    assert flp.backward_plan(M, H, V, ws.numel(), "vsplit")[1] == -(-(-(-V // 256) * 256) // cols)
+    base = torch.randn(V, H, device=dev)
+    dxt = torch.float32 if dx_f32 else torch.bfloat16
+    dwt = torch.bfloat16 if dw_bf16 else torch.float32
+    outs = {}
+    for sched, w in (("vsplit", ws), ("split", big)):
+        dW = base.clone() if acc else None
+        dX, dW = flp.backward(X, W, y, lse, en, g1, g2, workspace=w, schedule=sched, dx_dtype=dxt,
+                              dw_dtype=dwt, dW=dW, accumulate_dW=acc)
+        torch.cuda.synchronize()
+        assert flp.get_error(w) == flp.FLP_OK
+        outs[sched] = (dX.clone(), dW.clone())
+    assert torch.equal(outs["vsplit"][1], outs["split"][1])
+    Xb, Wb = inputs.bf16_bits(d["X"]), inputs.bf16_bits(d["W"])
+    o_dx, o_dw = oracle.backward(Xb, Wb, d["y"].numpy(), d["g_lp"].double().numpy(),
+                                 d["g_ent"].double().numpy())
+    check_grad(outs["vsplit"][0], o_dx, "dX")
+    want_dw = o_dw + (base.double().cpu().numpy() if acc else 0)
+    check_grad(outs["vsplit"][1], want_dw, "dW", rtol=2e-2 if dw_bf16 else RTOL_GRAD)
 
 
 @pytest.mark.parametrize("M", [4097, 5000])
@@ -269,11 +323,17 @@ def test_dw_bf16_single_wave(flp):
     _, o_dw = oracle.backward(Xb, Wb, d["y"].numpy(), d["g_lp"].double().numpy(),
                               d["g_ent"].double().numpy())
     check_grad(dW16, o_dw, "dW bf16")
-    # several waves, or accumulation, need the fp32 dW
+    # several row waves, or accumulation, need the fp32 dW
     small = flp.alloc_workspace(300, 200, 3001, True, chunk_rows=128, device=dev)
     with pytest.raises(flp.FlpError) as e:
-        flp.backward(X, W, y, lse, en, g1, g2, dw_dtype=torch.bfloat16, workspace=small)
+        flp.backward(X, W, y, lse, en, g1, g2, dw_dtype=torch.bfloat16, workspace=small,
+                     schedule="split")
     assert e.value.status == flp.FLP_ERR_UNSUPPORTED
+    # the vocabulary split (what auto runs on that workspace) writes each dW tile once
+    assert flp.backward_plan(300, 200, 3001, small.numel(), "auto")[2] == "vsplit"
+    _, dW16v = flp.backward(X, W, y, lse, en, g1, g2, dw_dtype=torch.bfloat16, workspace=small)
+    torch.cuda.synchronize()
+    assert torch.equal(dW16v, dW16)
     with pytest.raises(flp.FlpError) as e:
         flp.backward(X, W, y, lse, en, g1, g2, dW=dW16, accumulate_dW=True, workspace=ws)
     assert e.value.status == flp.FLP_ERR_UNSUPPORTED

@@ -75,7 +75,7 @@ def test_fused_dependency_wait_times_out_and_context_survives(flp):
         assert np.linalg.norm(g - want) / np.linalg.norm(want) < 1e-2
 
 
-@pytest.mark.parametrize("schedule", ["split", "fused"])
+@pytest.mark.parametrize("schedule", ["split", "fused", "vsplit"])
 def test_cuda_graph_capture_and_replay(flp, schedule):
     dev = torch.device("cuda")
     d = inputs.make_inputs(inputs.custom("graph", 700, 136, 2100, w_std=0.05, ignore_frac=0.1,

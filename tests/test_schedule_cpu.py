@@ -183,6 +183,18 @@ def test_fused_interleaves_dw_with_the_dz_sweep(flp):
     assert (dw_pos > last_dx).sum() >= 2 * 76 * (131072 // 64) // (4096 // 64)
 
 
+def test_auto_takes_vsplit_for_short_row_waves(flp):
+    """Row waves below 2048 rows (and below M) run the vocabulary split when
+    the workspace holds its fp32 dX scratch and a 256-column dZ chunk."""
+    M, H, V = 4096, 4096, 131072
+    for rows, want in ((1024, "vsplit"), (512, "vsplit"), (2048, "split"), (4096, "split")):
+        ws = workspace_for(flp, M, H, V, rows)
+        assert flp.backward_plan(M, H, V, ws, "auto")[2] == want, rows
+    # 128-row waves: 32 MiB does not hold the 64 MiB dX scratch
+    ws = workspace_for(flp, M, H, V, 128)
+    assert flp.backward_plan(M, H, V, ws, "auto")[:3] == (128, 32, "split")
+
+
 def test_plan_picks_and_rejects(flp):
     M, H, V = 5000, 64, 1000
     # a 384-row wave is a multiple of 128 but not 256: fused waves round down
@@ -196,7 +208,7 @@ def test_plan_picks_and_rejects(flp):
         assert flp.backward_plan(M, H, V, ws, "auto")[2] == "split"
     ws = workspace_for(flp, M, H, V, M)
     assert flp.backward_plan(M, H, V, ws, "fused")[:3] == (cdiv(M, 128) * 128, 1, "fused")
-    # 128 rows of dZ: split only
+    # 128 rows of dZ: split only (no room for the vocabulary-split plan either)
     ws = workspace_for(flp, M, H, V, 128)
     assert flp.backward_plan(M, H, V, ws, "auto")[2] == "split"
     with pytest.raises(flp.FlpError) as e:
@@ -205,3 +217,68 @@ def test_plan_picks_and_rejects(flp):
     with pytest.raises(flp.FlpError) as e:
         flp.backward_plan(M, H, V, 1024, "auto")
     assert e.value.status == flp.FLP_ERR_WORKSPACE
+
+
+def workspace_for_vsplit(flp, M, H, V, cols):
+    """Smallest workspace whose vocabulary-split chunks hold `cols` columns."""
+    lo, hi = 0, 1 << 42
+    while lo < hi:
+        mid = (lo + hi) // 2
+        try:
+            _, waves, _ = flp.backward_plan(M, H, V, mid, "vsplit")
+            ok = waves <= cdiv(cdiv(V, 256) * 256, cols)
+        except flp.FlpError:
+            ok = False
+        if ok:
+            hi = mid
+        else:
+            lo = mid + 1
+    return lo
+
+
+@pytest.mark.parametrize("M,H,V,cols", [
+    (4096, 4096, 131072, 32768), (4096, 4096, 131072, 256), (300, 200, 3001, 1024),
+    (20001, 4096, 128257, 8192), (1, 8, 1, 256), (700, 512, 2100, 768),
+])
+def test_vsplit_schedule(flp, M, H, V, cols):
+    """All rows in one wave; per vocabulary chunk a dZ launch then a dX + dW
+    launch; every dZ and dW tile once, each chunk's dX tiles once per chunk."""
+    ws = workspace_for_vsplit(flp, M, H, V, cols)
+    rows, chunks, used = flp.backward_plan(M, H, V, ws, "vsplit")
+    assert used == "vsplit" and rows >= M and chunks == cdiv(cdiv(V, 256) * 256, cols)
+    u = flp.backward_schedule(M, H, V, ws, "vsplit", 76)
+    launch = u[:, 0]
+    assert launch.max() + 1 == 2 * chunks
+    Vt, Nh, Mt = cdiv(V, 256), cdiv(H, 256), cdiv(M, 256)
+    per = cols // 256
+    seen_dz, seen_dw, seen_dx = [], [], []
+    for c in range(chunks):
+        dz = u[launch == 2 * c]
+        gm = u[launch == 2 * c + 1]
+        assert np.all(dz[:, 1] == DZ) and not np.any(gm[:, 1] == DZ)
+        vts = set(range(c * per, min(Vt, (c + 1) * per)))
+        assert set(dz[:, 4].tolist()) == vts          # the chunk's vocabulary tiles
+        dw = gm[gm[:, 1] == DW]
+        assert set(dw[:, 3].tolist()) == vts
+        seen_dz += [tuple(x) for x in dz[:, 3:].tolist()]
+        seen_dw += [tuple(x) for x in dw[:, 3:].tolist()]
+        dx = narrow(gm[gm[:, 1] != DW])
+        assert sorted(dx) == sorted((DX, 0, m, h) for m in range(Mt) for h in range(Nh))
+    assert sorted(seen_dz) == sorted((m, v) for m in range(Mt) for v in range(Vt))
+    assert sorted(seen_dw) == sorted((v, h) for v in range(Vt) for h in range(Nh))
+
+
+def test_vsplit_workspace_limits(flp):
+    M, H, V = 4096, 4096, 131072
+    # no room for the fp32 dX scratch, then no room for 256 columns of dZ
+    with pytest.raises(flp.FlpError) as e:
+        flp.backward_plan(M, H, V, 32 << 20, "vsplit")
+    assert e.value.status == flp.FLP_ERR_WORKSPACE
+    with pytest.raises(flp.FlpError) as e:
+        flp.backward_plan(M, H, V, (64 << 20) + (1 << 20), "vsplit")
+    assert e.value.status == flp.FLP_ERR_WORKSPACE
+    # a 1 GiB workspace: 64 MiB of fp32 dX scratch, the rest (less a few KiB
+    # of header and counters) as 4096-row dZ chunks of whole 256-column tiles
+    rows, chunks, _ = flp.backward_plan(M, H, V, 1 << 30, "vsplit")
+    cols = ((1 << 30) - (64 << 20) - 8192) // (4096 * 2) // 256 * 256
+    assert rows == 4096 and chunks == cdiv(131072, cols)
