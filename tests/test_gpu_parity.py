@@ -158,7 +158,7 @@ def test_waves_and_ragged_tail(flp, schedule):
     (1200, 264, 3001, 0),    # one wave
     (257, 136, 513, 256),    # two waves, the second a single row
     (2600, 72, 5000, 1024),  # fused: dZ tiles of a wave wait on the previous wave's dX / dW tiles
-    (2600, 512, 5000, 1024), # wide (256 x 512) dX tiles in three waves
+    (1300, 512, 16500, 512), # wide (256 x 512) dX tiles in three waves
 ])
 def test_schedules_match_oracle(flp, schedule, M, H, V, chunk):
     run_case(flp, case(M, H, V, seed=22), chunk_rows=chunk, schedule=schedule)
@@ -171,7 +171,8 @@ def test_schedules_match_oracle(flp, schedule, M, H, V, chunk):
     (2600, 72, 5000, 1024, True, True, False, False),
     (4096, 512, 16384, 0, True, False, False, False),
     (16384, 64, 1000, 256, True, False, False, True),  # 64 waves: the fused schedule spans two launches
-    (2600, 512, 5000, 1024, True, True, False, True),   # wide dX tiles, three waves, slot layouts switching
+    (1300, 512, 16500, 512, True, True, False, True),   # wide dX tiles, three waves, slot layouts switching
+    (1200, 264, 16500, 0, True, False, False, False),   # wide dX tiles whose second half is mostly beyond H
     (1000, 1024, 3000, 512, False, False, False, False),
 ])
 def test_fused_and_split_bit_identical(flp, M, H, V, chunk, ent, dx_f32, dw_bf16, acc):
@@ -219,6 +220,7 @@ def _vsplit_workspace(flp, M, H, V, cols, dev):
     (700, 512, 2100, 512, True, False, True),     # 5 chunks; fp32 dX added in place; wide dX tiles
     (1200, 264, 3001, 1024, False, True, False),  # bf16 dW, each tile written once
     (257, 72, 513, 256, False, False, False),     # three one-tile chunks
+    (600, 512, 40000, 16384, False, False, False),  # wide dX tiles; a shorter last chunk
 ])
 def test_vsplit_matches_oracle(flp, M, H, V, cols, dx_f32, dw_bf16, acc):
     """The vocabulary-split backward against the oracle; its dW against a
