@@ -489,6 +489,34 @@ def test_autograd_wrapper(flp):
     check_grad(W.grad, o_dw, "dW", rtol=2e-2)  # W.grad is rounded to bf16 (W's dtype)
 
 
+def test_headline_schedules_agree_at_full_size(flp):
+    """At the full headline shape: the fused backward equals the split one bit
+    for bit; the vocabulary split on a 256 MiB workspace (six chunks) gives the
+    same dW bits and a dX within rounding (fp32 sums over the chunks, then one
+    bf16 rounding).  The split schedule itself is checked against the oracle
+    below."""
+    dev = torch.device("cuda")
+    w = inputs.WORKLOADS["m4096_h4096_v131072"]
+    d = inputs.make_inputs(w)
+    X, W, y = d["X"].to(dev), d["W"].to(dev), d["y"].to(dev)
+    g1, g2 = d["g_lp"].to(dev), d["g_ent"].to(dev)
+    ws = flp.alloc_workspace(w.M, w.H, w.V, True, device=dev)
+    small = flp.alloc_workspace(w.M, w.H, w.V, True, chunk_rows=1024, device=dev)
+    lp, lse, en = flp.forward(X, W, y, workspace=ws)
+    out = {}
+    for sched, wsp in (("split", ws), ("fused", ws), ("vsplit", small)):
+        dX, dW = flp.backward(X, W, y, lse, en, g1, g2, workspace=wsp, schedule=sched)
+        torch.cuda.synchronize()
+        assert flp.get_error(wsp) == flp.FLP_OK
+        out[sched] = (dX, dW)
+    assert flp.backward_plan(w.M, w.H, w.V, small.numel(), "vsplit")[1] == 6
+    assert torch.equal(out["fused"][0], out["split"][0])
+    assert torch.equal(out["fused"][1], out["split"][1])
+    assert torch.equal(out["vsplit"][1], out["split"][1])
+    a, b = out["vsplit"][0].float(), out["split"][0].float()
+    assert float(torch.linalg.vector_norm(a - b) / torch.linalg.vector_norm(b)) < 4e-3
+
+
 # ------------------------------------------------- full-size workloads (sampled)
 
 @pytest.mark.parametrize("name", sorted(inputs.WORKLOADS))
