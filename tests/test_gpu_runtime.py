@@ -116,3 +116,29 @@ def test_cuda_graph_capture_and_replay(flp, schedule):
     for a, b in zip(eager, (lp, lse, en, dX, dW)):
         assert torch.equal(a, b)
     assert flp.get_error(ws) == flp.FLP_OK
+
+
+@pytest.mark.parametrize("schedule", ["split", "fused", "vsplit"])
+def test_repeated_backward_is_bit_stable(flp, schedule):
+    """60 back-to-back full-size backward launches (headline shape) per
+    schedule, every tenth checked bit for bit against the first: a race in the
+    tile hand-off, the fused schedule's counters or the dW / dX adds would
+    show as a changed bit or a timeout in the error word."""
+    dev = torch.device("cuda")
+    w = inputs.WORKLOADS["m4096_h4096_v131072"]
+    d = inputs.make_inputs(w)
+    X, W, y = d["X"].to(dev), d["W"].to(dev), d["y"].to(dev)
+    g1, g2 = d["g_lp"].to(dev), d["g_ent"].to(dev)
+    ws = flp.alloc_workspace(w.M, w.H, w.V, True, chunk_rows=1024 if schedule == "vsplit" else 0,
+                             device=dev)
+    fwd_ws = flp.alloc_workspace(w.M, w.H, w.V, True, device=dev)
+    _, lse, en = flp.forward(X, W, y, workspace=fwd_ws)
+    dX0, dW0 = flp.backward(X, W, y, lse, en, g1, g2, workspace=ws, schedule=schedule)
+    dX0, dW0 = dX0.clone(), dW0.clone()
+    dX, dW = torch.empty_like(dX0), torch.empty_like(dW0)
+    for i in range(60):
+        flp.backward(X, W, y, lse, en, g1, g2, dX=dX, dW=dW, workspace=ws, schedule=schedule)
+        if i % 10 == 9:
+            torch.cuda.synchronize()
+            assert flp.get_error(ws) == flp.FLP_OK
+            assert torch.equal(dX, dX0) and torch.equal(dW, dW0), f"launch {i} differs"
