@@ -294,6 +294,8 @@ def run_ours(args, world, rank, local):
     # library's own plan; host arithmetic)
     pairs = torch.cuda.get_device_properties(dev).multi_processor_count // 2
     bwd_launches = int(flp.backward_schedule(M, H, V, ws.numel(), args.schedule, pairs)[:, 0].max()) + 1
+    if sched == "vsplit" and waves > 1:
+        bwd_launches += 1  # the bf16 dX rounding of the fp32 sums over the vocabulary chunks
     launches = K * (2 + bwd_launches)
 
     result = {
