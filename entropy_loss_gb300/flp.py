@@ -40,8 +40,9 @@ FLP_BWD_VSPLIT = 3
 SCHEDULES = {"auto": FLP_BWD_AUTO, "split": FLP_BWD_SPLIT, "fused": FLP_BWD_FUSED,
              "vsplit": FLP_BWD_VSPLIT}
 # phase k of flp_set_phase_events is recorded around events 2k, 2k+1; the
-# backward records phase 2 (split: first wave's dZ launch; fused: the whole
-# backward launch) and, split only, phase 3 (first wave's dX and dW launch)
+# backward records phase 2 (split: first wave's dZ launch; vsplit: first
+# vocabulary chunk's; fused: the whole backward launch) and, except for the
+# fused schedule, phase 3 (the matching dX and dW launch)
 PHASES = ("fwd", "merge", "dz", "bwd_gemm")
 
 
@@ -138,9 +139,27 @@ def alloc_workspace(M: int, H: int, V: int, compute_entropy: bool = True, chunk_
 
 
 def _need(t, dtype, shape, name):
-    if t.dtype != dtype or tuple(t.shape) != tuple(shape) or not t.is_contiguous() or not t.is_cuda:
+    """t must be a contiguous CUDA tensor of `dtype` (or one of a tuple of
+    dtypes) and `shape`: the C ABI sees only its data pointer."""
+    ok_dtype = t.dtype in dtype if isinstance(dtype, tuple) else t.dtype == dtype
+    if not ok_dtype or tuple(t.shape) != tuple(shape) or not t.is_contiguous() or not t.is_cuda:
         raise ValueError(f"{name}: expected contiguous CUDA {dtype} of shape {tuple(shape)}, "
                          f"got {t.dtype} {tuple(t.shape)} on {t.device}")
+
+
+def _need_opt(t, dtype, shape, name):
+    if t is not None:
+        _need(t, dtype, shape, name)
+
+
+def _nbytes(t) -> int:
+    return t.numel() * t.element_size()
+
+
+def _workspace(t):
+    if not t.is_cuda or not t.is_contiguous():
+        raise ValueError("workspace: expected a contiguous CUDA tensor")
+    return _ptr(t), _nbytes(t)
 
 
 def forward(X, W, y, *, ignore_index: int = -100, scale: float = 1.0, compute_entropy: bool = True,
@@ -158,11 +177,14 @@ def forward(X, W, y, *, ignore_index: int = -100, scale: float = 1.0, compute_en
         entropy = torch.empty(M, dtype=torch.float32, device=dev)
     if not compute_entropy:
         entropy = None
+    for t, name in ((logprob, "logprob"), (lse, "lse"), (entropy, "entropy")):
+        _need_opt(t, torch.float32, (M,), name)
     if workspace is None:
         workspace = alloc_workspace(M, H, V, compute_entropy, device=dev)
+    ws_ptr, ws_bytes = _workspace(workspace)
     _check(load().flp_forward(_ptr(X), _ptr(W), _ptr(y), M, H, V, ignore_index, float(scale),
                               int(compute_entropy), _ptr(logprob), _ptr(lse), _ptr(entropy),
-                              _ptr(workspace), workspace.numel(), _stream(stream)), "flp_forward")
+                              ws_ptr, ws_bytes, _stream(stream)), "flp_forward")
     return logprob, lse, entropy
 
 
@@ -177,6 +199,10 @@ def forward_noalloc(X, W, y, logprob, lse, entropy=None, *, ignore_index: int = 
     _need(X, torch.bfloat16, (M, H), "X")
     _need(W, torch.bfloat16, (V, H), "W")
     _need(y, torch.int64, (M,), "targets")
+    _need(logprob, torch.float32, (M,), "logprob")
+    _need(lse, torch.float32, (M,), "lse")
+    if compute_entropy:
+        _need(entropy, torch.float32, (M,), "entropy")
     _check(load().flp_forward_noalloc(_ptr(X), _ptr(W), _ptr(y), M, H, V, ignore_index,
                                       float(scale), int(compute_entropy), _ptr(logprob), _ptr(lse),
                                       _ptr(entropy if compute_entropy else None), _stream(stream)),
@@ -225,21 +251,35 @@ def backward(X, W, y, lse, entropy, grad_logprob, grad_entropy, *, ignore_index:
     once, the vocabulary in chunks: dX accumulates over the chunks in fp32)."""
     M, H = X.shape
     V = W.shape[0]
+    _need(X, torch.bfloat16, (M, H), "X")
+    _need(W, torch.bfloat16, (V, H), "W")
+    _need(y, torch.int64, (M,), "targets")
+    _need(lse, torch.float32, (M,), "lse")
+    if compute_entropy:
+        _need(entropy, torch.float32, (M,), "entropy")
+    _need_opt(grad_logprob, torch.float32, (M,), "grad_logprob")
+    if compute_entropy:
+        _need_opt(grad_entropy, torch.float32, (M,), "grad_entropy")
+    if schedule not in SCHEDULES:
+        raise ValueError(f"schedule must be one of {sorted(SCHEDULES)}")
     dev = X.device
     if dX is None:
         dX = torch.empty(M, H, dtype=dx_dtype, device=dev)
     if dW is None:
         dW = torch.empty(V, H, dtype=dw_dtype, device=dev)
+    _need(dX, (torch.bfloat16, torch.float32), (M, H), "dX")
+    _need(dW, (torch.bfloat16, torch.float32), (V, H), "dW")
     dxt = FLP_F32 if dX.dtype == torch.float32 else FLP_BF16
     dwt = FLP_F32 if dW.dtype == torch.float32 else FLP_BF16
     if workspace is None:
         workspace = alloc_workspace(M, H, V, compute_entropy, device=dev)
+    ws_ptr, ws_bytes = _workspace(workspace)
     _check(load().flp_backward_ex(_ptr(X), _ptr(W), _ptr(y), M, H, V, ignore_index, float(scale),
                                   int(compute_entropy), _ptr(lse),
                                   _ptr(entropy if compute_entropy else None), _ptr(grad_logprob),
                                   _ptr(grad_entropy if compute_entropy else None), _ptr(dX), dxt,
-                                  _ptr(dW), dwt, int(accumulate_dW), _ptr(workspace),
-                                  workspace.numel(), SCHEDULES[schedule], _stream(stream)),
+                                  _ptr(dW), dwt, int(accumulate_dW), ws_ptr, ws_bytes,
+                                  SCHEDULES[schedule], _stream(stream)),
            "flp_backward_ex")
     return dX, dW
 
@@ -263,7 +303,7 @@ def selftest_wait_timeout(stall_after: int, wait_limit_ns: int, workspace=None, 
     detected, FLP_OK for a normal run)."""
     if workspace is None:
         workspace = torch.empty(SELFTEST_WORKSPACE_BYTES, dtype=torch.uint8, device="cuda")
-    return int(load().flp_selftest_wait_timeout(_ptr(workspace), workspace.numel(), stall_after,
+    return int(load().flp_selftest_wait_timeout(_ptr(workspace), _nbytes(workspace), stall_after,
                                                 wait_limit_ns, _stream(stream)))
 
 
@@ -274,7 +314,7 @@ def selftest_dependency_timeout(broken: bool, wait_limit_ns: int, workspace=None
     status the run leaves (FLP_ERR_TIMEOUT when broken, FLP_OK otherwise)."""
     if workspace is None:
         workspace = torch.empty(SELFTEST_WORKSPACE_BYTES, dtype=torch.uint8, device="cuda")
-    return int(load().flp_selftest_dependency_timeout(_ptr(workspace), workspace.numel(),
+    return int(load().flp_selftest_dependency_timeout(_ptr(workspace), _nbytes(workspace),
                                                       int(bool(broken)), wait_limit_ns,
                                                       _stream(stream)))
 
@@ -286,6 +326,10 @@ def loss(logprob, y, kind=FLP_LOSS_NLL_MEAN, *, ignore_index: int = -100, old_lo
     per-token terms [M] or None).  grad_logprob is the upstream gradient for
     `backward`."""
     M = logprob.shape[0]
+    _need(logprob, torch.float32, (M,), "logprob")
+    _need(y, torch.int64, (M,), "targets")
+    for t, name in ((old_logprob, "old_logprob"), (advantage, "advantage"), (ref_logprob, "ref_logprob")):
+        _need_opt(t, torch.float32, (M,), name)
     dev = logprob.device
     out = torch.empty(1, dtype=torch.float32, device=dev)
     grad = torch.empty(M, dtype=torch.float32, device=dev)
@@ -322,7 +366,7 @@ class FusedLinearLogprob(torch.autograd.Function):
         # a bf16 weight gets its bf16 gradient straight from the epilogue when
         # one backward wave covers every row; otherwise fp32 waves, then a cast
         M, H, V = X.shape[0], X.shape[1], W.shape[0]
-        wave_rows, _, _ = backward_plan(M, H, V, workspace.numel())
+        wave_rows, _, _ = backward_plan(M, H, V, _nbytes(workspace))
         direct = W.dtype == torch.bfloat16 and wave_rows >= M
         dX, dW = backward(X, W, y, lse, ent if compute_entropy else None, g_lp, g_ent,
                           ignore_index=ignore_index, scale=scale, compute_entropy=compute_entropy,

@@ -475,6 +475,33 @@ def test_argument_errors(flp):
     assert e.value.status == flp.FLP_ERR_UNSUPPORTED
 
 
+def test_binding_rejects_tensors_the_abi_cannot_describe(flp):
+    """The C ABI takes bare pointers, so the binding refuses non-contiguous,
+    wrongly typed or wrongly shaped tensors before calling it."""
+    dev = torch.device("cuda")
+    d = case(64, 64, 300, seed=25)
+    X, W, y = d["X"].to(dev), d["W"].to(dev), d["y"].to(dev)
+    lp, lse, en = flp.forward(X, W, y)
+    g = torch.zeros(64, device=dev)
+    bad = [
+        dict(X=X.t().contiguous().t()),                      # transposed view
+        dict(W=W.float()),                                   # fp32 weight
+        dict(y=y.int()),                                     # int32 targets
+        dict(lse=lse[:32]),                                  # short lse
+        dict(dX=torch.empty(64, 64, dtype=torch.float16, device=dev)),
+        dict(dW=torch.empty(64, 300, device=dev)),           # transposed dW shape
+    ]
+    for over in bad:
+        a = dict(X=X, W=W, y=y, lse=lse, dX=None, dW=None)
+        a.update(over)
+        with pytest.raises(ValueError):
+            flp.backward(a["X"], a["W"], a["y"], a["lse"], en, g, g, dX=a["dX"], dW=a["dW"])
+    with pytest.raises(ValueError):
+        flp.forward(X, W, y, logprob=torch.empty(64, dtype=torch.float64, device=dev))
+    with pytest.raises(ValueError):
+        flp.backward(X, W, y, lse, en, g, g, schedule="nope")
+
+
 def test_autograd_wrapper(flp):
     dev = torch.device("cuda")
     d = case(200, 64, 1000, seed=14)
