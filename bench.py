@@ -147,7 +147,7 @@ class ClockSampler:
         if not exe:
             return
         self.proc = subprocess.Popen([exe, f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                                      "-i", str(self.gpu), "-lms", "200"],
+                                      "-i", str(self.gpu), "-lms", "100"],
                                      stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         self.thread = threading.Thread(target=self._read, daemon=True)
         self.thread.start()

@@ -52,21 +52,6 @@ enum UnitKind : int { kUnitDz = 0, kUnitDx = 1, kUnitDw = 2 };
 //              hidden tiles outer
 enum SegKind : int { kSegDz = 0, kSegDx = 1, kSegDw = 2, kSegDzDw = 3, kSegDx2 = 4 };
 
-// Shared-memory slots.  Normal tiles: STAGES slots of 16 KiB of A and 16 KiB
-// of B (A slots first, then B slots).  Wide dX tiles: STAGES_W slots of 48 KiB
-// (A, then the B halves of the two 256-column sub-tiles), over the same bytes.
-constexpr int STAGES_W = 4;
-constexpr uint32_t STAGE_W_BYTES = A_STAGE_BYTES + 2 * B_STAGE_BYTES;
-constexpr uint32_t PAIR_STAGE_TX_W = 2 * STAGE_W_BYTES;
-static_assert(STAGES_W * STAGE_W_BYTES <= SMEM_STG, "wide slots must fit the pipeline region");
-
-__device__ __forceinline__ uint32_t slot_a(bool wide, int s) {
-    return wide ? s * STAGE_W_BYTES : SMEM_A + s * A_STAGE_BYTES;
-}
-__device__ __forceinline__ uint32_t slot_b(bool wide, int s) {
-    return wide ? s * STAGE_W_BYTES + A_STAGE_BYTES : SMEM_B + s * B_STAGE_BYTES;
-}
-
 struct BwdSeg {
     int start;  // first ticket
     int kind;

@@ -151,17 +151,18 @@ struct FwdPlan {
     size_t off_m, off_s, off_t, off_zy, bytes;
 };
 
-// Chooses the V-split: units are (256-row pair tile, run of tps 256-column
+// Chooses the V-split: units are (256-row pair tile, run of tps 512-column
 // tiles); a static round-robin over the persistent CTA pairs finishes after
-// ceil(units / pairs) * tps tiles.  Each extra split adds M * 24 bytes of
-// partial traffic, charged in tile-times so that near-ties favour fewer splits.
+// ceil(units / pairs) * tps tiles.  Each extra split adds M * 48 bytes of
+// partial traffic (two halves of m, sigma, tau and their reads), charged in
+// tile-times so that near-ties favour fewer splits.
 FwdPlan plan_forward(int64_t M, int64_t H, int64_t V, int compute_entropy, int pairs) {
     FwdPlan f{};
     pairs = std::max(1, pairs);
     f.Mt = static_cast<int>(cdiv(M, PM));
-    f.Vt = static_cast<int>(cdiv(V, BN));
-    const double tile_s = 2.0 * PM * BN * static_cast<double>(H) / 2.4e13;  // ~bf16 rate of a pair
-    const double split_cost = (static_cast<double>(M) * 24.0 / 6.0e12) / tile_s;
+    f.Vt = static_cast<int>(cdiv(V, 2 * BN));  // 512-column tiles
+    const double tile_s = 2.0 * PM * 2 * BN * static_cast<double>(H) / 2.4e13;  // ~bf16 rate of a pair
+    const double split_cost = (static_cast<double>(M) * 48.0 / 6.0e12) / tile_s;
     double best = 1e300;
     int best_tps = f.Vt;
     for (int tps = 1; tps <= f.Vt; ++tps) {
@@ -183,7 +184,7 @@ FwdPlan plan_forward(int64_t M, int64_t H, int64_t V, int compute_entropy, int p
     if (f.GM < 1) f.GM = 1;
     f.units = f.Mt * f.S;
     f.grid = 2 * std::min(f.units, pairs);
-    const size_t part = align_up(static_cast<size_t>(f.S) * M * sizeof(float), 1024);
+    const size_t part = align_up(static_cast<size_t>(2 * f.S) * M * sizeof(float), 1024);  // 2 halves per split
     f.off_m = kHeaderBytes;
     f.off_s = f.off_m + part;
     f.off_t = f.off_s + part;
@@ -374,11 +375,11 @@ flp_status check_on_current_device(const void* p, const char* what) {
 // Launches `kernel` on `grid` CTAs grouped in clusters of two (the CTA pairs
 // that share each tcgen05.mma.cta_group::2 tile).
 template <typename... KArgs, typename... Args>
-flp_status launch_pairs(void (*kernel)(KArgs...), int grid, cudaStream_t s, const char* what,
-                        Args&&... args) {
+flp_status launch_pairs_n(void (*kernel)(KArgs...), int grid, int threads, cudaStream_t s, const char* what,
+                          Args&&... args) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid));
-    cfg.blockDim = dim3(NUM_THREADS);
+    cfg.blockDim = dim3(static_cast<unsigned>(threads));
     cfg.dynamicSmemBytes = SMEM_ALLOC;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
@@ -394,10 +395,16 @@ flp_status launch_pairs(void (*kernel)(KArgs...), int grid, cudaStream_t s, cons
     return FLP_OK;
 }
 
+template <typename... KArgs, typename... Args>
+flp_status launch_pairs(void (*kernel)(KArgs...), int grid, cudaStream_t s, const char* what,
+                        Args&&... args) {
+    return launch_pairs_n(kernel, grid, NUM_THREADS, s, what, std::forward<Args>(args)...);
+}
+
 template <bool kEnt>
 flp_status launch_fwd(int grid, const CUtensorMap& a, const CUtensorMap& b, const FwdParams& p,
                       cudaStream_t s) {
-    return launch_pairs(flp_fwd_kernel<kEnt>, grid, s, "flp_fwd_kernel launch", a, b, p);
+    return launch_pairs_n(flp_fwd_kernel<kEnt>, grid, FWD_THREADS, s, "flp_fwd_kernel launch", a, b, p);
 }
 
 flp_status common_checks(const void* X, const void* W, const int64_t* targets, int64_t M,
@@ -513,7 +520,7 @@ flp_status flp_forward(const void* X, const void* W, const int64_t* targets, int
 
     MergeParams mp{};
     mp.M = static_cast<int>(M);
-    mp.S = f.S;
+    mp.S = 2 * f.S;  // two 256-column halves per split
     mp.V = static_cast<int>(V);
     mp.ignore_index = ignore_index;
     mp.compute_entropy = ent;
@@ -1112,7 +1119,7 @@ extern "C" flp_status flp_forward_noalloc(const void* X, const void* W, const in
 
     MergeParams mp{};
     mp.M = static_cast<int>(M);
-    mp.S = f.S;
+    mp.S = 2 * f.S;  // two 256-column halves per split
     mp.V = static_cast<int>(V);
     mp.ignore_index = ignore_index;
     mp.compute_entropy = ent;

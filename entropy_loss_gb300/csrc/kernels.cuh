@@ -26,6 +26,14 @@
 // accumulator on the leader's `tempty` barrier.  Two 256-column accumulators
 // (512 TMEM columns) let a tile's epilogue overlap the next tile's MMAs.
 //
+// The forward runs wide tiles instead: 256 rows x 512 columns, one per pair,
+// both accumulators (half h of the columns in accumulator h), so each SM loads
+// 16 KiB of A and 32 KiB of B per K step for twice the MACs (25 % fewer
+// operand bytes per MAC).  It has two epilogue groups of four warps (warps
+// 2..5 drain half 0, warps 6..9 half 1; 320 threads), and the MMA issuer
+// staggers the halves at both ends of a tile so that one half's epilogue runs
+// under the other half's MMAs.
+//
 // Every mbarrier wait is bounded (globaltimer); on expiry the kernel raises the
 // timeout bit in the error word, stops issuing work, lets its copies and MMAs
 // in flight finish (a bounded wait), frees its TMEM and returns.
@@ -45,6 +53,7 @@ constexpr int UMMA_K = 16;        // K per tcgen05.mma (bf16)
 constexpr int STAGES = 6;
 constexpr int NUM_THREADS = 192;
 constexpr int EPI_THREADS = 128;
+constexpr int FWD_THREADS = 64 + 2 * EPI_THREADS;  // the forward: two epilogue groups of four warps
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint16_t PAIR_MASK = 0x3;
 
@@ -72,6 +81,22 @@ constexpr uint32_t NUM_BARS = 2 * STAGES + 4 + 1 + 2 * SCHED_SLOTS;
 constexpr uint32_t SMEM_MISC = SMEM_BAR + NUM_BARS * 8;  // tmem slot, abort flag, sched slots
 constexpr uint32_t SMEM_TOTAL = SMEM_MISC + 8 + 4 * SCHED_SLOTS;
 constexpr uint32_t SMEM_ALLOC = SMEM_TOTAL + 1024;  // slack for 1024-byte alignment
+
+// Shared-memory slots.  Normal tiles: STAGES slots of 16 KiB of A and 16 KiB
+// of B (A slots first, then B slots).  Wide tiles (the forward's, and dX tiles
+// of the backward): STAGES_W slots of 48 KiB (A, then the B halves of the two
+// 256-column sub-tiles), over the same bytes.
+constexpr int STAGES_W = 4;
+constexpr uint32_t STAGE_W_BYTES = A_STAGE_BYTES + 2 * B_STAGE_BYTES;
+constexpr uint32_t PAIR_STAGE_TX_W = 2 * STAGE_W_BYTES;
+static_assert(STAGES_W * STAGE_W_BYTES <= SMEM_STG, "wide slots must fit the pipeline region");
+
+__device__ __forceinline__ uint32_t slot_a(bool wide, int s) {
+    return wide ? s * STAGE_W_BYTES : SMEM_A + s * A_STAGE_BYTES;
+}
+__device__ __forceinline__ uint32_t slot_b(bool wide, int s) {
+    return wide ? s * STAGE_W_BYTES + A_STAGE_BYTES : SMEM_B + s * B_STAGE_BYTES;
+}
 
 struct Smem {
     uint8_t* base;
@@ -244,7 +269,8 @@ __device__ __forceinline__ void tmem_row64_to_bf16(uint32_t taddr, uint32_t (&w)
 // ------------------------------------------------------------ forward kernel
 
 struct FwdParams {
-    // schedule: units are runs [n0, n1) of 256-column tiles sharing one 256-row pair tile
+    // schedule: units are runs [n0, n1) of 512-column tiles sharing one 256-row pair tile;
+    // each unit writes two partials per row (one per 256-column half): S * 2 in all
     int units, Mt, Nt, S, tps, GM;
     int KB;    // K blocks of 64 (H / 64, rounded up)
     int M;     // rows
@@ -283,8 +309,11 @@ __device__ __forceinline__ Unit decode_unit(const FwdParams& p, int u) {
     return t;
 }
 
+// k-blocks issued half by half at each end of a forward tile (at most the
+// number of wide slots: those k-blocks' stages stay held until both halves ran)
+constexpr int FWD_EDGE = STAGES_W;
 template <bool kEnt>
-__global__ void __launch_bounds__(NUM_THREADS, 1)
+__global__ void __launch_bounds__(FWD_THREADS, 1)
     flp_fwd_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const FwdParams p) {
     extern __shared__ uint8_t smem_raw[];
@@ -324,14 +353,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                             ok = false;
                             break;
                         }
-                        if (leader) mbar_arrive_expect_tx(&sm.full[stage], PAIR_STAGE_TX);
+                        if (leader) mbar_arrive_expect_tx(&sm.full[stage], PAIR_STAGE_TX_W);
                         const uint32_t bar = mapa_shared(smem_addr(&sm.full[stage]), 0);
-                        tma_load_2d_pair(smem + SMEM_A + stage * A_STAGE_BYTES, &tmA, kb * BK,
+                        tma_load_2d_pair(smem + slot_a(true, stage), &tmA, kb * BK,
                                          t.mt * PM + static_cast<int>(rank) * BM, bar);
-                        tma_load_2d_pair(smem + SMEM_B + stage * B_STAGE_BYTES, &tmB, kb * BK,
-                                         nt * BN + static_cast<int>(rank) * BNH, bar);
+#pragma unroll
+                        for (int h = 0; h < 2; ++h)
+                            tma_load_2d_pair(smem + slot_b(true, stage) + h * B_STAGE_BYTES, &tmB, kb * BK,
+                                             nt * 2 * BN + h * BN + static_cast<int>(rank) * BNH, bar);
                         ++issued;
-                        if (++stage == STAGES) {
+                        if (++stage == STAGES_W) {
                             stage = 0;
                             phase ^= 1u;
                         }
@@ -344,45 +375,79 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
     } else if (warp == 1) {
         // ---------------------------------------------- MMA issuer (leader)
+        // A 512-column tile uses both accumulators, half h in accumulator h.
+        // The first and last `edge` k-blocks are issued half by half: at the
+        // end of a tile half 0 completes (and its epilogue starts) while the
+        // half-1 MMAs of those k-blocks still run, and at the start of the
+        // next tile half 0 fills while half 1 is still being drained.
         if (lane == 0 && leader) {
-            int stage = 0;
-            uint32_t phase = 0;
-            int acc = 0;
+            uint32_t gk = 0;  // k-blocks consumed so far: stage gk % STAGES_W, parity (gk / STAGES_W) & 1
             uint32_t acc_phase = 0;
             bool ok = true;
             constexpr uint32_t idesc = idesc_bf16_f32(PM, BN, 0, 0);
+            constexpr int edge = FWD_EDGE;
+            auto issue = [&](uint32_t g, int h, int kb) {
+                const int s = static_cast<int>(g % STAGES_W);
+                const uint32_t a_base = smem_addr(smem + slot_a(true, s));
+                const uint32_t b_base = smem_addr(smem + slot_b(true, s)) + h * B_STAGE_BYTES;
+#pragma unroll
+                for (int k = 0; k < BK / UMMA_K; ++k)
+                    umma_bf16_pair(tmem_base + static_cast<uint32_t>(h * BN), operand_desc<0>(a_base, k),
+                                   operand_desc<0>(b_base, k), idesc, (kb > 0 || k > 0) ? 1u : 0u);
+            };
+            auto wait_full = [&](uint32_t g) {
+                if (!mbar_wait(&sm.full[g % STAGES_W], (g / STAGES_W) & 1u, limit, abort_flag)) return false;
+                tc_fence_after();
+                return true;
+            };
+            auto release = [&](uint32_t g) {
+                umma_commit_pair_mc(&sm.empty[g % STAGES_W], PAIR_MASK);  // stage free in both CTAs
+            };
             for (int u = pair; u < p.units && ok; u += npairs) {
                 const Unit t = decode_unit(p, u);
                 for (int nt = t.n0; nt < t.n1 && ok; ++nt) {
-                    if (!mbar_wait(&sm.tempty[acc], acc_phase ^ 1u, limit, abort_flag)) {
+                    const int head = min(edge, p.KB);
+                    const int tail0 = max(head, p.KB - edge);
+                    if (!mbar_wait(&sm.tempty[0], acc_phase ^ 1u, limit, abort_flag)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
-                    for (int kb = 0; kb < p.KB; ++kb) {
-                        if (!mbar_wait(&sm.full[stage], phase, limit, abort_flag)) {
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after();
-                        const uint32_t a_base = smem_addr(smem + SMEM_A + stage * A_STAGE_BYTES);
-                        const uint32_t b_base = smem_addr(smem + SMEM_B + stage * B_STAGE_BYTES);
-#pragma unroll
-                        for (int k = 0; k < BK / UMMA_K; ++k)
-                            umma_bf16_pair(d_tmem, operand_desc<0>(a_base, k),
-                                           operand_desc<0>(b_base, k), idesc,
-                                           (kb > 0 || k > 0) ? 1u : 0u);
-                        umma_commit_pair_mc(&sm.empty[stage], PAIR_MASK);  // stage free in both CTAs
-                        if (++stage == STAGES) {
-                            stage = 0;
-                            phase ^= 1u;
-                        }
+                    for (int kb = 0; kb < head && ok; ++kb) {
+                        ok = wait_full(gk + kb);
+                        if (ok) issue(gk + kb, 0, kb);
                     }
                     if (!ok) break;
-                    umma_commit_pair_mc(&sm.tfull[acc], PAIR_MASK);  // accumulator ready in both CTAs
-                    acc ^= 1;
-                    if (acc == 0) acc_phase ^= 1u;
+                    if (head == p.KB) umma_commit_pair_mc(&sm.tfull[0], PAIR_MASK);
+                    if (!mbar_wait(&sm.tempty[1], acc_phase ^ 1u, limit, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    for (int kb = 0; kb < head; ++kb) {
+                        issue(gk + kb, 1, kb);
+                        release(gk + kb);
+                    }
+                    for (int kb = head; kb < tail0 && ok; ++kb) {
+                        ok = wait_full(gk + kb);
+                        if (!ok) break;
+                        issue(gk + kb, 0, kb);
+                        issue(gk + kb, 1, kb);
+                        release(gk + kb);
+                    }
+                    for (int kb = tail0; kb < p.KB && ok; ++kb) {
+                        ok = wait_full(gk + kb);
+                        if (ok) issue(gk + kb, 0, kb);
+                    }
+                    if (!ok) break;
+                    if (head < p.KB) umma_commit_pair_mc(&sm.tfull[0], PAIR_MASK);  // half 0 ready in both CTAs
+                    for (int kb = tail0; kb < p.KB; ++kb) {
+                        issue(gk + kb, 1, kb);
+                        release(gk + kb);
+                    }
+                    umma_commit_pair_mc(&sm.tfull[1], PAIR_MASK);  // half 1 ready in both CTAs
+                    gk += static_cast<uint32_t>(p.KB);
+                    acc_phase ^= 1u;
                 }
             }
             if (!ok) {
@@ -394,12 +459,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
     } else {
         // --------------------------------------------------------- epilogue
+        // two groups of four warps: group g drains accumulator g, the
+        // 256-column half g of every 512-column tile
+        const int g = (warp - 2) >> 2;
         const int q = warp & 3;           // TMEM lane quadrant of this warp
         const int r = q * 32 + lane;      // accumulator row == TMEM lane
         const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
-        const uint32_t tempty_leader0 = mapa_shared(smem_addr(&sm.tempty[0]), 0);
-        const uint32_t tempty_leader1 = mapa_shared(smem_addr(&sm.tempty[1]), 0);
-        int acc = 0;
+        const uint32_t tempty_leader = mapa_shared(smem_addr(&sm.tempty[g]), 0);
+        const int acc = g;
         uint32_t acc_phase = 0;
         bool ok = true;
 
@@ -418,7 +485,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
                 tc_fence_after();
                 const uint32_t tbase = tmem_base + static_cast<uint32_t>(acc * BN) + lane_off;
-                const int col0 = nt * BN;
+                const int col0 = nt * 2 * BN + g * BN;
                 const int nvalid = min(BN, p.V - col0);
                 const long long tcol = yv - col0;
 #pragma unroll 1
@@ -428,7 +495,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     tmem_wait_ld();
                     if (c == BN / 32 - 1) {
                         tc_fence_before();
-                        mbar_arrive_cluster(acc ? tempty_leader1 : tempty_leader0);
+                        mbar_arrive_cluster(tempty_leader);
                     }
                     const long long tc = tcol - c * 32;
                     if (tc >= 0 && tc < 32) {
@@ -506,13 +573,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     run_s += s0;
                     if constexpr (kEnt) run_t += t0;
                 }
-                acc ^= 1;
-                if (acc == 0) acc_phase ^= 1u;
+                acc_phase ^= 1u;
             }
             if (!ok) break;
 
             if (row_ok) {
-                const size_t o = static_cast<size_t>(t.split) * p.M + row;
+                const size_t o = static_cast<size_t>(2 * t.split + g) * p.M + row;
                 p.part_m[o] = run_m;
                 p.part_s[o] = run_s;
                 if constexpr (kEnt) p.part_t[o] = run_t;
