@@ -130,7 +130,7 @@ def load_peaks():
 
 
 class ClockSampler:
-    """nvidia-smi clocks / throttle reasons sampled every 200 ms in a thread."""
+    """nvidia-smi clocks / throttle reasons sampled every 100 ms in a thread."""
 
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -275,7 +275,8 @@ def run_ours(args, world, rank, local):
     if sched == "vsplit":
         units = flp.backward_schedule(M, H, V, ws.numel(), "vsplit", 76)
         Vt, Mt = -(-V // 256), -(-M // 256)
-        share = M * (int((units[:, 0] == 0).sum()) // Mt) / Vt
+        first = units[units[:, 0] == 0, 1]  # the first chunk's dZ launch (kind 4: two 256-column tiles)
+        share = M * (int((first == 4).sum() * 2 + (first != 4).sum()) // Mt) / Vt
     phase_flops = {"fwd": 2.0 * M * H * V, "merge": 0.0,
                    "bwd": 6.0 * M * H * V,                       # fused: every wave in one launch
                    "bwd_dz": 2.0 * share * H * V,                # split / vsplit: the first wave's / chunk's launches
@@ -283,7 +284,7 @@ def run_ours(args, world, rank, local):
     dom = max(phase_ms, key=lambda n: phase_ms[n])
     achieved = phase_flops[dom] / (phase_ms[dom] * 1e-3) / 1e12
     peak = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
-    kname = {"fwd": "flp_fwd_kernel", "bwd": "flp_bwd_kernel", "bwd_dz": "flp_bwd_kernel/dz",
+    kname = {"fwd": "flp_fwd_kernel", "bwd": "flp_bwd_kernel", "bwd_dz": "flp_dz_kernel",
              "bwd_gemm": "flp_bwd_kernel/dx_dw"}[dom]
     roofline = {"bound": "tensor", "kernel": kname, "achieved": round(achieved, 1),
                 "peak": peak, "unit": UNIT, "frac": round(achieved / peak, 4),

@@ -50,7 +50,10 @@ enum UnitKind : int { kUnitDz = 0, kUnitDx = 1, kUnitDw = 2 };
 //              tile reads a dZ column written a few blocks earlier (in L2)
 //   kSegDx2  : wide (256 x 512) dX tiles of row tiles [a0, a0 + an); 512-column
 //              hidden tiles outer
-enum SegKind : int { kSegDz = 0, kSegDx = 1, kSegDw = 2, kSegDzDw = 3, kSegDx2 = 4 };
+//   kSegDz2  : wide (256 x 512) dZ tiles of row tiles [a0, a0 + an), vocabulary
+//              tiles (b0 + 2c, b0 + 2c + 1) for c = 0, 1, ...; vocabulary outer
+//              (run by flp_dz_kernel, never mixed with other kinds)
+enum SegKind : int { kSegDz = 0, kSegDx = 1, kSegDw = 2, kSegDzDw = 3, kSegDx2 = 4, kSegDz2 = 5 };
 
 struct BwdSeg {
     int start;  // first ticket
@@ -80,6 +83,7 @@ struct BwdParams {
     int static_order;  // 1: pair p runs units p, p + pairs, ... (no tickets, no hand-off ring)
     int dw_add0;     // wave 0 adds into dW (accumulate); later waves always add
     int vt0;         // first vocabulary tile of this launch's vocabulary chunk (0: all of V)
+    int vt_end;      // end of this launch's vocabulary tiles (wide dZ tiles store no half at or past it)
     int dx_add;      // dX tiles add into their (fp32) output (later vocabulary chunks)
     int dx_f32;      // dX boxes in fp32 (else bf16)
     int dw_bf16;     // dW boxes in bf16 (one wave, no accumulation; else fp32)
@@ -106,8 +110,9 @@ struct BwdParams {
 struct BUnit {
     int kind, wave;
     int mt;    // dZ, dX: row tile of the wave; dW: vocabulary tile
-    int nt;    // dZ: vocabulary tile; dX, dW: hidden tile (of 512 columns for a wide dX tile)
-    int wide;  // a 256 x 512 dX tile
+    int nt;    // dZ: vocabulary tile (the first of two for a wide one); dX, dW: hidden tile
+               // (of 512 columns for a wide dX tile)
+    int wide;  // a 256 x 512 tile
 };
 
 __host__ __device__ __forceinline__ BUnit decode_bwd(const BwdParams& p, int u) {
@@ -140,6 +145,11 @@ __host__ __device__ __forceinline__ BUnit decode_bwd(const BwdParams& p, int u) 
         t.kind = kUnitDx;
         t.wide = 1;
         t.nt = off / s.an;
+        t.mt = s.a0 + off % s.an;
+    } else if (s.kind == kSegDz2) {
+        t.kind = kUnitDz;
+        t.wide = 1;
+        t.nt = s.b0 + 2 * (off / s.an);
         t.mt = s.a0 + off % s.an;
     } else {
         const int blk = s.an + p.Nh;
@@ -219,6 +229,49 @@ __device__ __forceinline__ DzRow dz_row(const BwdParams& p, int grow, bool in_wa
     return d;
 }
 
+// dZ of 32 columns of this thread's row, from the accumulator columns at
+// taddr (vocabulary columns cb, cb + 32), as 16 packed bf16 pairs.  With
+// `release`, the accumulator is released after the TMEM read.
+__device__ __forceinline__ void dz_words32(uint32_t taddr, int cb, int V, float scale2, const DzRow& d,
+                                           bool release, uint32_t tempty, uint32_t (&w)[16]) {
+    uint32_t v[32];
+    tmem_ld_32x32b_x32(taddr, v);
+    tmem_wait_ld();
+    if (release) {
+        tc_fence_before();
+        mbar_arrive_cluster(tempty);
+    }
+    float dz[32];
+    {
+        // packed fp32 pairs: p = 2^(acc s log2e - lse2), dz = p (K1 + K2 acc)
+        const uint64_t sc2 = f2_pack(scale2, scale2);
+        const uint64_t nl = f2_pack(-d.lse2, -d.lse2);
+        const uint64_t k1 = f2_pack(d.K1, d.K1), k2 = f2_pack(d.K2, d.K2);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            const uint64_t a = f2_pack(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
+            float x0, x1;
+            f2_unpack(f2_fma(a, sc2, nl), x0, x1);
+            const uint64_t pp = f2_pack(ex2_approx(x0), ex2_approx(x1));
+            f2_unpack(f2_mul(pp, f2_fma(a, k2, k1)), dz[2 * j], dz[2 * j + 1]);
+        }
+    }
+    const long long tc = d.y - cb;
+    if (tc >= 0 && tc < 32) {
+        const uint32_t bit = 1u << static_cast<int>(tc);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) dz[j] += ((bit >> j) & 1u) ? d.Bc : 0.f;
+    }
+    const int nv = V - cb;
+    if (nv < 32) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+            if (j >= nv) dz[j] = 0.f;
+    }
+#pragma unroll
+    for (int j = 0; j < 16; ++j) w[j] = pack_bf16x2(dz[2 * j], dz[2 * j + 1]);
+}
+
 // One 256-column dZ tile of this thread's row: 4 store boxes of 64 bf16
 // columns; the accumulator is released after its last TMEM read.
 __device__ __forceinline__ void dz_tile_epilogue(StoreRing& ring, uint8_t* smem, int et, int r,
@@ -231,43 +284,11 @@ __device__ __forceinline__ void dz_tile_epilogue(StoreRing& ring, uint8_t* smem,
         uint32_t w[32];
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-            uint32_t v[32];
-            tmem_ld_32x32b_x32(tbase + b * 64 + h * 32, v);
-            tmem_wait_ld();
-            if (b == BN / 64 - 1 && h == 1) {
-                tc_fence_before();
-                mbar_arrive_cluster(tempty);
-            }
-            const int cbase = col0 + b * 64 + h * 32;
-            float dz[32];
-            {
-                // packed fp32 pairs: p = 2^(acc s log2e - lse2), dz = p (K1 + K2 acc)
-                const uint64_t sc2 = f2_pack(scale2, scale2);
-                const uint64_t nl = f2_pack(-d.lse2, -d.lse2);
-                const uint64_t k1 = f2_pack(d.K1, d.K1), k2 = f2_pack(d.K2, d.K2);
+            uint32_t wh[16];
+            dz_words32(tbase + b * 64 + h * 32, col0 + b * 64 + h * 32, V, scale2, d,
+                       b == BN / 64 - 1 && h == 1, tempty, wh);
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const uint64_t a = f2_pack(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
-                    float x0, x1;
-                    f2_unpack(f2_fma(a, sc2, nl), x0, x1);
-                    const uint64_t pp = f2_pack(ex2_approx(x0), ex2_approx(x1));
-                    f2_unpack(f2_mul(pp, f2_fma(a, k2, k1)), dz[2 * j], dz[2 * j + 1]);
-                }
-            }
-            const long long tc = d.y - cbase;
-            if (tc >= 0 && tc < 32) {
-                const uint32_t bit = 1u << static_cast<int>(tc);
-#pragma unroll
-                for (int j = 0; j < 32; ++j) dz[j] += ((bit >> j) & 1u) ? d.Bc : 0.f;
-            }
-            const int nv = V - cbase;
-            if (nv < 32) {
-#pragma unroll
-                for (int j = 0; j < 32; ++j)
-                    if (j >= nv) dz[j] = 0.f;
-            }
-#pragma unroll
-            for (int j = 0; j < 16; ++j) w[h * 16 + j] = pack_bf16x2(dz[2 * j], dz[2 * j + 1]);
+            for (int j = 0; j < 16; ++j) w[h * 16 + j] = wh[j];
         }
         stage_row(box, r, w);
         store_box_release(ring, smem, et, out, out_col0 + b * 64, out_row, false);
@@ -314,6 +335,9 @@ __device__ __forceinline__ void gemm_tile_epilogue(StoreRing& ring, uint8_t* sme
 // launch of dZ tiles alone (or of dX and dW tiles alone) carries no code for
 // the others.
 constexpr int kHasDz = 1, kHasDx = 2, kHasDw = 4;
+constexpr int kHasDzWide = 8;  // a launch of wide dZ tiles alone: flp_dz_kernel
+constexpr uint32_t DZ_BOX_BYTES = BM * 32 * 2;  // flp_dz_kernel's store box: 128 rows x 32 bf16
+static_assert(4 * DZ_BOX_BYTES <= NUM_STG * STG_BYTES, "two boxes per epilogue group");
 
 struct UnitClass {
     bool dz, dx, wide;  // dW when neither dz nor dx
@@ -687,6 +711,143 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (!ok) {
             raise_abort(sm, p.err);
         }
+        if (et == 0) bulk_wait_group<0>();
+    }
+
+    pair_epilogue(sm, warp, tmem_base);
+}
+
+// ------------------------------------------------------------ wide dZ tiles
+
+// The dZ launch of the split and vocabulary-split schedules (kSegDz2 segments,
+// equal tiles with K = H, a static round-robin over the pairs), built like the
+// forward: 256 x 512 tiles in both accumulators with the halves staggered at
+// the tile ends (wide_tile_mma), and two epilogue groups of four warps, group g
+// draining half g into its own store box.  A group computes a box's dZ before
+// it waits for that box's previous bulk store to finish reading it.  A half at
+// or past the launch's last vocabulary tile (odd tile counts) is computed but
+// not stored.  Each half runs the MMAs and the epilogue arithmetic of a
+// 256 x 256 dZ tile of flp_bwd_kernel, so both give the same bits.
+__global__ void __launch_bounds__(WIDE_THREADS, 1)
+    flp_dz_kernel(const __grid_constant__ CUtensorMap tmXk,  // X, K-major A (64 x 128 boxes)
+                  const __grid_constant__ CUtensorMap tmWk,  // W, K-major B (64 x 128)
+                  const __grid_constant__ CUtensorMap tmDz,  // dZ buffer: store boxes (32 x 128, 64-byte swizzle)
+                  const __grid_constant__ BwdParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    const Smem sm = smem_layout(smem_raw);
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
+    const bool leader = (rank == 0);
+    const int rofs = static_cast<int>(rank) * BM;
+    const int pair = blockIdx.x >> 1;
+    const int npairs = gridDim.x >> 1;
+
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmXk);
+        tma_prefetch_desc(&tmWk);
+        tma_prefetch_desc(&tmDz);
+    }
+    const uint32_t tmem_base = pair_prologue(sm, warp);
+    const uint64_t limit = p.wait_limit_ns;
+    volatile int* abort_flag = sm.abort_flag;
+
+    if (warp == 0) {
+        // ------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            for (int u = pair; u < p.total && ok; u += npairs) {
+                const BUnit t = decode_bwd(p, u);
+                const WaveInfo wi = wave_info(p, t.wave);
+                for (int kb = 0; kb < p.KB_h; ++kb) {
+                    if (!mbar_wait(&sm.empty[stage], phase ^ 1u, limit, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    load_wide_kblock(sm, stage, leader, &tmXk, wi.r0 + t.mt * PM + rofs, &tmWk,
+                                     t.nt * BN + rofs, kb);
+                    if (++stage == STAGES_W) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (!ok) raise_abort(sm, p.err);
+        }
+    } else if (warp == 1) {
+        // ---------------------------------------------- MMA issuer (leader)
+        if (lane == 0 && leader) {
+            uint32_t gk = 0;
+            uint32_t acc_phase = 0;
+            bool ok = true;
+            for (int u = pair; u < p.total && ok; u += npairs) {
+                ok = wide_tile_mma(sm, tmem_base, gk, acc_phase, p.KB_h, limit, abort_flag);
+                acc_phase ^= 1u;
+            }
+            if (!ok) raise_abort(sm, p.err);
+            umma_commit_pair_mc(sm.drain, 0x1);  // every MMA issued so far has completed
+            volatile int no_abort = 0;
+            mbar_wait(sm.drain, 0, limit, &no_abort);
+        }
+    } else {
+        // --------------------------------------------------------- epilogue
+        const int g = (warp - 2) >> 2;                 // the half this group drains
+        const int et = threadIdx.x - 64 - g * EPI_THREADS;  // 0..127; thread 0 issues the bulk stores
+        const int q = warp & 3;                        // TMEM lane quadrant of this warp
+        const int r = q * 32 + lane;                   // accumulator row == TMEM lane
+        const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
+        const uint32_t tempty = mapa_shared(smem_addr(&sm.tempty[g]), 0);
+        const uint32_t bar_box = 1 + g, bar_vote = 3 + g;  // named barriers of this group
+        // two store boxes per group (128 rows x 32 bf16 columns, 64-byte swizzle)
+        uint8_t* box_ptr = sm.base + SMEM_STG + g * (2 * DZ_BOX_BYTES);
+        uint32_t nbox = 0;  // boxes stored by this group so far; box nbox & 1 is next
+        uint32_t acc_phase = 0;
+        bool ok = true;
+        for (int u = pair; u < p.total; u += npairs) {
+            const BUnit t = decode_bwd(p, u);
+            const WaveInfo wi = wave_info(p, t.wave);
+            const int lrow = t.mt * PM + rofs + r;  // row inside the wave
+            const DzRow d = dz_row(p, wi.r0 + lrow, lrow < wi.rows);
+            const bool ready = mbar_wait(&sm.tfull[g], acc_phase, limit, abort_flag);
+            // every thread of the group takes the same branch (the box barriers need all of them)
+            if (!named_bar_all(bar_vote, EPI_THREADS, ready)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const int vt = t.nt + g;  // this half's vocabulary tile
+            const uint32_t tbase = tmem_base + static_cast<uint32_t>(g * BN) + lane_off;
+            if (vt < p.vt_end) {
+#pragma unroll 1
+                for (int b = 0; b < BN / 32; ++b) {
+                    uint32_t w[16];
+                    dz_words32(tbase + b * 32, vt * BN + b * 32, p.V, p.scale2, d, b == BN / 32 - 1, tempty, w);
+                    // box nbox & 1 was last read by the store two boxes back, which thread 0
+                    // waited for before the previous barrier
+                    uint8_t* bp = box_ptr + (nbox & 1u) * DZ_BOX_BYTES;
+                    const uint32_t row_addr = smem_addr(bp) + r * 64;
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+                        st_shared_v4(row_addr + ((c ^ ((r >> 1) & 3)) << 4), w[4 * c], w[4 * c + 1], w[4 * c + 2],
+                                     w[4 * c + 3]);
+                    fence_proxy_async_smem();
+                    if (et == 0) bulk_wait_group_read<0>();  // the other box is free again
+                    named_bar_sync(bar_box, EPI_THREADS);
+                    if (et == 0) {
+                        tma_store_2d(&tmDz, bp, (vt - p.vt0) * BN + b * 32, t.mt * PM + rofs);
+                        bulk_commit_group();
+                    }
+                    ++nbox;
+                }
+            } else {
+                tc_fence_before();
+                mbar_arrive_cluster(tempty);
+            }
+            acc_phase ^= 1u;
+        }
+        if (!ok) raise_abort(sm, p.err);
         if (et == 0) bulk_wait_group<0>();
     }
 

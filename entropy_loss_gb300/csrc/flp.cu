@@ -118,7 +118,7 @@ flp_status get_encode(PFN_cuTensorMapEncodeTiled_v12000* fn) {
 // 2-D tiled tensor map, 128-byte swizzle, zero fill outside the tensor.
 flp_status tmap_2d(CUtensorMap* tm, CUtensorMapDataType dt, const void* base, uint64_t inner,
                    uint64_t outer, uint64_t row_pitch_bytes, uint32_t box_inner,
-                   uint32_t box_outer) {
+                   uint32_t box_outer, CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
     PFN_cuTensorMapEncodeTiled_v12000 enc;
     flp_status st = get_encode(&enc);
     if (st != FLP_OK) return st;
@@ -127,7 +127,7 @@ flp_status tmap_2d(CUtensorMap* tm, CUtensorMapDataType dt, const void* base, ui
     cuuint32_t box[2] = {box_inner, box_outer};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = enc(tm, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
-                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) {
         char buf[160];
@@ -311,7 +311,7 @@ flp_status ensure_attrs(DevInfo* d) {
     if (e == cudaSuccess) e = set_fwd_smem_attr<true>();
     if (e == cudaSuccess) e = set_fwd_smem_attr<false>();
     if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(flp_bwd_kernel<kHasDz>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_ALLOC);
+        e = cudaFuncSetAttribute(flp_dz_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_ALLOC);
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(flp_bwd_kernel<kHasDx | kHasDw>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  SMEM_ALLOC);
@@ -404,7 +404,7 @@ flp_status launch_pairs(void (*kernel)(KArgs...), int grid, cudaStream_t s, cons
 template <bool kEnt>
 flp_status launch_fwd(int grid, const CUtensorMap& a, const CUtensorMap& b, const FwdParams& p,
                       cudaStream_t s) {
-    return launch_pairs_n(flp_fwd_kernel<kEnt>, grid, FWD_THREADS, s, "flp_fwd_kernel launch", a, b, p);
+    return launch_pairs_n(flp_fwd_kernel<kEnt>, grid, WIDE_THREADS, s, "flp_fwd_kernel launch", a, b, p);
 }
 
 flp_status common_checks(const void* X, const void* W, const int64_t* targets, int64_t M,
@@ -691,6 +691,7 @@ flp_status plan_backward_launches(int64_t M, int64_t H, int64_t V, const BwdChoi
         a.p.KB_v = (vt1 - vt0) * (BN / BK);
         a.p.Ndx = SegList::dx_per_row(Nh, a.p.KB_v);
         a.p.vt0 = vt0;
+        a.p.vt_end = vt1;
         a.p.M = static_cast<int>(rows);
         a.p.chunk = static_cast<int>(rows);
         a.p.nwaves = 1;
@@ -701,15 +702,16 @@ flp_status plan_backward_launches(int64_t M, int64_t H, int64_t V, const BwdChoi
         const int GM = std::min(Mt, gm_rows);
         LaunchSpec b = a;
         b.p.dx_add = dx_add ? 1 : 0;
-        a.p.static_order = 1;  // equal-length dZ tiles: static round-robin
+        a.p.static_order = 1;  // equal-length wide dZ tiles: static round-robin (flp_dz_kernel)
         a.mark_begin = first ? 4 : -1;
         a.mark_end = first ? 5 : -1;
         b.mark_begin = first ? 6 : -1;
         b.mark_end = first ? 7 : -1;
         SegList dzs{&a.p};
+        const int nw = (vt1 - vt0 + 1) / 2;  // 512-column dZ tiles per row tile
         for (int m0 = 0; m0 < Mt; m0 += GM) {
             const int gm = std::min(GM, Mt - m0);
-            dzs.add(kSegDz, 0, m0, gm, vt0, 0, static_cast<int64_t>(gm) * (vt1 - vt0));
+            dzs.add(kSegDz2, 0, m0, gm, vt0, 0, static_cast<int64_t>(gm) * nw);
         }
         SegList gl{&b.p};
         gl.dx_rows(0, 0, Mt, Nh, a.p.KB_v);
@@ -784,6 +786,7 @@ flp_status plan_backward_launches(int64_t M, int64_t H, int64_t V, const BwdChoi
 
 struct BwdMaps {
     CUtensorMap Xk, Wk, Dz, Wmn, DzMn, Xmn, Dx, Dw;
+    CUtensorMap DzSt;  // dZ buffer: the wide dZ tiles' 32-column store boxes (64-byte swizzle)
 };
 
 // The tile kinds (kHasDz | kHasDx | kHasDw) a launch's segments hold.
@@ -792,6 +795,7 @@ int launch_kinds(const BwdParams& p) {
     for (int i = 0; i < p.nseg; ++i) {
         switch (p.seg[i].kind) {
             case kSegDz: k |= kHasDz; break;
+            case kSegDz2: k |= kHasDzWide; break;
             case kSegDx:
             case kSegDx2: k |= kHasDx; break;
             case kSegDw: k |= kHasDw; break;
@@ -809,9 +813,9 @@ flp_status launch_bwd(int pairs, const BwdMaps& m, const BwdParams& p, unsigned 
     if (!p.static_order) *ticket_base += static_cast<unsigned long long>(p.total) + np;
     const char* what = "flp_bwd_kernel launch";
     switch (launch_kinds(p)) {
-        case kHasDz:
-            return launch_pairs(flp_bwd_kernel<kHasDz>, 2 * np, s, what, m.Xk, m.Wk, m.Dz, m.Wmn, m.DzMn,
-                                m.Xmn, m.Dx, m.Dw, p);
+        case kHasDzWide:
+            return launch_pairs_n(flp_dz_kernel, 2 * np, WIDE_THREADS, s, "flp_dz_kernel launch", m.Xk, m.Wk,
+                                  m.DzSt, p);
         case kHasDx | kHasDw:
             return launch_pairs(flp_bwd_kernel<kHasDx | kHasDw>, 2 * np, s, what, m.Xk, m.Wk, m.Dz, m.Wmn,
                                 m.DzMn, m.Xmn, m.Dx, m.Dw, p);
@@ -904,6 +908,9 @@ flp_status flp_backward_ex(const void* X, const void* W, const int64_t* targets,
         if ((e = tmap_2d(&m.Dz, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dz, dz_cols, dz_rows, dz_cols * 2, BK, BM)) != FLP_OK)
             return e;
         if ((e = tmap_2d(&m.DzMn, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dz, dz_cols, dz_rows, dz_cols * 2, 64, 64)) != FLP_OK)
+            return e;
+        if ((e = tmap_2d(&m.DzSt, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dz, dz_cols, dz_rows, dz_cols * 2, 32, BM,
+                         CU_TENSOR_MAP_SWIZZLE_64B)) != FLP_OK)
             return e;
         if (dx_scratch)
             return tmap_2d(&m.Dx, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, scr + r0 * H, H, rows, H * 4, 32, BM);
@@ -1000,7 +1007,8 @@ flp_status flp_backward_schedule(int64_t M, int64_t H, int64_t V, size_t workspa
             const BUnit t = decode_bwd(p, u);
             int32_t* e = units + 5 * n;
             e[0] = static_cast<int32_t>(li);
-            e[1] = t.wide ? 3 : t.kind;
+            // a wide dZ tile with its second half past the launch's vocabulary is listed as a dZ tile
+            e[1] = !t.wide ? t.kind : (t.kind == kUnitDx ? 3 : (t.nt + 1 < p.vt_end ? 4 : kUnitDz));
             e[2] = t.wave + w0;  // split launches number their one wave 0
             e[3] = t.mt;
             e[4] = t.nt;

@@ -53,7 +53,7 @@ constexpr int UMMA_K = 16;        // K per tcgen05.mma (bf16)
 constexpr int STAGES = 6;
 constexpr int NUM_THREADS = 192;
 constexpr int EPI_THREADS = 128;
-constexpr int FWD_THREADS = 64 + 2 * EPI_THREADS;  // the forward: two epilogue groups of four warps
+constexpr int WIDE_THREADS = 64 + 2 * EPI_THREADS;  // wide-tile kernels (forward, dZ): two epilogue groups of four warps
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint16_t PAIR_MASK = 0x3;
 
@@ -266,6 +266,91 @@ __device__ __forceinline__ void tmem_row64_to_bf16(uint32_t taddr, uint32_t (&w)
     }
 }
 
+// ------------------------------------------------------ wide (256 x 512) tiles
+
+// k-blocks issued half by half at each end of a wide tile (at most the number
+// of wide slots: those k-blocks' stages stay held until both halves ran)
+constexpr int WIDE_EDGE = STAGES_W;
+
+// Producer: one 64-deep k-block of a wide tile whose operands are both K-major
+// into wide slot `stage`: this CTA's 128 rows of A (from row a_row) and its
+// 128-row halves of the two 256-row B sub-tiles (from rows b_row, b_row + 256).
+__device__ __forceinline__ void load_wide_kblock(const Smem& sm, int stage, bool leader,
+                                                 const CUtensorMap* tmA, int a_row,
+                                                 const CUtensorMap* tmB, int b_row, int kb) {
+    if (leader) mbar_arrive_expect_tx(&sm.full[stage], PAIR_STAGE_TX_W);
+    const uint32_t bar = mapa_shared(smem_addr(&sm.full[stage]), 0);
+    tma_load_2d_pair(sm.base + slot_a(true, stage), tmA, kb * BK, a_row, bar);
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+        tma_load_2d_pair(sm.base + slot_b(true, stage) + h * B_STAGE_BYTES, tmB, kb * BK, b_row + h * BN, bar);
+}
+
+// MMA issuer: every MMA of one wide tile with K-major operands (KB k-blocks),
+// half h into accumulator h, then tfull[h] per half.  `gk` counts the
+// k-blocks consumed so far (slot gk % STAGES_W, fill parity
+// (gk / STAGES_W) & 1) and advances by KB; acc_phase is this tile's use
+// parity of the accumulators.  The first and last WIDE_EDGE k-blocks are
+// issued half by half: at the end of the tile half 0 completes (and its
+// epilogue starts) while the half-1 MMAs of those k-blocks still run, and at
+// the start half 0 fills while the previous tile's half 1 is still drained.
+// Returns false when a wait ran out.
+__device__ __forceinline__ bool wide_tile_mma(const Smem& sm, uint32_t tmem_base, uint32_t& gk,
+                                              uint32_t acc_phase, int KB, uint64_t limit,
+                                              volatile int* abort_flag) {
+    constexpr uint32_t idesc = idesc_bf16_f32(PM, BN, 0, 0);
+    auto issue = [&](uint32_t g, int h, int kb) {
+        const int s = static_cast<int>(g % STAGES_W);
+        const uint32_t a_base = smem_addr(sm.base + slot_a(true, s));
+        const uint32_t b_base = smem_addr(sm.base + slot_b(true, s)) + h * B_STAGE_BYTES;
+#pragma unroll
+        for (int k = 0; k < BK / UMMA_K; ++k)
+            umma_bf16_pair(tmem_base + static_cast<uint32_t>(h * BN), operand_desc<0>(a_base, k),
+                           operand_desc<0>(b_base, k), idesc, (kb > 0 || k > 0) ? 1u : 0u);
+    };
+    auto wait_full = [&](uint32_t g) {
+        if (!mbar_wait(&sm.full[g % STAGES_W], (g / STAGES_W) & 1u, limit, abort_flag)) return false;
+        tc_fence_after();
+        return true;
+    };
+    auto release = [&](uint32_t g) {
+        umma_commit_pair_mc(&sm.empty[g % STAGES_W], PAIR_MASK);  // stage free in both CTAs
+    };
+    const int head = min(WIDE_EDGE, KB);
+    const int tail0 = max(head, KB - WIDE_EDGE);
+    if (!mbar_wait(&sm.tempty[0], acc_phase ^ 1u, limit, abort_flag)) return false;
+    tc_fence_after();
+    for (int kb = 0; kb < head; ++kb) {
+        if (!wait_full(gk + kb)) return false;
+        issue(gk + kb, 0, kb);
+    }
+    if (head == KB) umma_commit_pair_mc(&sm.tfull[0], PAIR_MASK);
+    if (!mbar_wait(&sm.tempty[1], acc_phase ^ 1u, limit, abort_flag)) return false;
+    tc_fence_after();
+    for (int kb = 0; kb < head; ++kb) {
+        issue(gk + kb, 1, kb);
+        release(gk + kb);
+    }
+    for (int kb = head; kb < tail0; ++kb) {
+        if (!wait_full(gk + kb)) return false;
+        issue(gk + kb, 0, kb);
+        issue(gk + kb, 1, kb);
+        release(gk + kb);
+    }
+    for (int kb = tail0; kb < KB; ++kb) {
+        if (!wait_full(gk + kb)) return false;
+        issue(gk + kb, 0, kb);
+    }
+    if (head < KB) umma_commit_pair_mc(&sm.tfull[0], PAIR_MASK);  // half 0 ready in both CTAs
+    for (int kb = tail0; kb < KB; ++kb) {
+        issue(gk + kb, 1, kb);
+        release(gk + kb);
+    }
+    umma_commit_pair_mc(&sm.tfull[1], PAIR_MASK);  // half 1 ready in both CTAs
+    gk += static_cast<uint32_t>(KB);
+    return true;
+}
+
 // ------------------------------------------------------------ forward kernel
 
 struct FwdParams {
@@ -309,16 +394,12 @@ __device__ __forceinline__ Unit decode_unit(const FwdParams& p, int u) {
     return t;
 }
 
-// k-blocks issued half by half at each end of a forward tile (at most the
-// number of wide slots: those k-blocks' stages stay held until both halves ran)
-constexpr int FWD_EDGE = STAGES_W;
 template <bool kEnt>
-__global__ void __launch_bounds__(FWD_THREADS, 1)
+__global__ void __launch_bounds__(WIDE_THREADS, 1)
     flp_fwd_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const FwdParams p) {
     extern __shared__ uint8_t smem_raw[];
     const Smem sm = smem_layout(smem_raw);
-    uint8_t* smem = sm.base;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const uint32_t rank = cluster_ctarank();
@@ -353,14 +434,8 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
                             ok = false;
                             break;
                         }
-                        if (leader) mbar_arrive_expect_tx(&sm.full[stage], PAIR_STAGE_TX_W);
-                        const uint32_t bar = mapa_shared(smem_addr(&sm.full[stage]), 0);
-                        tma_load_2d_pair(smem + slot_a(true, stage), &tmA, kb * BK,
-                                         t.mt * PM + static_cast<int>(rank) * BM, bar);
-#pragma unroll
-                        for (int h = 0; h < 2; ++h)
-                            tma_load_2d_pair(smem + slot_b(true, stage) + h * B_STAGE_BYTES, &tmB, kb * BK,
-                                             nt * 2 * BN + h * BN + static_cast<int>(rank) * BNH, bar);
+                        load_wide_kblock(sm, stage, leader, &tmA, t.mt * PM + static_cast<int>(rank) * BM,
+                                         &tmB, nt * 2 * BN + static_cast<int>(rank) * BNH, kb);
                         ++issued;
                         if (++stage == STAGES_W) {
                             stage = 0;
@@ -375,78 +450,14 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
         }
     } else if (warp == 1) {
         // ---------------------------------------------- MMA issuer (leader)
-        // A 512-column tile uses both accumulators, half h in accumulator h.
-        // The first and last `edge` k-blocks are issued half by half: at the
-        // end of a tile half 0 completes (and its epilogue starts) while the
-        // half-1 MMAs of those k-blocks still run, and at the start of the
-        // next tile half 0 fills while half 1 is still being drained.
         if (lane == 0 && leader) {
-            uint32_t gk = 0;  // k-blocks consumed so far: stage gk % STAGES_W, parity (gk / STAGES_W) & 1
+            uint32_t gk = 0;
             uint32_t acc_phase = 0;
             bool ok = true;
-            constexpr uint32_t idesc = idesc_bf16_f32(PM, BN, 0, 0);
-            constexpr int edge = FWD_EDGE;
-            auto issue = [&](uint32_t g, int h, int kb) {
-                const int s = static_cast<int>(g % STAGES_W);
-                const uint32_t a_base = smem_addr(smem + slot_a(true, s));
-                const uint32_t b_base = smem_addr(smem + slot_b(true, s)) + h * B_STAGE_BYTES;
-#pragma unroll
-                for (int k = 0; k < BK / UMMA_K; ++k)
-                    umma_bf16_pair(tmem_base + static_cast<uint32_t>(h * BN), operand_desc<0>(a_base, k),
-                                   operand_desc<0>(b_base, k), idesc, (kb > 0 || k > 0) ? 1u : 0u);
-            };
-            auto wait_full = [&](uint32_t g) {
-                if (!mbar_wait(&sm.full[g % STAGES_W], (g / STAGES_W) & 1u, limit, abort_flag)) return false;
-                tc_fence_after();
-                return true;
-            };
-            auto release = [&](uint32_t g) {
-                umma_commit_pair_mc(&sm.empty[g % STAGES_W], PAIR_MASK);  // stage free in both CTAs
-            };
             for (int u = pair; u < p.units && ok; u += npairs) {
                 const Unit t = decode_unit(p, u);
                 for (int nt = t.n0; nt < t.n1 && ok; ++nt) {
-                    const int head = min(edge, p.KB);
-                    const int tail0 = max(head, p.KB - edge);
-                    if (!mbar_wait(&sm.tempty[0], acc_phase ^ 1u, limit, abort_flag)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    for (int kb = 0; kb < head && ok; ++kb) {
-                        ok = wait_full(gk + kb);
-                        if (ok) issue(gk + kb, 0, kb);
-                    }
-                    if (!ok) break;
-                    if (head == p.KB) umma_commit_pair_mc(&sm.tfull[0], PAIR_MASK);
-                    if (!mbar_wait(&sm.tempty[1], acc_phase ^ 1u, limit, abort_flag)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    for (int kb = 0; kb < head; ++kb) {
-                        issue(gk + kb, 1, kb);
-                        release(gk + kb);
-                    }
-                    for (int kb = head; kb < tail0 && ok; ++kb) {
-                        ok = wait_full(gk + kb);
-                        if (!ok) break;
-                        issue(gk + kb, 0, kb);
-                        issue(gk + kb, 1, kb);
-                        release(gk + kb);
-                    }
-                    for (int kb = tail0; kb < p.KB && ok; ++kb) {
-                        ok = wait_full(gk + kb);
-                        if (ok) issue(gk + kb, 0, kb);
-                    }
-                    if (!ok) break;
-                    if (head < p.KB) umma_commit_pair_mc(&sm.tfull[0], PAIR_MASK);  // half 0 ready in both CTAs
-                    for (int kb = tail0; kb < p.KB; ++kb) {
-                        issue(gk + kb, 1, kb);
-                        release(gk + kb);
-                    }
-                    umma_commit_pair_mc(&sm.tfull[1], PAIR_MASK);  // half 1 ready in both CTAs
-                    gk += static_cast<uint32_t>(p.KB);
+                    ok = wide_tile_mma(sm, tmem_base, gk, acc_phase, p.KB, limit, abort_flag);
                     acc_phase ^= 1u;
                 }
             }
@@ -656,6 +667,7 @@ __device__ __forceinline__ Stats combine(Stats a, Stats b) {
 
 constexpr int MERGE_ROWS = 32;   // rows per block (one per lane)
 constexpr int MERGE_WAYS = 8;    // warps per block; warp w reads splits w, w + 8, ...
+constexpr int MERGE_BATCH = 8;   // splits whose loads a warp has in flight at once
 
 // Combines the per-split partials of each row into the final lse / logprob /
 // entropy (the "reduced" and "result" stages kept in buffers separate from the
@@ -669,10 +681,21 @@ __global__ void __launch_bounds__(MERGE_ROWS * MERGE_WAYS) flp_merge_kernel(cons
     const int i = blockIdx.x * MERGE_ROWS + lane;
     Stats acc{-INFINITY, 0.f, 0.f};
     if (i < p.M) {
-        for (int k = w; k < p.S; k += MERGE_WAYS) {
-            const size_t o = static_cast<size_t>(k) * p.M + i;
-            Stats v{p.part_m[o], p.part_s[o], p.compute_entropy ? p.part_t[o] : 0.f};
-            acc = combine(acc, v);
+        // splits w, w + 8, w + 16, ... in order; the loads of MERGE_BATCH of
+        // them are issued before any is combined (the loop is latency-bound)
+        for (int k0 = w; k0 < p.S; k0 += MERGE_BATCH * MERGE_WAYS) {
+            Stats v[MERGE_BATCH];
+#pragma unroll
+            for (int j = 0; j < MERGE_BATCH; ++j) {
+                const int k = k0 + j * MERGE_WAYS;
+                v[j] = Stats{-INFINITY, 0.f, 0.f};
+                if (k < p.S) {
+                    const size_t o = static_cast<size_t>(k) * p.M + i;
+                    v[j] = Stats{p.part_m[o], p.part_s[o], p.compute_entropy ? p.part_t[o] : 0.f};
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < MERGE_BATCH; ++j) acc = combine(acc, v[j]);
         }
     }
     part[w][lane] = acc;

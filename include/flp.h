@@ -201,7 +201,10 @@ flp_status flp_backward_plan(int64_t M, int64_t H, int64_t V, size_t workspace_b
  * tile of the wave, b = vocabulary tile), 1 = dX tile (a = row tile, b =
  * hidden tile), 2 = dW tile (a = vocabulary tile, b = hidden tile), 3 = wide
  * dX tile (a = row tile, b = 512-column hidden tile: the hidden tiles 2b and
- * 2b + 1); tiles are 256 x 256 except the wide ones.  At most `capacity` entries are written; *count receives the
+ * 2b + 1), 4 = wide dZ tile (a = row tile, b = its first vocabulary tile: the
+ * vocabulary tiles b and b + 1; one whose second half lies past the launch's
+ * vocabulary is listed as the dZ tile b, kind 0); tiles are 256 x 256 except
+ * the wide ones.  At most `capacity` entries are written; *count receives the
  * total.  units may be NULL to query the count.
  */
 flp_status flp_backward_schedule(int64_t M, int64_t H, int64_t V, size_t workspace_bytes,

@@ -7,16 +7,19 @@ earlier ticket, which is what rules out a deadlock of the persistent launch."""
 import numpy as np
 import pytest
 
-DZ, DX, DW, DX2 = 0, 1, 2, 3
+DZ, DX, DW, DX2, DZ2 = 0, 1, 2, 3, 4
 
 
 def narrow(u):
     """Units as (kind, wave, a, b) 256 x 256 tiles; a wide dX tile (kind 3,
-    512-column hidden tile b) counts as the dX tiles 2b and 2b + 1."""
+    512-column hidden tile b) counts as the dX tiles 2b and 2b + 1, a wide dZ
+    tile (kind 4, first vocabulary tile b) as the dZ tiles b and b + 1."""
     out = []
     for _, k, w, a, b in u.tolist():
         if k == DX2:
             out += [(DX, w, a, 2 * b), (DX, w, a, 2 * b + 1)]
+        elif k == DZ2:
+            out += [(DZ, w, a, b), (DZ, w, a, b + 1)]
         else:
             out.append((k, w, a, b))
     return sorted(out)
@@ -107,9 +110,12 @@ def test_split_schedule_orders_phases_by_launch(flp, M, H, V, chunk, pairs):
         sel = launch == li
         assert np.all(wave[sel] == li // 2)
         if li % 2 == 0:
-            assert np.all(kind[sel] == DZ)
+            # wide dZ tiles; a 256-column one only for an odd last vocabulary tile
+            assert np.all(np.isin(kind[sel], (DZ, DZ2)))
+            narrow_dz = u[sel & (kind == DZ)]
+            assert np.all(narrow_dz[:, 4] == cdiv(V, 256) - 1) and cdiv(V, 256) % 2 == (len(narrow_dz) > 0)
         else:
-            assert np.all(kind[sel] != DZ)
+            assert not np.any(np.isin(kind[sel], (DZ, DZ2)))
             # the long dX tiles first, the short dW tiles fill the tail
             k = np.where(kind[sel] == DX2, DX, kind[sel])
             assert np.all(np.diff(k) >= 0)
@@ -255,12 +261,13 @@ def test_vsplit_schedule(flp, M, H, V, cols):
     for c in range(chunks):
         dz = u[launch == 2 * c]
         gm = u[launch == 2 * c + 1]
-        assert np.all(dz[:, 1] == DZ) and not np.any(gm[:, 1] == DZ)
+        assert np.all(np.isin(dz[:, 1], (DZ, DZ2))) and not np.any(np.isin(gm[:, 1], (DZ, DZ2)))
         vts = set(range(c * per, min(Vt, (c + 1) * per)))
-        assert set(dz[:, 4].tolist()) == vts          # the chunk's vocabulary tiles
+        dzn = narrow(dz)
+        assert {v for _, _, _, v in dzn} == vts          # the chunk's vocabulary tiles
         dw = gm[gm[:, 1] == DW]
         assert set(dw[:, 3].tolist()) == vts
-        seen_dz += [tuple(x) for x in dz[:, 3:].tolist()]
+        seen_dz += [(m, v) for _, _, m, v in dzn]
         seen_dw += [tuple(x) for x in dw[:, 3:].tolist()]
         dx = narrow(gm[gm[:, 1] != DW])
         assert sorted(dx) == sorted((DX, 0, m, h) for m in range(Mt) for h in range(Nh))
