@@ -53,7 +53,9 @@ enum UnitKind : int { kUnitDz = 0, kUnitDx = 1, kUnitDw = 2 };
 //   kSegDz2  : wide (256 x 512) dZ tiles of row tiles [a0, a0 + an), vocabulary
 //              tiles (b0 + 2c, b0 + 2c + 1) for c = 0, 1, ...; vocabulary outer
 //              (run by flp_dz_kernel, never mixed with other kinds)
-enum SegKind : int { kSegDz = 0, kSegDx = 1, kSegDw = 2, kSegDzDw = 3, kSegDx2 = 4, kSegDz2 = 5 };
+//   kSegDw2  : wide (256 x 512) dW tiles of vocabulary tiles from b0 on;
+//              512-column hidden tiles inner
+enum SegKind : int { kSegDz = 0, kSegDx = 1, kSegDw = 2, kSegDzDw = 3, kSegDx2 = 4, kSegDz2 = 5, kSegDw2 = 6 };
 
 struct BwdSeg {
     int start;  // first ticket
@@ -104,6 +106,7 @@ struct BwdParams {
     unsigned long long ticket_base;
     int* err;
     unsigned long long wait_limit_ns;
+    int debug_stop_at;  // flp_dz_kernel self-test: 0 off; n > 0: its producers stop after n - 1 stages
     BwdSeg seg[MAX_SEGS];
 };
 
@@ -111,7 +114,7 @@ struct BUnit {
     int kind, wave;
     int mt;    // dZ, dX: row tile of the wave; dW: vocabulary tile
     int nt;    // dZ: vocabulary tile (the first of two for a wide one); dX, dW: hidden tile
-               // (of 512 columns for a wide dX tile)
+               // (of 512 columns for a wide one)
     int wide;  // a 256 x 512 tile
 };
 
@@ -151,6 +154,11 @@ __host__ __device__ __forceinline__ BUnit decode_bwd(const BwdParams& p, int u) 
         t.wide = 1;
         t.nt = s.b0 + 2 * (off / s.an);
         t.mt = s.a0 + off % s.an;
+    } else if (s.kind == kSegDw2) {
+        t.kind = kUnitDw;
+        t.wide = 1;
+        t.mt = s.b0 + off / (p.Nh / 2);
+        t.nt = off % (p.Nh / 2);
     } else {
         const int blk = s.an + p.Nh;
         const int c = off / blk;
@@ -340,7 +348,7 @@ constexpr uint32_t DZ_BOX_BYTES = BM * 32 * 2;  // flp_dz_kernel's store box: 12
 static_assert(4 * DZ_BOX_BYTES <= NUM_STG * STG_BYTES, "two boxes per epilogue group");
 
 struct UnitClass {
-    bool dz, dx, wide;  // dW when neither dz nor dx
+    bool dz, dx, wide;  // dW when neither dz nor dx; wide: a 256 x 512 dX or dW tile
 };
 
 template <int kKinds>
@@ -348,7 +356,7 @@ __device__ __forceinline__ UnitClass classify(const BUnit& t) {
     UnitClass c;
     c.dz = (kKinds == kHasDz) || ((kKinds & kHasDz) && t.kind == kUnitDz);
     c.dx = (kKinds == kHasDx) || ((kKinds & kHasDx) && !c.dz && t.kind == kUnitDx);
-    c.wide = (kKinds & kHasDx) && c.dx && t.wide;
+    c.wide = !c.dz && t.wide != 0;  // wide dZ tiles run in flp_dz_kernel only
     return c;
 }
 
@@ -501,10 +509,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         for (int j = 0; j < BM / 64; ++j)
                             tma_load_2d_pair(a_dst + j * 8192, &tmDzMn, (t.mt - p.vt0) * PM + rofs + j * 64,
                                              kb * BK, bar);
+                        const int nsub = c.wide ? 2 : 1;
+                        for (int h = 0; h < nsub; ++h) {
 #pragma unroll
-                        for (int j = 0; j < BNH / 64; ++j)
-                            tma_load_2d_pair(b_dst + j * 8192, &tmXmn, t.nt * BN + rofs + j * 64,
-                                             wi.r0 + kb * BK, bar);
+                            for (int j = 0; j < BNH / 64; ++j)
+                                tma_load_2d_pair(b_dst + h * B_STAGE_BYTES + j * 8192, &tmXmn,
+                                                 (t.nt * nsub + h) * BN + rofs + j * 64, wi.r0 + kb * BK, bar);
+                        }
                     }
                     fill_par ^= 1u << stage;
                     if (++stage == nslots) stage = 0;
@@ -520,7 +531,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             int stage = 0;
             uint32_t full_par = 0;   // bit i: parity of the consumptions of slot i so far
             bool wide_mode = false;  // slot layout in use, switched at the same units as the producer's
-            int acc = 0;             // next accumulator (a wide dX tile takes both, starting here)
+            int acc = 0;             // next accumulator (a wide tile takes both, starting here)
             uint32_t tpar = 0;       // bit a: parity of the uses of accumulator a so far
             bool ok = true;
             constexpr uint32_t idesc_kk = idesc_bf16_f32(PM, BN, 0, 0);  // dZ: X and W K-major
@@ -550,56 +561,112 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     stage = 0;
                 }
                 const int nslots = wide_mode ? STAGES_W : STAGES;
-                const int nacc = c.wide ? 2 : 1;
-                for (int h = 0; h < nacc && ok; ++h) {
-                    const int a = acc ^ h;
-                    ok = mbar_wait(&sm.tempty[a], ((tpar >> a) & 1u) ^ 1u, limit, abort_flag);
-                }
-                if (!ok) break;
-                tc_fence_after();
-                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
                 const int kbn = unit_kblocks(p, c, wi);
-                for (int kb = 0; kb < kbn; ++kb) {
-                    if (!mbar_wait(&sm.full[stage], (full_par >> stage) & 1u, limit, abort_flag)) {
+                // k-block kb of this unit sits in slot (stage + kb) % nslots
+                auto wait_full = [&](int kb) {
+                    const int s = (stage + kb) % nslots;
+                    if (!mbar_wait(&sm.full[s], (full_par >> s) & 1u, limit, abort_flag)) return false;
+                    full_par ^= 1u << s;
+                    tc_fence_after();
+                    return true;
+                };
+                auto release = [&](int kb) {
+                    umma_commit_pair_mc(&sm.empty[(stage + kb) % nslots], PAIR_MASK);  // stage free in both CTAs
+                };
+                // the MMAs of k-block kb into half h (accumulator acc ^ h; a wide
+                // tile's half h reads the B half of its 256-column sub-tile h)
+                auto issue = [&](int kb, int h) {
+                    const int s = (stage + kb) % nslots;
+                    const uint32_t a_base = smem_addr(smem + slot_a(wide_mode, s));
+                    const uint32_t b_base = smem_addr(smem + slot_b(wide_mode, s)) + h * B_STAGE_BYTES;
+                    const uint32_t d_h = tmem_base + static_cast<uint32_t>((acc ^ h) * BN);
+                    if (c.dz) {
+#pragma unroll
+                        for (int k = 0; k < BK / UMMA_K; ++k)
+                            umma_bf16_pair(d_h, operand_desc<0>(a_base, k), operand_desc<0>(b_base, k), idesc_kk,
+                                           (kb > 0 || k > 0) ? 1u : 0u);
+                    } else if (c.dx) {
+#pragma unroll
+                        for (int k = 0; k < BK / UMMA_K; ++k)
+                            umma_bf16_pair(d_h, operand_desc<0>(a_base, k), operand_desc<1>(b_base, k), idesc_km,
+                                           (kb > 0 || k > 0) ? 1u : 0u);
+                    } else {
+#pragma unroll
+                        for (int k = 0; k < BK / UMMA_K; ++k)
+                            umma_bf16_pair(d_h, operand_desc<1>(a_base, k), operand_desc<1>(b_base, k), idesc_mm,
+                                           (kb > 0 || k > 0) ? 1u : 0u);
+                    }
+                };
+                auto wait_tempty = [&](int a) {
+                    return mbar_wait(&sm.tempty[a], ((tpar >> a) & 1u) ^ 1u, limit, abort_flag);
+                };
+                auto publish = [&](int a) {
+                    umma_commit_pair_mc(&sm.tfull[a], PAIR_MASK);  // accumulator ready in both CTAs
+                    tpar ^= 1u << a;
+                };
+                if (!c.wide) {
+                    if (!wait_tempty(acc)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t a_base = smem_addr(smem + slot_a(wide_mode, stage));
-                    const uint32_t b_base = smem_addr(smem + slot_b(wide_mode, stage));
-                    if (c.dz) {
-#pragma unroll
-                        for (int k = 0; k < BK / UMMA_K; ++k)
-                            umma_bf16_pair(d_tmem, operand_desc<0>(a_base, k), operand_desc<0>(b_base, k),
-                                           idesc_kk, (kb > 0 || k > 0) ? 1u : 0u);
-                    } else if (c.dx) {
-                        // a wide tile: the same A stage against both sub-tiles' B halves,
-                        // into accumulators acc and acc ^ 1
-                        for (int h = 0; h < nacc; ++h) {
-                            const uint32_t d_h = tmem_base + static_cast<uint32_t>((acc ^ h) * BN);
-#pragma unroll
-                            for (int k = 0; k < BK / UMMA_K; ++k)
-                                umma_bf16_pair(d_h, operand_desc<0>(a_base, k),
-                                               operand_desc<1>(b_base + h * B_STAGE_BYTES, k), idesc_km,
-                                               (kb > 0 || k > 0) ? 1u : 0u);
-                        }
-                    } else {
-#pragma unroll
-                        for (int k = 0; k < BK / UMMA_K; ++k)
-                            umma_bf16_pair(d_tmem, operand_desc<1>(a_base, k), operand_desc<1>(b_base, k),
-                                           idesc_mm, (kb > 0 || k > 0) ? 1u : 0u);
+                    for (int kb = 0; kb < kbn && ok; ++kb) {
+                        ok = wait_full(kb);
+                        if (!ok) break;
+                        issue(kb, 0);
+                        release(kb);
                     }
-                    umma_commit_pair_mc(&sm.empty[stage], PAIR_MASK);  // stage free in both CTAs
-                    full_par ^= 1u << stage;
-                    if (++stage == nslots) stage = 0;
+                    if (!ok) break;
+                    publish(acc);
+                    acc ^= 1;
+                } else {
+                    // A wide tile holds both accumulators (half 0 in acc, half 1 in
+                    // acc ^ 1), so its first and last STAGES_W k-blocks are issued
+                    // half by half: half 0 completes (and is drained) while the
+                    // last half-1 MMAs run, and the next tile's half 0 starts while
+                    // this tile's half 1 is still drained.
+                    const int head = min(STAGES_W, kbn);
+                    const int tail0 = max(head, kbn - STAGES_W);
+                    if (!wait_tempty(acc)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    for (int kb = 0; kb < head && ok; ++kb) {
+                        ok = wait_full(kb);
+                        if (ok) issue(kb, 0);
+                    }
+                    if (!ok) break;
+                    if (head == kbn) publish(acc);
+                    if (!wait_tempty(acc ^ 1)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    for (int kb = 0; kb < head; ++kb) {
+                        issue(kb, 1);
+                        release(kb);
+                    }
+                    for (int kb = head; kb < tail0 && ok; ++kb) {
+                        ok = wait_full(kb);
+                        if (!ok) break;
+                        issue(kb, 0);
+                        issue(kb, 1);
+                        release(kb);
+                    }
+                    for (int kb = tail0; kb < kbn && ok; ++kb) {
+                        ok = wait_full(kb);
+                        if (ok) issue(kb, 0);
+                    }
+                    if (!ok) break;
+                    if (head < kbn) publish(acc);
+                    for (int kb = tail0; kb < kbn; ++kb) {
+                        issue(kb, 1);
+                        release(kb);
+                    }
+                    publish(acc ^ 1);  // the next tile starts at acc again
                 }
-                if (!ok) break;
-                for (int h = 0; h < nacc; ++h) {
-                    const int a = acc ^ h;
-                    umma_commit_pair_mc(&sm.tfull[a], PAIR_MASK);  // accumulator ready in both CTAs
-                    tpar ^= 1u << a;
-                }
-                if (nacc == 1) acc ^= 1;
+                stage = (stage + kbn) % nslots;
             }
             if (!ok) {
                 raise_abort(sm, p.err);
@@ -689,7 +756,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                                        (t.nt * nacc + h) * BN, wi.r0 + t.mt * PM + rofs, tempty);
                 } else {
                     gemm_tile_epilogue(ring, smem, et, r, tbase, p.dw_bf16 != 0, t.wave > 0 || p.dw_add0,
-                                       &tmDw, t.nt * BN, t.mt * PM + rofs, tempty);
+                                       &tmDw, (t.nt * nacc + h) * BN, t.mt * PM + rofs, tempty);
                 }
                 tpar ^= 1u << a;
             }
@@ -757,24 +824,30 @@ __global__ void __launch_bounds__(WIDE_THREADS, 1)
         if (lane == 0) {
             int stage = 0;
             uint32_t phase = 0;
+            int issued = 0;
             bool ok = true;
             for (int u = pair; u < p.total && ok; u += npairs) {
                 const BUnit t = decode_bwd(p, u);
                 const WaveInfo wi = wave_info(p, t.wave);
                 for (int kb = 0; kb < p.KB_h; ++kb) {
+                    if (p.debug_stop_at > 0 && issued >= p.debug_stop_at - 1) {
+                        ok = false;  // injected stall: stop feeding the MMA
+                        break;
+                    }
                     if (!mbar_wait(&sm.empty[stage], phase ^ 1u, limit, abort_flag)) {
                         ok = false;
                         break;
                     }
                     load_wide_kblock(sm, stage, leader, &tmXk, wi.r0 + t.mt * PM + rofs, &tmWk,
                                      t.nt * BN + rofs, kb);
+                    ++issued;
                     if (++stage == STAGES_W) {
                         stage = 0;
                         phase ^= 1u;
                     }
                 }
             }
-            if (!ok) raise_abort(sm, p.err);
+            if (!ok && p.debug_stop_at == 0) raise_abort(sm, p.err);
         }
     } else if (warp == 1) {
         // ---------------------------------------------- MMA issuer (leader)

@@ -715,7 +715,11 @@ flp_status plan_backward_launches(int64_t M, int64_t H, int64_t V, const BwdChoi
         }
         SegList gl{&b.p};
         gl.dx_rows(0, 0, Mt, Nh, a.p.KB_v);
-        gl.add(kSegDw, 0, 0, 0, vt0, 0, static_cast<int64_t>(vt1 - vt0) * Nh);
+        // dW tiles wide (256 x 512) when H spans an even number of 256-column tiles
+        if (Nh % 2 == 0)
+            gl.add(kSegDw2, 0, 0, 0, vt0, 0, static_cast<int64_t>(vt1 - vt0) * (Nh / 2));
+        else
+            gl.add(kSegDw, 0, 0, 0, vt0, 0, static_cast<int64_t>(vt1 - vt0) * Nh);
         if (dzs.overflow || gl.overflow) return fail(FLP_ERR_UNSUPPORTED, "backward schedule too large");
         out.push_back(a);
         out.push_back(b);
@@ -798,7 +802,8 @@ int launch_kinds(const BwdParams& p) {
             case kSegDz2: k |= kHasDzWide; break;
             case kSegDx:
             case kSegDx2: k |= kHasDx; break;
-            case kSegDw: k |= kHasDw; break;
+            case kSegDw:
+            case kSegDw2: k |= kHasDw; break;
             default: k |= kHasDz | kHasDw; break;
         }
     }
@@ -1008,7 +1013,11 @@ flp_status flp_backward_schedule(int64_t M, int64_t H, int64_t V, size_t workspa
             int32_t* e = units + 5 * n;
             e[0] = static_cast<int32_t>(li);
             // a wide dZ tile with its second half past the launch's vocabulary is listed as a dZ tile
-            e[1] = !t.wide ? t.kind : (t.kind == kUnitDx ? 3 : (t.nt + 1 < p.vt_end ? 4 : kUnitDz));
+            e[1] = !t.wide                 ? t.kind
+                   : t.kind == kUnitDx     ? 3
+                   : t.kind == kUnitDw     ? 5
+                   : t.nt + 1 < p.vt_end   ? 4
+                                           : kUnitDz;
             e[2] = t.wave + w0;  // split launches number their one wave 0
             e[3] = t.mt;
             e[4] = t.nt;
@@ -1271,6 +1280,67 @@ extern "C" flp_status flp_selftest_dependency_timeout(void* workspace, size_t wo
     p.ticket_base = 0;
     p.err = reinterpret_cast<int*>(ws);
     p.wait_limit_ns = static_cast<unsigned long long>(wait_limit_ns);
+    unsigned long long tb = 0;
+    if ((st = launch_bwd(d->pairs, m, p, &tb, s)) != FLP_OK) return st;
+    return flp_get_error(workspace, stream);
+}
+
+// The split schedule's dZ kernel (flp_dz_kernel) on a small internal all-zero
+// problem (M = 256, H = 256, V = 512: one 256 x 512 tile) laid out in the
+// workspace; stall_after >= 0 stops its producers after that many stages.
+extern "C" flp_status flp_selftest_dz_wait_timeout(void* workspace, size_t workspace_bytes,
+                                                   int stall_after, int64_t wait_limit_ns,
+                                                   void* stream) {
+    if (!workspace || !aligned16(workspace) || workspace_bytes < FLP_SELFTEST_WORKSPACE_BYTES)
+        return fail(FLP_ERR_WORKSPACE, "self-test needs FLP_SELFTEST_WORKSPACE_BYTES of workspace");
+    if (wait_limit_ns <= 0 || wait_limit_ns > 60ll * 1000 * 1000 * 1000)
+        return fail(FLP_ERR_INVALID_ARG, "wait_limit_ns must be in (0, 60 s]");
+    DevInfo* d;
+    flp_status st = check_device(&d);
+    if (st != FLP_OK) return st;
+    constexpr int64_t M = 256, H = 256, V = 512;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    const size_t off_dz = kHeaderBytes;
+    const size_t off_x = align_up(off_dz + M * V * 2, 1024);
+    const size_t off_w = off_x + align_up(M * H * 2, 1024);
+    const size_t off_y = off_w + align_up(V * H * 2, 1024);
+    const size_t off_f = off_y + align_up(M * 8, 1024);  // lse, g_lp: fp32 [M] each
+    const size_t end = off_f + 2 * M * 4;
+    if (end > FLP_SELFTEST_WORKSPACE_BYTES)
+        return fail(FLP_ERR_UNSUPPORTED, "self-test layout exceeds its workspace");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    FLP_CUDA(cudaMemsetAsync(ws, 0, end, s));  // header, dZ, inputs (zeros), targets (0)
+
+    BwdMaps m{};
+    if ((st = tmap_2d(&m.Xk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, ws + off_x, H, M, H * 2, BK, BM)) != FLP_OK)
+        return st;
+    if ((st = tmap_2d(&m.Wk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, ws + off_w, H, V, H * 2, BK, BNH)) != FLP_OK)
+        return st;
+    if ((st = tmap_2d(&m.DzSt, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, ws + off_dz, V, M, V * 2, 32, BM,
+                      CU_TENSOR_MAP_SWIZZLE_64B)) != FLP_OK)
+        return st;
+    BwdParams p{};
+    SegList sl{&p};
+    sl.add(kSegDz2, 0, 0, 1, 0, 0, 1);  // the one wide dZ tile
+    p.M = static_cast<int>(M);
+    p.V = static_cast<int>(V);
+    p.chunk = static_cast<int>(M);
+    p.nwaves = 1;
+    p.Mt_full = 1;
+    p.Vt = static_cast<int>(V / BN);
+    p.vt0 = 0;
+    p.vt_end = p.Vt;
+    p.KB_h = static_cast<int>(H / BK);
+    p.static_order = 1;
+    p.ignore_index = -100;
+    p.scale = 1.f;
+    p.scale2 = LOG2E;
+    p.y = reinterpret_cast<const long long*>(ws + off_y);
+    p.lse = reinterpret_cast<const float*>(ws + off_f);
+    p.g_lp = reinterpret_cast<const float*>(ws + off_f + M * 4);
+    p.err = reinterpret_cast<int*>(ws);
+    p.wait_limit_ns = static_cast<unsigned long long>(wait_limit_ns);
+    p.debug_stop_at = stall_after < 0 ? 0 : stall_after + 1;
     unsigned long long tb = 0;
     if ((st = launch_bwd(d->pairs, m, p, &tb, s)) != FLP_OK) return st;
     return flp_get_error(workspace, stream);

@@ -28,7 +28,8 @@ FLP_BF16 = 1
 EXPORTS = ("flp_workspace_query", "flp_forward", "flp_backward", "flp_get_error",
            "flp_set_phase_events", "flp_status_string", "flp_last_error_message",
            "flp_forward_noalloc", "flp_selftest_wait_timeout", "flp_loss", "flp_backward_ex",
-           "flp_backward_plan", "flp_backward_schedule", "flp_selftest_dependency_timeout")
+           "flp_backward_plan", "flp_backward_schedule", "flp_selftest_dependency_timeout",
+           "flp_selftest_dz_wait_timeout")
 FLP_LOSS_NLL_MEAN = 1
 FLP_LOSS_CLIPPED_SURROGATE = 2
 SELFTEST_WORKSPACE_BYTES = 1 << 20
@@ -88,6 +89,8 @@ def load(path: str = LIB_PATH):
     lib.flp_selftest_wait_timeout.restype = i32
     lib.flp_selftest_dependency_timeout.argtypes = [p, ctypes.c_size_t, i32, i64, p]
     lib.flp_selftest_dependency_timeout.restype = i32
+    lib.flp_selftest_dz_wait_timeout.argtypes = [p, ctypes.c_size_t, i32, i64, p]
+    lib.flp_selftest_dz_wait_timeout.restype = i32
     lib.flp_loss.argtypes = [p, p, i64, i64, i32, p, p, p, ctypes.c_float, ctypes.c_float,
                              ctypes.c_float, p, p, p, p]
     lib.flp_loss.restype = i32
@@ -305,6 +308,17 @@ def selftest_wait_timeout(stall_after: int, wait_limit_ns: int, workspace=None, 
         workspace = torch.empty(SELFTEST_WORKSPACE_BYTES, dtype=torch.uint8, device="cuda")
     return int(load().flp_selftest_wait_timeout(_ptr(workspace), _nbytes(workspace), stall_after,
                                                 wait_limit_ns, _stream(stream)))
+
+
+def selftest_dz_wait_timeout(stall_after: int, wait_limit_ns: int, workspace=None, stream=None) -> int:
+    """Run the backward's dZ kernel on one internal 256 x 512 tile with its
+    producers stopped after `stall_after` stages (< 0: no stall) and every wait
+    bounded by `wait_limit_ns`; returns the error status the run leaves
+    (FLP_ERR_TIMEOUT when the stall was detected, FLP_OK for a normal run)."""
+    if workspace is None:
+        workspace = torch.empty(SELFTEST_WORKSPACE_BYTES, dtype=torch.uint8, device="cuda")
+    return int(load().flp_selftest_dz_wait_timeout(_ptr(workspace), _nbytes(workspace), stall_after,
+                                                   wait_limit_ns, _stream(stream)))
 
 
 def selftest_dependency_timeout(broken: bool, wait_limit_ns: int, workspace=None, stream=None) -> int:

@@ -203,8 +203,9 @@ flp_status flp_backward_plan(int64_t M, int64_t H, int64_t V, size_t workspace_b
  * dX tile (a = row tile, b = 512-column hidden tile: the hidden tiles 2b and
  * 2b + 1), 4 = wide dZ tile (a = row tile, b = its first vocabulary tile: the
  * vocabulary tiles b and b + 1; one whose second half lies past the launch's
- * vocabulary is listed as the dZ tile b, kind 0); tiles are 256 x 256 except
- * the wide ones.  At most `capacity` entries are written; *count receives the
+ * vocabulary is listed as the dZ tile b, kind 0), 5 = wide dW tile (a =
+ * vocabulary tile, b = 512-column hidden tile: the hidden tiles 2b and
+ * 2b + 1); tiles are 256 x 256 except the wide ones.  At most `capacity` entries are written; *count receives the
  * total.  units may be NULL to query the count.
  */
 flp_status flp_backward_schedule(int64_t M, int64_t H, int64_t V, size_t workspace_bytes,
@@ -319,6 +320,22 @@ flp_status flp_selftest_wait_timeout(void* workspace, size_t workspace_bytes, in
  */
 flp_status flp_selftest_dependency_timeout(void* workspace, size_t workspace_bytes, int broken,
                                            int64_t wait_limit_ns, void* stream);
+
+/*
+ * The same self-test for the backward's dZ kernel (the split and
+ * vocabulary-split schedules' dZ launch; a diagnostic, the pages have no
+ * counterpart): one 256 x 512 dZ tile of a small internal all-zero problem
+ * (M = 256, H = 256, V = 512) laid out in `workspace` (at least
+ * FLP_SELFTEST_WORKSPACE_BYTES).  With stall_after >= 0 its TMA producers
+ * stop after that many pipeline stages: the MMA issuer's wait gives up after
+ * wait_limit_ns, the kernel records FLP_ERR_TIMEOUT, its epilogue warps stop
+ * together (a vote before any store barrier), it winds down (bounded) and
+ * returns; nothing faults and the context stays usable.  With
+ * stall_after < 0 the tile runs normally.  Synchronises `stream` and returns
+ * the error word (FLP_ERR_TIMEOUT or FLP_OK), or an argument / CUDA error.
+ */
+flp_status flp_selftest_dz_wait_timeout(void* workspace, size_t workspace_bytes, int stall_after,
+                                        int64_t wait_limit_ns, void* stream);
 
 /* Static description of a status code. */
 const char* flp_status_string(flp_status status);

@@ -137,6 +137,16 @@ def test_dependency_selftest_argument_checks_need_no_device(lib):
     assert lib.flp_selftest_dependency_timeout(base, 1 << 20, 1, 0, None) == flp.FLP_ERR_INVALID_ARG
 
 
+def test_dz_selftest_argument_checks_need_no_device(lib):
+    from entropy_loss_gb300 import flp
+    buf = ctypes.create_string_buffer(64)
+    base = (ctypes.addressof(buf) + 15) // 16 * 16
+    assert lib.flp_selftest_dz_wait_timeout(None, 1 << 20, 1, 1000, None) == flp.FLP_ERR_WORKSPACE
+    assert lib.flp_selftest_dz_wait_timeout(base, 1024, 1, 1000, None) == flp.FLP_ERR_WORKSPACE
+    assert lib.flp_selftest_dz_wait_timeout(base, 1 << 20, 1, 0, None) == flp.FLP_ERR_INVALID_ARG
+    assert lib.flp_selftest_dz_wait_timeout(base, 1 << 20, 1, 61 * 10**9, None) == flp.FLP_ERR_INVALID_ARG
+
+
 def test_loss_argument_checks_need_no_device(lib):
     from entropy_loss_gb300 import flp
     import ctypes as C

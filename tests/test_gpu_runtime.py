@@ -48,6 +48,36 @@ def test_bounded_wait_times_out_and_context_survives(flp):
     assert np.abs(en.cpu().double().numpy() - o_en).max() < 2e-3
 
 
+def test_dz_kernel_wait_times_out_and_context_survives(flp):
+    """The split schedule's dZ kernel (256 x 512 tiles, two epilogue groups
+    with store barriers) stalls, gives up after the bounded wait, reports the
+    timeout, and leaves a context that still runs a correct split backward."""
+    limit_ns = 200_000_000
+    assert flp.selftest_dz_wait_timeout(-1, limit_ns) == flp.FLP_OK  # same launch, no stall
+    for stall in (1, 0, 3):  # after the first stage, before any data, before the last of 4 stages
+        t0 = time.perf_counter()
+        st = flp.selftest_dz_wait_timeout(stall, limit_ns)
+        elapsed = time.perf_counter() - t0
+        assert st == flp.FLP_ERR_TIMEOUT, stall
+        assert elapsed < 5.0, f"timed-out kernel took {elapsed:.2f} s to return"
+    assert flp.selftest_dz_wait_timeout(-1, limit_ns) == flp.FLP_OK
+    M, H, V = 300, 64, 1000
+    d = inputs.make_inputs(inputs.custom("after_dz", M, H, V, w_std=0.05, seed=44))
+    dev = torch.device("cuda")
+    X, W, y = d["X"].to(dev), d["W"].to(dev), d["y"].to(dev)
+    ws = flp.alloc_workspace(M, H, V, True, device=dev)
+    lp, lse, en = flp.forward(X, W, y, workspace=ws)
+    dX, dW = flp.backward(X, W, y, lse, en, d["g_lp"].to(dev), d["g_ent"].to(dev), workspace=ws,
+                          schedule="split")
+    torch.cuda.synchronize()
+    assert flp.get_error(ws) == flp.FLP_OK
+    o_dx, o_dw = oracle.backward(inputs.bf16_bits(d["X"]), inputs.bf16_bits(d["W"]), d["y"].numpy(),
+                                 d["g_lp"].double().numpy(), d["g_ent"].double().numpy())
+    for got, want in ((dX, o_dx), (dW, o_dw)):
+        g = got.float().cpu().double().numpy()
+        assert np.linalg.norm(g - want) / np.linalg.norm(want) < 1e-2
+
+
 def test_fused_dependency_wait_times_out_and_context_survives(flp):
     limit_ns = 200_000_000
     assert flp.selftest_dependency_timeout(False, limit_ns) == flp.FLP_OK  # full schedule

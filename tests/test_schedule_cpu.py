@@ -7,19 +7,22 @@ earlier ticket, which is what rules out a deadlock of the persistent launch."""
 import numpy as np
 import pytest
 
-DZ, DX, DW, DX2, DZ2 = 0, 1, 2, 3, 4
+DZ, DX, DW, DX2, DZ2, DW2 = 0, 1, 2, 3, 4, 5
 
 
 def narrow(u):
     """Units as (kind, wave, a, b) 256 x 256 tiles; a wide dX tile (kind 3,
     512-column hidden tile b) counts as the dX tiles 2b and 2b + 1, a wide dZ
-    tile (kind 4, first vocabulary tile b) as the dZ tiles b and b + 1."""
+    tile (kind 4, first vocabulary tile b) as the dZ tiles b and b + 1, a wide
+    dW tile (kind 5) as the dW tiles 2b and 2b + 1."""
     out = []
     for _, k, w, a, b in u.tolist():
         if k == DX2:
             out += [(DX, w, a, 2 * b), (DX, w, a, 2 * b + 1)]
         elif k == DZ2:
             out += [(DZ, w, a, b), (DZ, w, a, b + 1)]
+        elif k == DW2:
+            out += [(DW, w, a, 2 * b), (DW, w, a, 2 * b + 1)]
         else:
             out.append((k, w, a, b))
     return sorted(out)
@@ -91,12 +94,14 @@ def test_every_tile_exactly_once(flp, schedule, M, H, V, chunk, pairs):
     u = flp.backward_schedule(M, H, V, ws, schedule, pairs)
     assert narrow(u) == expected_units(M, H, V, rows)
     assert waves == cdiv(M, rows)
-    # dX tiles are wide exactly when H spans an even number of 256-column tiles
+    # dX tiles (and the split schedule's dW tiles) are wide exactly when H
+    # spans an even number of 256-column tiles
     kinds = set(u[:, 1].tolist())
     if cdiv(H, 256) % 2 == 0:
         assert DX2 in kinds and DX not in kinds
+        assert (DW2 in kinds and DW not in kinds) if schedule == "split" else (DW in kinds and DW2 not in kinds)
     else:
-        assert DX in kinds and DX2 not in kinds
+        assert DX in kinds and DX2 not in kinds and DW2 not in kinds
 
 
 @pytest.mark.parametrize("M,H,V,chunk,pairs", SHAPES)
@@ -117,7 +122,7 @@ def test_split_schedule_orders_phases_by_launch(flp, M, H, V, chunk, pairs):
         else:
             assert not np.any(np.isin(kind[sel], (DZ, DZ2)))
             # the long dX tiles first, the short dW tiles fill the tail
-            k = np.where(kind[sel] == DX2, DX, kind[sel])
+            k = np.where(kind[sel] == DX2, DX, np.where(kind[sel] == DW2, DW, kind[sel]))
             assert np.all(np.diff(k) >= 0)
 
 
@@ -265,11 +270,12 @@ def test_vsplit_schedule(flp, M, H, V, cols):
         vts = set(range(c * per, min(Vt, (c + 1) * per)))
         dzn = narrow(dz)
         assert {v for _, _, _, v in dzn} == vts          # the chunk's vocabulary tiles
-        dw = gm[gm[:, 1] == DW]
-        assert set(dw[:, 3].tolist()) == vts
+        is_dw = np.isin(gm[:, 1], (DW, DW2))
+        dwn = narrow(gm[is_dw])
+        assert {v for _, _, v, _ in dwn} == vts
         seen_dz += [(m, v) for _, _, m, v in dzn]
-        seen_dw += [tuple(x) for x in dw[:, 3:].tolist()]
-        dx = narrow(gm[gm[:, 1] != DW])
+        seen_dw += [(v, h) for _, _, v, h in dwn]
+        dx = narrow(gm[~is_dw])
         assert sorted(dx) == sorted((DX, 0, m, h) for m in range(Mt) for h in range(Nh))
     assert sorted(seen_dz) == sorted((m, v) for m in range(Mt) for v in range(Vt))
     assert sorted(seen_dw) == sorted((v, h) for v in range(Vt) for h in range(Nh))
