@@ -1,38 +1,44 @@
 // bwd.cuh - the backward of the fused linear log-prob head on CTA pairs.
 //
-// One persistent kernel (instantiated per set of tile kinds a launch holds)
-// whose units are pair tiles of three kinds, 256 x 256 unless noted:
+// Two persistent kernels.  flp_bwd_kernel (instantiated per set of tile kinds
+// a launch holds) runs pair tiles of three kinds, 256 x 256 unless noted:
 //   dZ : the logits tile recomputed (K = H), then
 //        dZ = s [g_lp (onehot - p) + g_ent p (sum_j p_j z_j - z)]  in bf16,
 //        TMA-stored to the wave's dZ buffer (rows of the wave x padded V)
-//   dX : dX[wave] tile = dZ W        (K = padded vocabulary; W read MN-major),
-//        256 x 512 when H allows: two N = 256 MMAs share each A stage, so
-//        an SM loads 48 KiB per 64-deep K step for twice the MACs (the
-//        mainloops are bound by how fast an SM ingests operands from L2)
+//   dX : dX[wave] tile = dZ W        (K = padded vocabulary; W read MN-major)
 //   dW : dW tile (+)= dZ^T X[wave]   (K = wave rows; both operands MN-major)
+// dX tiles, and the split schedules' dW tiles, are 256 x 512 when H allows:
+// two N = 256 MMAs share each A stage, so an SM loads 48 KiB per 64-deep K
+// step for twice the MACs (the mainloops are bound by how fast an SM ingests
+// operands from L2), with the two halves staggered at the tile ends.
+// flp_dz_kernel runs the split schedules' dZ launch on 256 x 512 tiles, the
+// forward's mainloop with a dZ epilogue.
 // The leader CTA of each pair takes tickets from a global counter and maps
 // them to units through a schedule of segments that the host lays down, then
 // publishes each unit to both CTAs' roles through a shared-memory ring.  A
-// launch of equal-length units (the split schedule's dZ launch) instead runs
-// a static round-robin that every role computes for itself.
+// launch of equal-length units (the dZ launch) instead runs a static
+// round-robin that every role computes for itself.
 //
-// Two schedules drive it (the host picks one per call):
-//   split : per row wave, one launch with the wave's dZ tiles, then one launch
-//           with its dX tiles (long, first) and dW tiles (short, filling the
-//           tail); the kernel boundary orders the phases.
+// Three schedules drive them (the host picks one per call):
+//   split : per row wave, one flp_dz_kernel launch with the wave's dZ tiles,
+//           then one flp_bwd_kernel launch with its dX tiles (long, first)
+//           and dW tiles (short, filling the tail); the kernel boundary
+//           orders the phases.
 //   vsplit: all rows in one wave and the vocabulary in chunks: per chunk the
 //           same two launches over the chunk's columns; dX accumulates over
 //           the chunks in fp32, each dW tile is written once (K = all rows).
-//   fused : every wave in one launch.  A dX tile waits until the dZ tiles of
-//           its rows are stored, a dW tile until those of its vocabulary
-//           column are; from the second wave on, a dZ tile waits until the
-//           previous wave's dX and dW tiles that read its buffer slot are
-//           done, and a dW tile until the previous wave's add into the same
-//           dW rows is.  The counters live in the workspace; every wait is on
-//           a ticket handed out earlier, so the lowest unfinished ticket can
-//           always proceed, and every wait is bounded in time.
-// Both schedules compute every output tile with the same instructions in the
-// same K order, so their results agree bit for bit.
+//   fused : every wave in one flp_bwd_kernel launch (256 x 256 dZ and dW
+//           tiles).  A dX tile waits until the dZ tiles of its rows are
+//           stored, a dW tile until those of its vocabulary column are; from
+//           the second wave on, a dZ tile waits until the previous wave's dX
+//           and dW tiles that read its buffer slot are done, and a dW tile
+//           until the previous wave's add into the same dW rows is.  The
+//           counters live in the workspace; every wait is on a ticket handed
+//           out earlier, so the lowest unfinished ticket can always proceed,
+//           and every wait is bounded in time.
+// Every schedule computes each 256 x 256 block of an output with the same
+// instructions in the same K order (a wide tile's halves are two such
+// blocks), so their results agree bit for bit.
 #pragma once
 #include "kernels.cuh"
 

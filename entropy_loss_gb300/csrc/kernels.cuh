@@ -1,19 +1,21 @@
 // kernels.cuh - sm_103a kernels of the fused linear log-prob / cross-entropy head.
 //
 // Every contraction of the path runs on CTA pairs (clusters of two CTAs on two
-// SMs) that share one 256 x 256 output tile: tcgen05.mma.cta_group::2 with
-// M = 256 (128 rows of A in each CTA) and N = 256 (B split along N, 128 rows
-// in each CTA), fp32 accumulators in both CTAs' TMEM.  Each SM therefore loads
-// 16 KiB of A and 16 KiB of B per 64-deep K step for 2 * 128 * 256 * 64 MACs.
+// SMs) that share an output tile: tcgen05.mma.cta_group::2 with M = 256 (128
+// rows of A in each CTA) and N = 256 (B split along N, 128 rows in each CTA),
+// fp32 accumulators in both CTAs' TMEM.  For a 256 x 256 tile each SM loads
+// 16 KiB of A and 16 KiB of B per 64-deep K step for 2 * 128 * 256 * 64 MACs;
+// a wide 256 x 512 tile (both accumulators) loads 48 KiB for twice that.
 //
 //   flp_fwd_kernel   : z = s X W^T tiles -> online max / sum-exp / (entropy) /
 //                      target pick per row -> raw per-split partials
 //   flp_merge_kernel : per-split partials -> lse, logprob, entropy
-//   flp_bwd_kernel   : (bwd.cuh) dZ, dX and dW tiles of the backward
+//   flp_dz_kernel    : (bwd.cuh) the dZ tiles of the split backward schedules
+//   flp_bwd_kernel   : (bwd.cuh) dX and dW tiles, and all tiles of the fused one
 //
 // This file holds the pieces every pair kernel shares (shared-memory layout,
-// barrier set-up and teardown, descriptors, store boxes), the forward and the
-// merge.
+// barrier set-up and teardown, descriptors, store boxes, the wide tiles'
+// producer step and staggered MMA issue), the forward and the merge.
 //
 // Roles (192 threads per CTA, one CTA per SM):
 //   warp 0      TMA producer (one lane) for this CTA's halves of A and B
