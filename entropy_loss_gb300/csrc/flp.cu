@@ -155,19 +155,30 @@ struct FwdPlan {
 // tiles); a static round-robin over the persistent CTA pairs finishes after
 // ceil(units / pairs) * tps tiles.  Each extra split adds M * 48 bytes of
 // partial traffic (two halves of m, sigma, tau and their reads), charged in
-// tile-times so that near-ties favour fewer splits.
-FwdPlan plan_forward(int64_t M, int64_t H, int64_t V, int compute_entropy, int pairs) {
+// tile-times so that near-ties favour fewer splits.  Only plans whose
+// workspace fits max_bytes are considered (the allocation-free forward's
+// fixed scratch); when none does, the one-split plan is returned and the
+// caller sees its size.
+FwdPlan plan_forward(int64_t M, int64_t H, int64_t V, int compute_entropy, int pairs,
+                     size_t max_bytes = SIZE_MAX) {
     FwdPlan f{};
     pairs = std::max(1, pairs);
     f.Mt = static_cast<int>(cdiv(M, PM));
     f.Vt = static_cast<int>(cdiv(V, 2 * BN));  // 512-column tiles
     const double tile_s = 2.0 * PM * 2 * BN * static_cast<double>(H) / 2.4e13;  // ~bf16 rate of a pair
     const double split_cost = (static_cast<double>(M) * 48.0 / 6.0e12) / tile_s;
+    // workspace of a plan with S splits: header | m, sigma (, tau) [2 S][M] | z_y [M]
+    auto bytes_for = [&](int S) {
+        const size_t part = align_up(static_cast<size_t>(2 * S) * M * sizeof(float), 1024);  // 2 halves per split
+        return kHeaderBytes + part * (compute_entropy ? 3 : 2) +
+               align_up(static_cast<size_t>(M) * sizeof(float), 1024);
+    };
     double best = 1e300;
     int best_tps = f.Vt;
     for (int tps = 1; tps <= f.Vt; ++tps) {
         const int S = static_cast<int>(cdiv(f.Vt, tps));
         if (tps > 1 && cdiv(f.Vt, tps - 1) == S) continue;  // same split count, shorter runs win
+        if (bytes_for(S) > max_bytes) continue;
         const double units = static_cast<double>(f.Mt) * S;
         const double waves = std::ceil(units / pairs);
         const double cost = waves * tps + S * split_cost;
@@ -190,6 +201,7 @@ FwdPlan plan_forward(int64_t M, int64_t H, int64_t V, int compute_entropy, int p
     f.off_t = f.off_s + part;
     f.off_zy = f.off_t + (compute_entropy ? part : 0);
     f.bytes = f.off_zy + align_up(static_cast<size_t>(M) * sizeof(float), 1024);
+    // (== bytes_for(f.S))
     return f;
 }
 
@@ -1088,7 +1100,8 @@ extern "C" flp_status flp_forward_noalloc(const void* X, const void* W, const in
     st = check_device(&d);
     if (st != FLP_OK) return st;
     if (M > 0 && (st = check_on_current_device(X, "X")) != FLP_OK) return st;
-    const FwdPlan f = plan_forward(M, H, V, ent, d->pairs);
+    // the fastest split plan whose scratch fits the static array
+    const FwdPlan f = plan_forward(M, H, V, ent, d->pairs, FLP_STATIC_SCRATCH_BYTES);
     if (f.bytes > FLP_STATIC_SCRATCH_BYTES) {
         char buf[200];
         snprintf(buf, sizeof buf,

@@ -222,8 +222,11 @@ flp_status flp_backward_schedule(int64_t M, int64_t H, int64_t V, size_t workspa
  * per-split partials and the error word live instead in one file-scope
  * device array of FLP_STATIC_SCRATCH_BYTES (16 MiB) that every GPU which
  * loads this library holds until the process exits.
- *  - Problems whose forward workspace (flp_workspace_query's fwd_bytes) exceeds
- *    that size are rejected with FLP_ERR_UNSUPPORTED before any launch.
+ *  - It takes the fastest vocabulary-split plan whose scratch fits that size
+ *    (flp_forward's own plan when its fwd_bytes fit, with the same results
+ *    bit for bit; otherwise fewer splits, whose merged results can differ from
+ *    flp_forward's in the last bits).  Problems that do not fit even with one
+ *    split are rejected with FLP_ERR_UNSUPPORTED before any launch.
  *  - The first call on a device looks up the array's device address on that
  *    device (cudaGetSymbolAddress, with the device current); make that first
  *    call before any stream capture.  No cudaMalloc, cudaFree or allocating

@@ -67,10 +67,36 @@ def test_noalloc_forward_matches_workspace_forward_twice(lib):
             torch.testing.assert_close(en, r_en, rtol=0, atol=ATOL_FWD)
 
 
+def test_noalloc_takes_fewer_splits_when_the_default_plan_does_not_fit(lib):
+    """12288 rows, H = 1024, a 128K vocabulary: flp_forward's own plan (128
+    splits) needs 36 MiB of partials, so the allocation-free forward runs a
+    plan with fewer splits that fits its 16 MiB (same values within the
+    forward tolerance)."""
+    from entropy_loss_gb300 import flp
+    M, H, V = 12288, 1024, 131072
+    f, _ = flp.workspace_query(M, H, V, True)
+    assert f > flp.STATIC_SCRATCH_BYTES
+    dev = torch.device("cuda")
+    d = inputs.make_inputs(inputs.custom("c", M, H, V, w_std=0.05, ignore_frac=0.05, seed=33),
+                           with_grads=False)
+    X, W, y = d["X"].to(dev), d["W"].to(dev), d["y"].to(dev)
+    lp = torch.full((M,), float("nan"), device=dev)
+    lse = torch.full((M,), float("nan"), device=dev)
+    en = torch.full((M,), float("nan"), device=dev)
+    stream = torch.cuda.current_stream().cuda_stream
+    st = _call_noalloc(lib, X, W, y, lp, lse, en, True, 1.0, stream)
+    assert st == flp.FLP_OK, lib.flp_last_error_message()
+    r_lp, r_lse, r_en = flp.forward(X, W, y)
+    torch.cuda.synchronize()
+    torch.testing.assert_close(lp, r_lp, rtol=0, atol=ATOL_FWD)
+    torch.testing.assert_close(lse, r_lse, rtol=0, atol=ATOL_FWD)
+    torch.testing.assert_close(en, r_en, rtol=0, atol=ATOL_FWD)
+
+
 def test_noalloc_rejects_problems_beyond_the_static_scratch(lib):
     from entropy_loss_gb300 import flp
-    # 2^20 rows need at least 3 x 4 MiB of partials and 4 MiB of target
-    # logits plus the header, beyond 16 MiB whatever the split count
+    # 2^20 rows need at least 3 x 8 MiB of partials (two per split) and 4 MiB
+    # of target logits plus the header, beyond 16 MiB whatever the split count
     M, H, V = 1 << 20, 8, 1 << 20
     f, _ = flp.workspace_query(M, H, V, True)
     assert f > flp.STATIC_SCRATCH_BYTES
