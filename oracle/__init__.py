@@ -60,6 +60,13 @@ def _load():
                 fn = getattr(lib, name)
                 fn.argtypes = args
                 fn.restype = ctypes.c_int
+            for name in ("flpo_backward_dw_cols_bf16", "flpo_backward_dw_cols_f64"):
+                fn = getattr(lib, name)
+                fn.argtypes = [p, p, p, i64, i64, i64, i64, ctypes.c_double, ctypes.c_int, p, p, p,
+                               i64, ctypes.c_int, p]
+                fn.restype = ctypes.c_int
+            lib.flpo_round_bf16.argtypes = [p, p, i64]
+            lib.flpo_round_bf16.restype = None
             lib.flpo_loss.argtypes = [p, p, i64, i64, ctypes.c_int, p, p, p, ctypes.c_double,
                                       ctypes.c_double, ctypes.c_double, p, p, p]
             lib.flpo_loss.restype = ctypes.c_int
@@ -139,6 +146,34 @@ def backward(X, W, y, g_lp, g_ent, ignore_index=-100, scale=1.0, compute_entropy
     if st not in (FLPO_OK, FLPO_BAD_TARGET):
         raise OracleError(f"oracle backward failed with status {st}")
     return dx, dw
+
+
+def backward_dw_cols(X, W, y, g_lp, g_ent, cols, ignore_index=-100, scale=1.0,
+                     compute_entropy=True, round_dz_bf16=False):
+    """dW restricted to the vocabulary rows `cols`, with every row's upstream
+    gradient live: returns an fp64 array [len(cols), H] whose row c is
+    sum_i dZ[i, cols[c]] X[i, :] over all rows i."""
+    lib = _load()
+    X, W, y, kind, M, H, V = _prep(X, W, y)
+    c = np.ascontiguousarray(cols, dtype=np.int64)
+    g_lp = None if g_lp is None else np.ascontiguousarray(g_lp, dtype=np.float64)
+    g_ent = None if g_ent is None else np.ascontiguousarray(g_ent, dtype=np.float64)
+    out = np.zeros((c.shape[0], H), np.float64)
+    fn = lib.flpo_backward_dw_cols_bf16 if kind == "bf16" else lib.flpo_backward_dw_cols_f64
+    st = fn(_ptr(X), _ptr(W), _ptr(y), M, H, V, int(ignore_index), float(scale),
+            int(bool(compute_entropy)), _ptr(g_lp), _ptr(g_ent), _ptr(c), c.shape[0],
+            int(bool(round_dz_bf16)), _ptr(out))
+    if st not in (FLPO_OK, FLPO_BAD_TARGET):
+        raise OracleError(f"oracle backward_dw_cols failed with status {st}")
+    return out
+
+
+def round_bf16(a) -> np.ndarray:
+    """The oracle's fp32 -> bf16 rounding of each element (uint16 bit patterns)."""
+    f = np.ascontiguousarray(a, dtype=np.float32)
+    out = np.zeros(f.shape, np.uint16)
+    _load().flpo_round_bf16(_ptr(f), _ptr(out), f.size)
+    return out
 
 
 def bf16_bits_to_f64(a: np.ndarray) -> np.ndarray:

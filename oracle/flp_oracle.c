@@ -261,6 +261,72 @@ static int backward_impl(const void* X, const void* W, int type, const int64_t* 
     return status;
 }
 
+/*
+ * dW restricted to the vocabulary rows listed in `cols`, with every row's
+ * upstream gradient live:
+ *   dW_cols[c, :] = sum_i dZ[i, cols[c]] X[i, :]      over all rows i in [0, M)
+ * Each dZ entry needs its row's LSE and sum_j p_ij z_ij, hence every row's full
+ * logit row (the same forward definitions as above); only the listed columns
+ * of dZ are kept.  This is the sampled form of the backward for problems whose
+ * full fp64 dW does not fit a test's time budget.  round_dz_bf16 as in
+ * backward_impl.
+ */
+static int backward_dw_cols_impl(const void* X, const void* W, int type, const int64_t* y,
+                                 int64_t M, int64_t H, int64_t V, int64_t ignore_index,
+                                 double s, int compute_entropy, const double* g_lp,
+                                 const double* g_ent, const int64_t* cols, int64_t ncols,
+                                 int round_dz_bf16, double* dW_cols) {
+    if (M < 0 || H < 1 || V < 1 || ncols < 0 || (ncols > 0 && !cols)) return FLPO_INVALID_ARG;
+    for (int64_t c = 0; c < ncols; ++c)
+        if (cols[c] < 0 || cols[c] >= V) return FLPO_INVALID_ARG;
+    /* dZ[i, cols[c]] for every row i: M x ncols */
+    double* dZ = (double*)malloc(sizeof(double) * (size_t)(M > 0 ? M : 1) * (size_t)(ncols > 0 ? ncols : 1));
+    if (!dZ) return FLPO_NO_MEMORY;
+    int status = FLPO_OK;
+#pragma omp parallel
+    {
+        double* xrow = (double*)malloc(sizeof(double) * (size_t)H);
+        double* z = (double*)malloc(sizeof(double) * (size_t)V);
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t i = 0; i < M; ++i) {
+            double* dz = dZ + i * ncols;
+            double glp = g_lp ? g_lp[i] : 0.0;
+            double gent = (compute_entropy && g_ent) ? g_ent[i] : 0.0;
+            if (y[i] != ignore_index && !target_ok(y[i], V)) {
+#pragma omp atomic write
+                status = FLPO_BAD_TARGET;
+            }
+            if (y[i] == ignore_index || (glp == 0.0 && gent == 0.0)) {  /* dZ row is zero */
+                for (int64_t c = 0; c < ncols; ++c) dz[c] = 0.0;
+                continue;
+            }
+            logits_row(X, W, type, i, H, V, s, xrow, z);
+            row_stats st = stats_from_logits(z, V);
+            for (int64_t c = 0; c < ncols; ++c) {
+                int64_t j = cols[c];
+                double p = exp(z[j] - st.lse);
+                double onehot = (j == y[i]) ? 1.0 : 0.0;
+                double v = s * (glp * (onehot - p) + gent * p * (st.sum_pz - z[j]));
+                dz[c] = round_dz_bf16 ? bf16_to_double(float_to_bf16_rne((float)v)) : v;
+            }
+        }
+        free(xrow);
+        free(z);
+    }
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t c = 0; c < ncols; ++c) {
+        double* out = dW_cols + c * H;
+        for (int64_t h = 0; h < H; ++h) out[h] = 0.0;
+        for (int64_t i = 0; i < M; ++i) {
+            double d = dZ[i * ncols + c];
+            if (d == 0.0) continue;
+            for (int64_t h = 0; h < H; ++h) out[h] += d * get_elem(X, type, i * H + h);
+        }
+    }
+    free(dZ);
+    return status;
+}
+
 /* ---- exported entry points (ctypes) ---- */
 
 int flpo_forward_bf16(const uint16_t* X, const uint16_t* W, const int64_t* y, int64_t M,
@@ -295,6 +361,30 @@ int flpo_backward_f64(const double* X, const double* W, const int64_t* y, int64_
                       double* dW) {
     return backward_impl(X, W, FLPO_F64, y, M, H, V, ignore_index, s, compute_entropy, g_lp,
                          g_ent, rows, nrows, round_dz_bf16, dX_rows, dW);
+}
+
+int flpo_backward_dw_cols_bf16(const uint16_t* X, const uint16_t* W, const int64_t* y,
+                               int64_t M, int64_t H, int64_t V, int64_t ignore_index, double s,
+                               int compute_entropy, const double* g_lp, const double* g_ent,
+                               const int64_t* cols, int64_t ncols, int round_dz_bf16,
+                               double* dW_cols) {
+    return backward_dw_cols_impl(X, W, FLPO_BF16, y, M, H, V, ignore_index, s, compute_entropy,
+                                 g_lp, g_ent, cols, ncols, round_dz_bf16, dW_cols);
+}
+
+int flpo_backward_dw_cols_f64(const double* X, const double* W, const int64_t* y, int64_t M,
+                              int64_t H, int64_t V, int64_t ignore_index, double s,
+                              int compute_entropy, const double* g_lp, const double* g_ent,
+                              const int64_t* cols, int64_t ncols, int round_dz_bf16,
+                              double* dW_cols) {
+    return backward_dw_cols_impl(X, W, FLPO_F64, y, M, H, V, ignore_index, s, compute_entropy,
+                                 g_lp, g_ent, cols, ncols, round_dz_bf16, dW_cols);
+}
+
+/* The oracle's binary32 -> bf16 rounding (round to nearest, ties to even),
+ * exported so that tests can pin it bit for bit. */
+void flpo_round_bf16(const float* in, uint16_t* out, int64_t n) {
+    for (int64_t i = 0; i < n; ++i) out[i] = float_to_bf16_rne(in[i]);
 }
 
 /* Threads OpenMP will use for the parallel regions above. */

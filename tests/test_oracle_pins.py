@@ -320,3 +320,108 @@ def test_round_dz_bf16_is_small_perturbation():
     assert 0 < rel < 2 ** -8
     rel = np.linalg.norm(dx1 - dx0) / np.linalg.norm(dx0)
     assert 0 < rel < 2 ** -8
+
+
+# ------------------------------------------------- bf16 rounding of dZ, bit for bit
+
+def _f32(bits):
+    return np.array([bits], dtype=np.uint32).view(np.float32)[0]
+
+
+@pytest.mark.parametrize("bits,want", [
+    (0x3F800000, 0x3F80),  # 1.0, exact
+    (0x3F808000, 0x3F80),  # tie, the lower neighbour is even: stays
+    (0x3F818000, 0x3F82),  # tie, the lower neighbour is odd: rounds up to even
+    (0x3F808001, 0x3F81),  # just above a tie: up
+    (0x3F807FFF, 0x3F80),  # just below a tie: down
+    (0xBF808000, 0xBF80),  # negative tie to even (magnitude rounds down)
+    (0xBF818000, 0xBF82),  # negative tie to even (magnitude rounds up)
+    (0xBF80C000, 0xBF81),  # negative, above the tie in magnitude
+    (0x7F7F8000, 0x7F80),  # tie between the largest finite bf16 (odd) and +inf: +inf
+    (0x7F7FFFFF, 0x7F80),  # the largest binary32 overflows to +inf
+    (0x7F7F7FFF, 0x7F7F),  # below that tie: the largest finite bf16
+    (0xFF7FFFFF, 0xFF80),  # ... and to -inf
+    (0x7F800000, 0x7F80),  # +inf
+    (0xFF800000, 0xFF80),  # -inf
+    (0x00000000, 0x0000),  # +0
+    (0x80000000, 0x8000),  # -0
+    (0x00008000, 0x0000),  # subnormal tie to even (zero)
+    (0x00018000, 0x0002),  # subnormal tie to even (up)
+    (0x007FFFFF, 0x0080),  # largest subnormal rounds up to the smallest normal
+])
+def test_oracle_bf16_rounding_exact_bits(bits, want):
+    """Round to nearest, ties to even (IEEE 754 roundTiesToEven applied at the
+    bf16 precision: 8 significand bits); the expected patterns follow from
+    that rule by hand."""
+    got = int(oracle.round_bf16(np.array([_f32(bits)]))[0])
+    assert got == want, f"{bits:#010x}: got {got:#06x}, want {want:#06x}"
+
+
+@pytest.mark.parametrize("bits", [0x7FC00000, 0x7F800001, 0xFFC00001, 0x7FBFFFFF])
+def test_oracle_bf16_rounding_keeps_nan(bits):
+    """A NaN stays a NaN (a quiet one): a signalling NaN whose payload sits in
+    the low half must not turn into an infinity."""
+    got = int(oracle.round_bf16(np.array([_f32(bits)]))[0])
+    assert (got & 0x7F80) == 0x7F80 and (got & 0x007F) != 0, f"{bits:#010x} -> {got:#06x}"
+    assert (got & 0x8000) == (bits >> 16 & 0x8000)
+
+
+def test_oracle_bf16_rounding_matches_torch_on_random_patterns():
+    """torch's float32 -> bfloat16 conversion is round-to-nearest-even; on a
+    million random non-NaN bit patterns (every exponent, both signs) and on
+    every tie pattern of a few exponents the oracle agrees bit for bit."""
+    import torch
+    r = rng(99)
+    bits = r.integers(0, 2**32, size=1_000_000, dtype=np.uint64).astype(np.uint32)
+    ties = ((np.arange(0, 2**16, dtype=np.uint32) << 16) | 0x8000)
+    bits = np.concatenate([bits, ties, ties - 1, ties + 1])
+    f = bits.view(np.float32)
+    f = f[~np.isnan(f)]
+    want = torch.from_numpy(f.copy()).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    got = oracle.round_bf16(f)
+    bad = np.flatnonzero(got != want)
+    assert bad.size == 0, f"{bad.size} mismatches, first {f.view(np.uint32)[bad[0]]:#010x}"
+
+
+def test_round_dz_bf16_rounds_each_dz_entry_before_the_contractions():
+    """With H = 1 and X = 1, dW[j] is dZ[0, j] itself, so the rounding mode
+    shows up unmixed: dW[j] = bf16(fp32(dZ_j)) with dZ from the closed form of
+    a two-class row (logistic): p_1 = 1 / (1 + e^{z_0 - z_1})."""
+    import torch
+    s, g = 1.0, 1.0
+    X = np.ones((1, 1))
+    for z0, z1 in ((0.3, -1.7), (2.0, 2.0 + 1e-3), (-0.123456, 0.5)):
+        W = np.array([[z0], [z1]])
+        y = np.array([0])
+        p1 = 1.0 / (1.0 + math.exp(z0 - z1))
+        dz = np.array([s * g * (1.0 - (1.0 - p1)), s * g * (0.0 - p1)])  # onehot - p
+        want = torch.from_numpy(dz.astype(np.float32)).to(torch.bfloat16).double().numpy()
+        _, dw = oracle.backward(X, W, y, np.array([g]), None, compute_entropy=False, scale=s,
+                                round_dz_bf16=True)
+        np.testing.assert_array_equal(dw[:, 0], want)
+        _, dw0 = oracle.backward(X, W, y, np.array([g]), None, compute_entropy=False, scale=s)
+        np.testing.assert_allclose(dw0[:, 0], dz, rtol=1e-15, atol=1e-17)
+
+
+# ------------------------------------------- dW on selected vocabulary rows
+
+@pytest.mark.parametrize("rnd", [False, True])
+def test_backward_dw_cols_equals_the_full_backward_rows(rnd):
+    """The sampled-vocabulary dW (every row's gradient live) equals the rows
+    of the full backward's dW, which the finite-difference pins above tie to
+    the forward; also with an ignored row, s != 1 and entropy on."""
+    M, H, V = 13, 7, 41
+    X, W, y = rand_case(40, M, H, V)
+    y[[3, 9]] = -100
+    g_lp = rng(41).normal(size=M)
+    g_ent = rng(42).normal(size=M)
+    cols = np.array([0, 5, 17, 40, 17])
+    _, dw = oracle.backward(X, W, y, g_lp, g_ent, scale=0.8, round_dz_bf16=rnd)
+    got = oracle.backward_dw_cols(X, W, y, g_lp, g_ent, cols, scale=0.8, round_dz_bf16=rnd)
+    np.testing.assert_allclose(got, dw[cols], rtol=1e-13, atol=1e-15)
+    # bf16 inputs take the same path as their exact fp64 widening
+    Xb, Wb = to_bf16_bits(X), to_bf16_bits(W)
+    got_b = oracle.backward_dw_cols(Xb, Wb, y, g_lp, None, cols, compute_entropy=False)
+    _, dw_b = oracle.backward(oracle.bf16_bits_to_f64(Xb), oracle.bf16_bits_to_f64(Wb), y, g_lp,
+                              None, compute_entropy=False)
+    np.testing.assert_allclose(got_b, dw_b[cols], rtol=1e-13, atol=1e-15)
