@@ -63,13 +63,17 @@ def _load():
             for name in ("flpo_backward_dw_cols_bf16", "flpo_backward_dw_cols_f64"):
                 fn = getattr(lib, name)
                 fn.argtypes = [p, p, p, i64, i64, i64, i64, ctypes.c_double, ctypes.c_int, p, p, p,
-                               i64, ctypes.c_int, p]
+                               i64, ctypes.c_int, p, p, p, p]
                 fn.restype = ctypes.c_int
             lib.flpo_round_bf16.argtypes = [p, p, i64]
             lib.flpo_round_bf16.restype = None
             lib.flpo_loss.argtypes = [p, p, i64, i64, ctypes.c_int, p, p, p, ctypes.c_double,
                                       ctypes.c_double, ctypes.c_double, p, p, p]
             lib.flpo_loss.restype = ctypes.c_int
+            lib.flpo_policy_loss.argtypes = [p, p, i64, i64, p, i64, p, p, p, ctypes.c_double,
+                                             ctypes.c_double, ctypes.c_double, ctypes.c_int,
+                                             ctypes.c_int, ctypes.c_double, p, p, p]
+            lib.flpo_policy_loss.restype = ctypes.c_int
             lib.flpo_num_threads.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -149,23 +153,28 @@ def backward(X, W, y, g_lp, g_ent, ignore_index=-100, scale=1.0, compute_entropy
 
 
 def backward_dw_cols(X, W, y, g_lp, g_ent, cols, ignore_index=-100, scale=1.0,
-                     compute_entropy=True, round_dz_bf16=False):
+                     compute_entropy=True, round_dz_bf16=False, with_forward=False):
     """dW restricted to the vocabulary rows `cols`, with every row's upstream
     gradient live: returns an fp64 array [len(cols), H] whose row c is
-    sum_i dZ[i, cols[c]] X[i, :] over all rows i."""
+    sum_i dZ[i, cols[c]] X[i, :] over all rows i.  With `with_forward`,
+    returns (dW_cols, logprob, lse, entropy-or-None) of every row as well
+    (the same logit rows, formed once)."""
     lib = _load()
     X, W, y, kind, M, H, V = _prep(X, W, y)
     c = np.ascontiguousarray(cols, dtype=np.int64)
     g_lp = None if g_lp is None else np.ascontiguousarray(g_lp, dtype=np.float64)
     g_ent = None if g_ent is None else np.ascontiguousarray(g_ent, dtype=np.float64)
     out = np.zeros((c.shape[0], H), np.float64)
+    lp = np.zeros(M, np.float64) if with_forward else None
+    lse = np.zeros(M, np.float64) if with_forward else None
+    ent = np.zeros(M, np.float64) if (with_forward and compute_entropy) else None
     fn = lib.flpo_backward_dw_cols_bf16 if kind == "bf16" else lib.flpo_backward_dw_cols_f64
     st = fn(_ptr(X), _ptr(W), _ptr(y), M, H, V, int(ignore_index), float(scale),
             int(bool(compute_entropy)), _ptr(g_lp), _ptr(g_ent), _ptr(c), c.shape[0],
-            int(bool(round_dz_bf16)), _ptr(out))
+            int(bool(round_dz_bf16)), _ptr(out), _ptr(lp), _ptr(lse), _ptr(ent))
     if st not in (FLPO_OK, FLPO_BAD_TARGET):
         raise OracleError(f"oracle backward_dw_cols failed with status {st}")
-    return out
+    return (out, lp, lse, ent) if with_forward else out
 
 
 def round_bf16(a) -> np.ndarray:
@@ -183,6 +192,9 @@ def bf16_bits_to_f64(a: np.ndarray) -> np.ndarray:
 
 LOSS_NLL_MEAN = 1
 LOSS_GRPO = 2
+LOSS_NLL_SUM = 3
+IS_TOKEN, IS_SEQUENCE = 0, 1
+AGG_TOKEN_MEAN, AGG_SEQUENCE_MEAN, AGG_SUM_OVER = 0, 1, 2
 
 
 def loss(logprob, y, kind, ignore_index=-100, old_logprob=None, advantage=None,
@@ -202,4 +214,29 @@ def loss(logprob, y, kind, ignore_index=-100, old_logprob=None, advantage=None,
                        _ptr(grad), _ptr(out))
     if st != FLPO_OK:
         raise OracleError(f"oracle loss failed with status {st}")
+    return per_row, grad, float(out[0])
+
+
+def policy_loss(logprob, y, old_logprob, advantage, seq_offsets=None, ignore_index=-100,
+                ref_logprob=None, eps_low=0.2, eps_high=0.2, beta=0.0, is_level=IS_TOKEN,
+                aggregation=AGG_TOKEN_MEAN, normalizer=0.0):
+    """Policy-gradient loss over sequences: returns (per_row, grad_logprob, scalar).
+    seq_offsets: int64 [B + 1] row offsets of the sequences (None: one sequence)."""
+    lib = _load()
+    lp = np.ascontiguousarray(logprob, dtype=np.float64)
+    y = np.ascontiguousarray(y, dtype=np.int64)
+    M = lp.shape[0]
+    conv = (lambda a: None if a is None else np.ascontiguousarray(a, dtype=np.float64))
+    old, adv, ref = conv(old_logprob), conv(advantage), conv(ref_logprob)
+    off = None if seq_offsets is None else np.ascontiguousarray(seq_offsets, dtype=np.int64)
+    B = 0 if off is None else off.shape[0] - 1
+    per_row = np.zeros(M)
+    grad = np.zeros(M)
+    out = np.zeros(1)
+    st = lib.flpo_policy_loss(_ptr(lp), _ptr(y), M, int(ignore_index), _ptr(off), B, _ptr(old),
+                              _ptr(adv), _ptr(ref), float(eps_low), float(eps_high), float(beta),
+                              int(is_level), int(aggregation), float(normalizer), _ptr(per_row),
+                              _ptr(grad), _ptr(out))
+    if st != FLPO_OK:
+        raise OracleError(f"oracle policy loss failed with status {st}")
     return per_row, grad, float(out[0])

@@ -125,6 +125,24 @@ static row_stats stats_from_logits(const double* z, int64_t V) {
 
 static int target_ok(int64_t y, int64_t V) { return y >= 0 && y < V; }
 
+/* logprob and entropy of one row from its logits and statistics; ignored rows
+ * give 0 and 0, an out-of-range target NaN (returns 0 then, else 1). */
+static int row_outputs(const double* z, row_stats st, int64_t y, int64_t ignore_index, int64_t V,
+                       double* lp, double* ent) {
+    *ent = st.lse - st.sum_pz;
+    if (y == ignore_index) {
+        *lp = 0.0;
+        *ent = 0.0;
+        return 1;
+    }
+    if (!target_ok(y, V)) {
+        *lp = NAN;
+        return 0;
+    }
+    *lp = z[y] - st.lse;
+    return 1;
+}
+
 /*
  * Forward outputs for the rows listed in `rows` (all rows when rows == NULL).
  * Output k belongs to row rows[k].  entropy may be NULL when compute_entropy
@@ -153,16 +171,10 @@ static int forward_impl(const void* X, const void* W, int type, const int64_t* y
             logits_row(X, W, type, i, H, V, s, xrow, z);
             row_stats st = stats_from_logits(z, V);
             if (lse) lse[k] = st.lse;
-            double lp, ent = st.lse - st.sum_pz;
-            if (y[i] == ignore_index) {
-                lp = 0.0;
-                ent = 0.0;
-            } else if (!target_ok(y[i], V)) {
-                lp = NAN;
+            double lp, ent;
+            if (!row_outputs(z, st, y[i], ignore_index, V, &lp, &ent)) {
 #pragma omp atomic write
                 status = FLPO_BAD_TARGET;
-            } else {
-                lp = z[y[i]] - st.lse;
             }
             if (logprob) logprob[k] = lp;
             if (compute_entropy && entropy) entropy[k] = ent;
@@ -269,13 +281,16 @@ static int backward_impl(const void* X, const void* W, int type, const int64_t* 
  * logit row (the same forward definitions as above); only the listed columns
  * of dZ are kept.  This is the sampled form of the backward for problems whose
  * full fp64 dW does not fit a test's time budget.  round_dz_bf16 as in
- * backward_impl.
+ * backward_impl.  Since every row's logits are formed anyway, the forward
+ * outputs of every row can be returned too (logprob, lse, entropy: each may
+ * be NULL), by the same definitions as forward_impl.
  */
 static int backward_dw_cols_impl(const void* X, const void* W, int type, const int64_t* y,
                                  int64_t M, int64_t H, int64_t V, int64_t ignore_index,
                                  double s, int compute_entropy, const double* g_lp,
                                  const double* g_ent, const int64_t* cols, int64_t ncols,
-                                 int round_dz_bf16, double* dW_cols) {
+                                 int round_dz_bf16, double* dW_cols, double* logprob,
+                                 double* lse, double* entropy) {
     if (M < 0 || H < 1 || V < 1 || ncols < 0 || (ncols > 0 && !cols)) return FLPO_INVALID_ARG;
     for (int64_t c = 0; c < ncols; ++c)
         if (cols[c] < 0 || cols[c] >= V) return FLPO_INVALID_ARG;
@@ -292,16 +307,20 @@ static int backward_dw_cols_impl(const void* X, const void* W, int type, const i
             double* dz = dZ + i * ncols;
             double glp = g_lp ? g_lp[i] : 0.0;
             double gent = (compute_entropy && g_ent) ? g_ent[i] : 0.0;
-            if (y[i] != ignore_index && !target_ok(y[i], V)) {
+            logits_row(X, W, type, i, H, V, s, xrow, z);
+            row_stats st = stats_from_logits(z, V);
+            double lp, ent;
+            if (!row_outputs(z, st, y[i], ignore_index, V, &lp, &ent)) {
 #pragma omp atomic write
                 status = FLPO_BAD_TARGET;
             }
-            if (y[i] == ignore_index || (glp == 0.0 && gent == 0.0)) {  /* dZ row is zero */
+            if (logprob) logprob[i] = lp;
+            if (lse) lse[i] = st.lse;
+            if (compute_entropy && entropy) entropy[i] = ent;
+            if (y[i] == ignore_index) {  /* an ignored row's dZ row is zero */
                 for (int64_t c = 0; c < ncols; ++c) dz[c] = 0.0;
                 continue;
             }
-            logits_row(X, W, type, i, H, V, s, xrow, z);
-            row_stats st = stats_from_logits(z, V);
             for (int64_t c = 0; c < ncols; ++c) {
                 int64_t j = cols[c];
                 double p = exp(z[j] - st.lse);
@@ -367,18 +386,20 @@ int flpo_backward_dw_cols_bf16(const uint16_t* X, const uint16_t* W, const int64
                                int64_t M, int64_t H, int64_t V, int64_t ignore_index, double s,
                                int compute_entropy, const double* g_lp, const double* g_ent,
                                const int64_t* cols, int64_t ncols, int round_dz_bf16,
-                               double* dW_cols) {
+                               double* dW_cols, double* logprob, double* lse, double* entropy) {
     return backward_dw_cols_impl(X, W, FLPO_BF16, y, M, H, V, ignore_index, s, compute_entropy,
-                                 g_lp, g_ent, cols, ncols, round_dz_bf16, dW_cols);
+                                 g_lp, g_ent, cols, ncols, round_dz_bf16, dW_cols, logprob, lse,
+                                 entropy);
 }
 
 int flpo_backward_dw_cols_f64(const double* X, const double* W, const int64_t* y, int64_t M,
                               int64_t H, int64_t V, int64_t ignore_index, double s,
                               int compute_entropy, const double* g_lp, const double* g_ent,
                               const int64_t* cols, int64_t ncols, int round_dz_bf16,
-                              double* dW_cols) {
+                              double* dW_cols, double* logprob, double* lse, double* entropy) {
     return backward_dw_cols_impl(X, W, FLPO_F64, y, M, H, V, ignore_index, s, compute_entropy,
-                                 g_lp, g_ent, cols, ncols, round_dz_bf16, dW_cols);
+                                 g_lp, g_ent, cols, ncols, round_dz_bf16, dW_cols, logprob, lse,
+                                 entropy);
 }
 
 /* The oracle's binary32 -> bf16 rounding (round to nearest, ties to even),
@@ -419,7 +440,20 @@ int flpo_num_threads(void) {
 int flpo_loss(const double* lp, const int64_t* y, int64_t M, int64_t ignore_index, int kind,
               const double* old_lp, const double* adv, const double* ref_lp, double eps_low,
               double eps_high, double beta, double* per_row, double* grad, double* loss) {
-    if (M < 0 || (kind != 1 && kind != 2)) return FLPO_INVALID_ARG;
+    if (M < 0 || (kind != 1 && kind != 2 && kind != 3)) return FLPO_INVALID_ARG;
+    if (kind == 3) {
+        /* kind 3 (token-sum NLL): loss = -sum_i lp_i over the valid rows, no
+         * normalisation; d loss / d lp_i = -1 on a valid row. */
+        double total = 0.0;
+        for (int64_t i = 0; i < M; ++i) {
+            int valid = y[i] != ignore_index;
+            if (per_row) per_row[i] = valid ? -lp[i] : 0.0;
+            if (grad) grad[i] = valid ? -1.0 : 0.0;
+            if (valid) total += -lp[i];
+        }
+        if (loss) *loss = total;
+        return FLPO_OK;
+    }
     if (kind == 2 && (!old_lp || !adv)) return FLPO_INVALID_ARG;
     int64_t n = 0;
     for (int64_t i = 0; i < M; ++i)
@@ -452,5 +486,104 @@ int flpo_loss(const double* lp, const int64_t* y, int64_t M, int64_t ignore_inde
         if (grad) grad[i] = n > 0 ? g / (double)n : 0.0;
     }
     if (loss) *loss = n > 0 ? total / (double)n : 0.0;
+    return FLPO_OK;
+}
+
+/*
+ * Policy-gradient loss over sequences (the chunked GRPO page: "Setup" runs
+ * loss_type="dapo" with importance_sampling_level="sequence" and
+ * num_items_in_batch; "Correctness" lists the grpo / bnpo / dr_grpo / dapo
+ * aggregations with token- and sequence-level importance sampling).  The page
+ * names these options without defining them; the readings taken here:
+ *
+ *   rows [off[b], off[b+1]) form sequence b (b < B); a row is a token of the
+ *   loss when its target is not ignore_index; n_b = tokens of sequence b,
+ *   N = sum_b n_b.  off == NULL means one sequence of all M rows.
+ *   ratio, token level:    log r_t = lp_t - old_t
+ *   ratio, sequence level: log r_t = (1/n_b) sum_{u in b} (lp_u - old_u)  (every t in b)
+ *   term_t = -min(r_t A_t, clip(r_t, 1 - eps_low, 1 + eps_high) A_t)
+ *            + beta (exp(ref_t - lp_t) - (ref_t - lp_t) - 1)   (KL only when ref given)
+ *   aggregation 0, token mean (bnpo):     loss = (1/N) sum_t term_t
+ *   aggregation 1, sequence mean (grpo):  loss = (1/B) sum_b (1/max(n_b, 1)) sum_{t in b} term_t
+ *   aggregation 2, sum over a normaliser (dapo: num_items_in_batch; dr_grpo:
+ *                 B x the longest completion):  loss = (1/D) sum_t term_t,
+ *                 D = normalizer when > 0, else N
+ *
+ * Outputs: per-token terms (0 on rows that are not tokens), the scalar loss,
+ * and d loss / d lp_t.  Each token's weight in the loss is c_t (1/N,
+ * 1/(B max(n_b, 1)) or 1/D); the min picks r A unless the clipped term is
+ * strictly smaller, and a clipped ratio has zero derivative.  With a
+ * sequence-level ratio every term of sequence b depends on every lp_u of b
+ * through log r_b, whose derivative with respect to lp_u is 1/n_b.
+ */
+int flpo_policy_loss(const double* lp, const int64_t* y, int64_t M, int64_t ignore_index,
+                     const int64_t* off, int64_t B, const double* old_lp, const double* adv,
+                     const double* ref_lp, double eps_low, double eps_high, double beta,
+                     int is_level, int aggregation, double normalizer, double* per_row,
+                     double* grad, double* loss) {
+    if (M < 0 || !old_lp || !adv || (is_level != 0 && is_level != 1) || aggregation < 0 ||
+        aggregation > 2)
+        return FLPO_INVALID_ARG;
+    int64_t one_seq[2] = {0, M};
+    if (!off) {
+        off = one_seq;
+        B = 1;
+    }
+    if (B < 1) return FLPO_INVALID_ARG;
+    for (int64_t b = 0; b < B; ++b)
+        if (off[b] < 0 || off[b + 1] < off[b] || off[b + 1] > M) return FLPO_INVALID_ARG;
+    for (int64_t i = 0; i < M; ++i) {
+        if (per_row) per_row[i] = 0.0;
+        if (grad) grad[i] = 0.0;
+    }
+    int64_t N = 0;
+    for (int64_t b = 0; b < B; ++b)
+        for (int64_t t = off[b]; t < off[b + 1]; ++t)
+            if (y[t] != ignore_index) ++N;
+    double D = (aggregation == 2 && normalizer > 0.0) ? normalizer : (double)N;
+    double total = 0.0;
+    double lo = 1.0 - eps_low, hi = 1.0 + eps_high;
+    for (int64_t b = 0; b < B; ++b) {
+        int64_t nb = 0;
+        double sum_log = 0.0;
+        for (int64_t t = off[b]; t < off[b + 1]; ++t)
+            if (y[t] != ignore_index) {
+                ++nb;
+                sum_log += lp[t] - old_lp[t];
+            }
+        double seq_log_r = nb > 0 ? sum_log / (double)nb : 0.0;
+        double c;
+        if (aggregation == 0) c = N > 0 ? 1.0 / (double)N : 0.0;
+        else if (aggregation == 1) c = 1.0 / ((double)B * (double)(nb > 0 ? nb : 1));
+        else c = D > 0.0 ? 1.0 / D : 0.0;
+        double G = 0.0; /* sum over the tokens of b of c * d term_t / d log r_b */
+        for (int64_t t = off[b]; t < off[b + 1]; ++t) {
+            if (y[t] == ignore_index) continue;
+            double log_r = is_level == 1 ? seq_log_r : lp[t] - old_lp[t];
+            double r = exp(log_r);
+            double rc = r < lo ? lo : (r > hi ? hi : r);
+            double s1 = r * adv[t], s2 = rc * adv[t];
+            double term = -(s1 <= s2 ? s1 : s2);
+            double dterm_dlogr = s1 <= s2 ? -r * adv[t] : 0.0;
+            double g_kl = 0.0;
+            if (ref_lp && beta != 0.0) {
+                double d = ref_lp[t] - lp[t];
+                term += beta * (exp(d) - d - 1.0);
+                g_kl = beta * (1.0 - exp(d));
+            }
+            if (per_row) per_row[t] = term;
+            total += c * term;
+            if (is_level == 1) {
+                G += c * dterm_dlogr;
+                if (grad) grad[t] = c * g_kl;
+            } else if (grad) {
+                grad[t] = c * (dterm_dlogr + g_kl);
+            }
+        }
+        if (is_level == 1 && grad && nb > 0)
+            for (int64_t t = off[b]; t < off[b + 1]; ++t)
+                if (y[t] != ignore_index) grad[t] += G / (double)nb;
+    }
+    if (loss) *loss = total;
     return FLPO_OK;
 }

@@ -4,6 +4,7 @@ rows, and central finite differences of the scalar loss."""
 import math
 
 import numpy as np
+import pytest
 
 import oracle
 
@@ -82,3 +83,115 @@ def test_grpo_gradient_matches_finite_differences():
         fd = (oracle.loss(a, y, oracle.LOSS_GRPO, **kw)[2] - oracle.loss(b, y, oracle.LOSS_GRPO, **kw)[2]) / (2 * eps)
         assert abs(fd - grad[i]) < 1e-8, (i, fd, grad[i])
     assert grad[4] == 0.0
+
+
+# ------------------------------------------------ token-sum NLL
+
+def test_nll_sum_closed_form():
+    lp = np.array([-1.0, -2.5, 0.0, -0.25])
+    y = np.array([3, -100, 7, 1])
+    per, grad, loss = oracle.loss(lp, y, oracle.LOSS_NLL_SUM)
+    assert loss == 1.25
+    np.testing.assert_array_equal(grad, [-1.0, 0.0, -1.0, -1.0])
+    np.testing.assert_array_equal(per, [1.0, 0.0, 0.0, 0.25])
+
+
+# ------------------------------------------------ policy loss over sequences
+
+def test_sequence_ratio_closed_form():
+    """Two sequences; hand-derived values.  Sequence 0 has two tokens with
+    lp - old = 0.1 and 0.3 (one ignored row between them): log r = 0.2,
+    r = e^0.2 = 1.2214 > 1 + 0.2.  With A = +1 the clipped term wins
+    (-1.2 each, zero gradient); with A = -1 the unclipped one (r each, and
+    each lp_u gets -A r / n_b summed over the two tokens' weights).
+    Sequence 1 has one token, lp - old = log 0.9 (inside the range)."""
+    lp = np.array([-1.0, -5.0, -2.0, -0.5])
+    old = np.array([-1.1, -5.0, -2.3, -0.5 - math.log(0.9)])
+    y = np.array([4, -100, 2, 9])
+    off = np.array([0, 3, 4])
+    r0, r1 = math.exp(0.2), 0.9
+    for A0, A1 in ((1.0, 2.0), (-1.0, 2.0)):
+        adv = np.array([A0, 0.0, A0, A1])
+        per, grad, loss = oracle.policy_loss(lp, y, old, adv, off, is_level=oracle.IS_SEQUENCE,
+                                             aggregation=oracle.AGG_SUM_OVER, normalizer=5.0)
+        t0 = -min(r0 * A0, 1.2 * A0)
+        t1 = -r1 * A1
+        np.testing.assert_allclose(per, [t0, 0.0, t0, t1], rtol=1e-14)
+        assert abs(loss - (2 * t0 + t1) / 5.0) < 1e-14
+        g0 = 0.0 if A0 > 0 else (2 * (-r0 * A0) / 5.0) / 2
+        np.testing.assert_allclose(grad, [g0, 0.0, g0, -r1 * A1 / 5.0], rtol=1e-14, atol=1e-16)
+    # aggregation: sequence mean (grpo) with the same terms, A0 = -1
+    per, grad, loss = oracle.policy_loss(lp, y, old, np.array([-1.0, 0, -1.0, 2.0]), off,
+                                         is_level=oracle.IS_SEQUENCE,
+                                         aggregation=oracle.AGG_SEQUENCE_MEAN)
+    t0, t1 = r0, -r1 * 2.0
+    assert abs(loss - 0.5 * ((2 * t0) / 2 + t1 / 1)) < 1e-14
+
+
+def _policy_case(seed, M=23):
+    r = np.random.default_rng(seed)
+    lp = r.normal(-2, 0.5, M)
+    old = lp + r.normal(0, 0.05, M)  # ratios near 1, away from the clip edges
+    adv = r.normal(0, 1, M)
+    ref = lp + r.normal(0, 0.3, M)
+    y = r.integers(0, 10, M)
+    y[[3, 11]] = -100
+    off = np.array([0, 5, 5, 12, 20, M])  # an empty sequence, ragged lengths
+    return lp, y, old, adv, ref, off
+
+
+@pytest.mark.parametrize("is_level", [0, 1])
+@pytest.mark.parametrize("agg,norm", [(0, 0.0), (1, 0.0), (2, 0.0), (2, 57.0)])
+def test_policy_loss_gradient_matches_finite_differences(is_level, agg, norm):
+    lp, y, old, adv, ref, off = _policy_case(5)
+    kw = dict(seq_offsets=off, ref_logprob=ref, eps_low=0.3, eps_high=0.4, beta=0.05,
+              is_level=is_level, aggregation=agg, normalizer=norm)
+    _, grad, _ = oracle.policy_loss(lp, y, old, adv, **kw)
+    eps = 1e-6
+    for i in range(lp.size):
+        a, b = lp.copy(), lp.copy()
+        a[i] += eps
+        b[i] -= eps
+        fd = (oracle.policy_loss(a, y, old, adv, **kw)[2] - oracle.policy_loss(b, y, old, adv, **kw)[2]) / (2 * eps)
+        assert abs(fd - grad[i]) < 1e-8, (i, fd, grad[i])
+    assert grad[3] == 0.0 and grad[11] == 0.0
+
+
+def test_policy_loss_reductions():
+    lp, y, old, adv, ref, off = _policy_case(6)
+    kw = dict(ref_logprob=ref, eps_low=0.2, eps_high=0.28, beta=0.04)
+    # token-level ratio, token mean: the clipped surrogate of flpo_loss
+    p0, g0, l0 = oracle.loss(lp, y, oracle.LOSS_GRPO, old_logprob=old, advantage=adv, **kw)
+    p1, g1, l1 = oracle.policy_loss(lp, y, old, adv, off, **kw)
+    np.testing.assert_allclose(p1, p0, rtol=1e-14)
+    np.testing.assert_allclose(g1, g0, rtol=1e-13, atol=1e-17)
+    assert abs(l1 - l0) < 1e-14
+    # dapo without num_items_in_batch normalises by the token count: bnpo
+    _, g2, l2 = oracle.policy_loss(lp, y, old, adv, off, aggregation=oracle.AGG_SUM_OVER, **kw)
+    np.testing.assert_allclose(g2, g0, rtol=1e-13, atol=1e-17)
+    assert abs(l2 - l0) < 1e-14
+    # ... and with it, the same sum over another denominator
+    N = int((y != -100).sum())
+    _, g3, l3 = oracle.policy_loss(lp, y, old, adv, off, aggregation=oracle.AGG_SUM_OVER,
+                                   normalizer=4 * N, **kw)
+    assert abs(4 * l3 - l0) < 1e-14
+    np.testing.assert_allclose(4 * g3, g0, rtol=1e-13, atol=1e-17)
+    # one token per sequence: the sequence-level ratio is the token-level one
+    M = lp.size
+    ones = np.arange(M + 1)
+    for agg in (0, 1, 2):
+        a = oracle.policy_loss(lp, y, old, adv, ones, aggregation=agg, is_level=1, **kw)
+        b = oracle.policy_loss(lp, y, old, adv, ones, aggregation=agg, is_level=0, **kw)
+        np.testing.assert_allclose(a[0], b[0], rtol=1e-14)
+        np.testing.assert_allclose(a[1], b[1], rtol=1e-13, atol=1e-17)
+    # sequences of equal token counts: the sequence mean is the token mean
+    yy = np.zeros(20, dtype=np.int64)
+    eq = np.array([0, 5, 10, 15, 20])
+    c = oracle.policy_loss(lp[:20], yy, old[:20], adv[:20], eq, aggregation=1, is_level=1, **kw)
+    d = oracle.policy_loss(lp[:20], yy, old[:20], adv[:20], eq, aggregation=0, is_level=1, **kw)
+    assert abs(c[2] - d[2]) < 1e-14
+    np.testing.assert_allclose(c[1], d[1], rtol=1e-13, atol=1e-17)
+    # no offsets: one sequence of every row
+    e = oracle.policy_loss(lp, y, old, adv, None, is_level=1, **kw)
+    f = oracle.policy_loss(lp, y, old, adv, np.array([0, M]), is_level=1, **kw)
+    np.testing.assert_array_equal(e[1], f[1])
