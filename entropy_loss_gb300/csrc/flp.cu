@@ -432,6 +432,88 @@ flp_status common_checks(const void* X, const void* W, const int64_t* targets, i
     return FLP_OK;
 }
 
+// The forward's two launches for plan f, its scratch (header with the error
+// word, per-split partials, target logits) at ws: the header is cleared, the
+// tile kernel writes the raw partials, the merge the outputs.  Shared by the
+// workspace forward, the allocation-free forward and the wait self-test, so
+// that their results come from the same code.
+flp_status launch_forward(const void* X, const void* W, const int64_t* targets, int64_t M, int64_t H,
+                          int64_t V, int64_t ignore_index, float scale, int ent, float* logprob,
+                          float* lse, float* entropy, const FwdPlan& f, uint8_t* ws,
+                          unsigned long long wait_limit_ns, int debug_stall_after, cudaStream_t s) {
+    int* err = reinterpret_cast<int*>(ws);
+    FLP_CUDA(cudaMemsetAsync(ws, 0, kHeaderBytes, s));
+    if (M == 0) return FLP_OK;
+
+    CUtensorMap tmX, tmW;
+    flp_status st = tmap_2d(&tmX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, X, H, M, H * 2, BK, BM);
+    if (st != FLP_OK) return st;
+    st = tmap_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, W, H, V, H * 2, BK, BNH);
+    if (st != FLP_OK) return st;
+
+    FwdParams p{};
+    p.units = f.units;
+    p.Mt = f.Mt;
+    p.Nt = f.Vt;
+    p.S = f.S;
+    p.tps = f.tps;
+    p.GM = f.GM;
+    p.KB = static_cast<int>(cdiv(H, BK));
+    p.M = static_cast<int>(M);
+    p.V = static_cast<int>(V);
+    p.ignore_index = ignore_index;
+    p.scale = scale;
+    p.scale2 = scale * LOG2E;
+    p.y = reinterpret_cast<const long long*>(targets);
+    p.part_m = reinterpret_cast<float*>(ws + f.off_m);
+    p.part_s = reinterpret_cast<float*>(ws + f.off_s);
+    p.part_t = ent ? reinterpret_cast<float*>(ws + f.off_t) : nullptr;
+    p.zy = reinterpret_cast<float*>(ws + f.off_zy);
+    p.err = err;
+    p.wait_limit_ns = wait_limit_ns;
+    p.debug_stall_after = debug_stall_after;
+    mark(0, s);
+    st = ent ? launch_fwd<true>(f.grid, tmX, tmW, p, s) : launch_fwd<false>(f.grid, tmX, tmW, p, s);
+    if (st != FLP_OK) return st;
+    mark(1, s);
+
+    MergeParams mp{};
+    mp.M = static_cast<int>(M);
+    mp.S = 2 * f.S;  // two 256-column halves per split
+    mp.V = static_cast<int>(V);
+    mp.ignore_index = ignore_index;
+    mp.compute_entropy = ent;
+    mp.y = p.y;
+    mp.part_m = p.part_m;
+    mp.part_s = p.part_s;
+    mp.part_t = p.part_t;
+    mp.zy = p.zy;
+    mp.logprob = logprob;
+    mp.lse = lse;
+    mp.entropy = entropy;
+    mp.err = err;
+    mark(2, s);
+    flp_merge_kernel<<<static_cast<unsigned>(cdiv(M, MERGE_ROWS)), MERGE_ROWS * MERGE_WAYS, 0, s>>>(mp);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "flp_merge_kernel launch");
+    mark(3, s);
+    return FLP_OK;
+}
+
+// Argument checks shared by both forward entry points.
+flp_status forward_checks(const void* X, const void* W, const int64_t* targets, int64_t M, int64_t H,
+                          int64_t V, float scale, int ent, const float* logprob, const float* lse,
+                          const float* entropy) {
+    flp_status st = common_checks(X, W, targets, M, H, V);
+    if (st != FLP_OK) return st;
+    if (M > 0 && (!logprob || !lse || (ent && !entropy) || (!ent && entropy)))
+        return fail(FLP_ERR_INVALID_ARG, "logprob and lse required; entropy iff compute_entropy");
+    if (!aligned16(logprob) || !aligned16(lse) || (entropy && !aligned16(entropy)))
+        return fail(FLP_ERR_INVALID_ARG, "outputs must be 16-byte aligned");
+    if (!std::isfinite(scale)) return fail(FLP_ERR_INVALID_ARG, "scale must be finite");
+    return FLP_OK;
+}
+
 }  // namespace
 
 // =================================================================== C ABI
@@ -462,7 +544,12 @@ flp_status flp_set_phase_events(void* const* events, int count) {
 }
 
 flp_status flp_workspace_query(int64_t M, int64_t H, int64_t V, int compute_entropy,
-                               int64_t chunk_rows, size_t* fwd_bytes, size_t* bwd_bytes) {
+                               size_t* fwd_bytes, size_t* bwd_bytes) {
+    return flp_workspace_query_ex(M, H, V, compute_entropy, 0, fwd_bytes, bwd_bytes);
+}
+
+flp_status flp_workspace_query_ex(int64_t M, int64_t H, int64_t V, int compute_entropy,
+                                  int64_t chunk_rows, size_t* fwd_bytes, size_t* bwd_bytes) {
     if (M < 0 || H < 1 || V < 1) return fail(FLP_ERR_INVALID_ARG, "M >= 0, H >= 1 and V >= 1 required");
     DevInfo* d;
     flp_status st = check_device(&d);
@@ -477,14 +564,9 @@ flp_status flp_forward(const void* X, const void* W, const int64_t* targets, int
                        int compute_entropy, float* logprob, float* lse, float* entropy,
                        void* workspace, size_t workspace_bytes, void* stream) {
     NvtxRange range("flp_forward");
-    flp_status st = common_checks(X, W, targets, M, H, V);
-    if (st != FLP_OK) return st;
     const int ent = compute_entropy ? 1 : 0;
-    if (M > 0 && (!logprob || !lse || (ent && !entropy) || (!ent && entropy)))
-        return fail(FLP_ERR_INVALID_ARG, "logprob and lse required; entropy iff compute_entropy");
-    if (!aligned16(logprob) || !aligned16(lse) || (entropy && !aligned16(entropy)))
-        return fail(FLP_ERR_INVALID_ARG, "outputs must be 16-byte aligned");
-    if (!std::isfinite(scale)) return fail(FLP_ERR_INVALID_ARG, "scale must be finite");
+    flp_status st = forward_checks(X, W, targets, M, H, V, scale, ent, logprob, lse, entropy);
+    if (st != FLP_OK) return st;
     DevInfo* d;
     st = check_device(&d);
     if (st != FLP_OK) return st;
@@ -492,65 +574,9 @@ flp_status flp_forward(const void* X, const void* W, const int64_t* targets, int
     const FwdPlan f = plan_forward(M, H, V, ent, d->pairs);
     if (!workspace || workspace_bytes < f.bytes || !aligned16(workspace))
         return fail(FLP_ERR_WORKSPACE, "forward workspace null, misaligned or too small");
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    uint8_t* ws = static_cast<uint8_t*>(workspace);
-    int* err = reinterpret_cast<int*>(ws);
-    FLP_CUDA(cudaMemsetAsync(ws, 0, kHeaderBytes, s));
-    if (M == 0) return FLP_OK;
-
-    CUtensorMap tmX, tmW;
-    st = tmap_2d(&tmX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, X, H, M, H * 2, BK, BM);
-    if (st != FLP_OK) return st;
-    st = tmap_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, W, H, V, H * 2, BK, BNH);
-    if (st != FLP_OK) return st;
-
-    FwdParams p{};
-    p.units = f.units;
-    p.Mt = f.Mt;
-    p.Nt = f.Vt;
-    p.S = f.S;
-    p.tps = f.tps;
-    p.GM = f.GM;
-    p.KB = static_cast<int>(cdiv(H, BK));
-    p.M = static_cast<int>(M);
-    p.V = static_cast<int>(V);
-    p.ignore_index = ignore_index;
-    p.scale = scale;
-    p.scale2 = scale * LOG2E;
-    p.y = reinterpret_cast<const long long*>(targets);
-    p.part_m = reinterpret_cast<float*>(ws + f.off_m);
-    p.part_s = reinterpret_cast<float*>(ws + f.off_s);
-    p.part_t = ent ? reinterpret_cast<float*>(ws + f.off_t) : nullptr;
-    p.zy = reinterpret_cast<float*>(ws + f.off_zy);
-    p.err = err;
-    p.wait_limit_ns = kWaitLimitNs;
-    p.debug_stall_after = -1;
-    mark(0, s);
-    st = ent ? launch_fwd<true>(f.grid, tmX, tmW, p, s) : launch_fwd<false>(f.grid, tmX, tmW, p, s);
-    if (st != FLP_OK) return st;
-    mark(1, s);
-
-    MergeParams mp{};
-    mp.M = static_cast<int>(M);
-    mp.S = 2 * f.S;  // two 256-column halves per split
-    mp.V = static_cast<int>(V);
-    mp.ignore_index = ignore_index;
-    mp.compute_entropy = ent;
-    mp.y = p.y;
-    mp.part_m = p.part_m;
-    mp.part_s = p.part_s;
-    mp.part_t = p.part_t;
-    mp.zy = p.zy;
-    mp.logprob = logprob;
-    mp.lse = lse;
-    mp.entropy = entropy;
-    mp.err = err;
-    mark(2, s);
-    flp_merge_kernel<<<static_cast<unsigned>(cdiv(M, MERGE_ROWS)), MERGE_ROWS * MERGE_WAYS, 0, s>>>(mp);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return cuda_fail(e, "flp_merge_kernel launch");
-    mark(3, s);
-    return FLP_OK;
+    return launch_forward(X, W, targets, M, H, V, ignore_index, scale, ent, logprob, lse, entropy, f,
+                          static_cast<uint8_t*>(workspace), kWaitLimitNs, -1,
+                          static_cast<cudaStream_t>(stream));
 }
 
 flp_status flp_backward_plan(int64_t M, int64_t H, int64_t V, size_t workspace_bytes,
@@ -1085,14 +1111,10 @@ extern "C" flp_status flp_forward_noalloc(const void* X, const void* W, const in
                                           int64_t M, int64_t H, int64_t V, int64_t ignore_index,
                                           float scale, int compute_entropy, float* logprob,
                                           float* lse, float* entropy, void* stream) {
-    flp_status st = common_checks(X, W, targets, M, H, V);
-    if (st != FLP_OK) return st;
+    NvtxRange range("flp_forward_noalloc");
     const int ent = compute_entropy ? 1 : 0;
-    if (M > 0 && (!logprob || !lse || (ent && !entropy) || (!ent && entropy)))
-        return fail(FLP_ERR_INVALID_ARG, "logprob and lse required; entropy iff compute_entropy");
-    if (!aligned16(logprob) || !aligned16(lse) || (entropy && !aligned16(entropy)))
-        return fail(FLP_ERR_INVALID_ARG, "outputs must be 16-byte aligned");
-    if (!std::isfinite(scale)) return fail(FLP_ERR_INVALID_ARG, "scale must be finite");
+    flp_status st = forward_checks(X, W, targets, M, H, V, scale, ent, logprob, lse, entropy);
+    if (st != FLP_OK) return st;
     DevInfo* d;
     int dev = 0;
     st = device_info(&d, &dev);
@@ -1112,60 +1134,9 @@ extern "C" flp_status flp_forward_noalloc(const void* X, const void* W, const in
     uint8_t* ws = nullptr;
     st = static_scratch(dev, &ws);
     if (st != FLP_OK) return st;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    int* err = reinterpret_cast<int*>(ws);
-    FLP_CUDA(cudaMemsetAsync(ws, 0, kHeaderBytes, s));  // the array keeps the last call's contents
-    if (M == 0) return FLP_OK;
-
-    CUtensorMap tmX, tmW;
-    st = tmap_2d(&tmX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, X, H, M, H * 2, BK, BM);
-    if (st != FLP_OK) return st;
-    st = tmap_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, W, H, V, H * 2, BK, BNH);
-    if (st != FLP_OK) return st;
-
-    FwdParams p{};
-    p.units = f.units;
-    p.Mt = f.Mt;
-    p.Nt = f.Vt;
-    p.S = f.S;
-    p.tps = f.tps;
-    p.GM = f.GM;
-    p.KB = static_cast<int>(cdiv(H, BK));
-    p.M = static_cast<int>(M);
-    p.V = static_cast<int>(V);
-    p.ignore_index = ignore_index;
-    p.scale = scale;
-    p.scale2 = scale * LOG2E;
-    p.y = reinterpret_cast<const long long*>(targets);
-    p.part_m = reinterpret_cast<float*>(ws + f.off_m);
-    p.part_s = reinterpret_cast<float*>(ws + f.off_s);
-    p.part_t = ent ? reinterpret_cast<float*>(ws + f.off_t) : nullptr;
-    p.zy = reinterpret_cast<float*>(ws + f.off_zy);
-    p.err = err;
-    p.wait_limit_ns = kWaitLimitNs;
-    p.debug_stall_after = -1;
-    st = ent ? launch_fwd<true>(f.grid, tmX, tmW, p, s) : launch_fwd<false>(f.grid, tmX, tmW, p, s);
-    if (st != FLP_OK) return st;
-
-    MergeParams mp{};
-    mp.M = static_cast<int>(M);
-    mp.S = 2 * f.S;  // two 256-column halves per split
-    mp.V = static_cast<int>(V);
-    mp.ignore_index = ignore_index;
-    mp.compute_entropy = ent;
-    mp.y = p.y;
-    mp.part_m = p.part_m;
-    mp.part_s = p.part_s;
-    mp.part_t = p.part_t;
-    mp.zy = p.zy;
-    mp.logprob = logprob;
-    mp.lse = lse;
-    mp.entropy = entropy;
-    mp.err = err;
-    flp_merge_kernel<<<static_cast<unsigned>(cdiv(M, MERGE_ROWS)), MERGE_ROWS * MERGE_WAYS, 0, s>>>(mp);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return cuda_fail(e, "flp_merge_kernel launch");
-    return FLP_OK;
+    // the array keeps the last call's contents: launch_forward clears the header
+    return launch_forward(X, W, targets, M, H, V, ignore_index, scale, ent, logprob, lse, entropy, f, ws,
+                          kWaitLimitNs, -1, static_cast<cudaStream_t>(stream));
 }
 
 // ================================================ bounded-wait self-test
@@ -1186,38 +1157,15 @@ extern "C" flp_status flp_selftest_wait_timeout(void* workspace, size_t workspac
     const size_t off_x = align_up(f.bytes, 1024);
     const size_t off_w = off_x + align_up(M * H * 2, 1024);
     const size_t off_y = off_w + align_up(V * H * 2, 1024);
-    if (off_y + M * 8 > FLP_SELFTEST_WORKSPACE_BYTES)
+    const size_t off_o = FLP_SELFTEST_OUTPUT_OFFSET;
+    if (off_y + M * 8 > off_o || off_o + 3 * M * 4 > FLP_SELFTEST_WORKSPACE_BYTES)
         return fail(FLP_ERR_UNSUPPORTED, "self-test layout exceeds its workspace");
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     FLP_CUDA(cudaMemsetAsync(ws, 0, off_y + M * 8, s));  // header, inputs (zeros) and targets (0)
-
-    CUtensorMap tmX, tmW;
-    st = tmap_2d(&tmX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, ws + off_x, H, M, H * 2, BK, BM);
-    if (st != FLP_OK) return st;
-    st = tmap_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, ws + off_w, H, V, H * 2, BK, BNH);
-    if (st != FLP_OK) return st;
-    FwdParams p{};
-    p.units = f.units;
-    p.Mt = f.Mt;
-    p.Nt = f.Vt;
-    p.S = f.S;
-    p.tps = f.tps;
-    p.GM = f.GM;
-    p.KB = static_cast<int>(cdiv(H, BK));
-    p.M = static_cast<int>(M);
-    p.V = static_cast<int>(V);
-    p.ignore_index = -100;
-    p.scale = 1.f;
-    p.scale2 = LOG2E;
-    p.y = reinterpret_cast<const long long*>(ws + off_y);
-    p.part_m = reinterpret_cast<float*>(ws + f.off_m);
-    p.part_s = reinterpret_cast<float*>(ws + f.off_s);
-    p.part_t = reinterpret_cast<float*>(ws + f.off_t);
-    p.zy = reinterpret_cast<float*>(ws + f.off_zy);
-    p.err = reinterpret_cast<int*>(ws);
-    p.wait_limit_ns = static_cast<unsigned long long>(wait_limit_ns);
-    p.debug_stall_after = stall_after < 0 ? -1 : stall_after;
-    st = launch_fwd<true>(f.grid, tmX, tmW, p, s);
+    float* out = reinterpret_cast<float*>(ws + off_o);   // logprob, lse, entropy: fp32 [M] each
+    st = launch_forward(ws + off_x, ws + off_w, reinterpret_cast<const int64_t*>(ws + off_y), M, H, V, -100,
+                        1.f, 1, out, out + M, out + 2 * M, f, ws, static_cast<unsigned long long>(wait_limit_ns),
+                        stall_after < 0 ? -1 : stall_after, s);
     if (st != FLP_OK) return st;
     return flp_get_error(workspace, stream);
 }
@@ -1367,7 +1315,7 @@ extern "C" flp_status flp_loss(const float* logprob, const int64_t* targets, int
                                float eps_high, float beta, float* per_token_loss,
                                float* grad_logprob, float* loss, void* stream) {
     if (M < 0) return fail(FLP_ERR_INVALID_ARG, "M >= 0 required");
-    if (kind != FLP_LOSS_NLL_MEAN && kind != FLP_LOSS_CLIPPED_SURROGATE)
+    if (kind != FLP_LOSS_NLL_MEAN && kind != FLP_LOSS_CLIPPED_SURROGATE && kind != FLP_LOSS_NLL_SUM)
         return fail(FLP_ERR_INVALID_ARG, "unknown loss kind");
     if (!loss || (M > 0 && (!logprob || !targets)))
         return fail(FLP_ERR_INVALID_ARG, "logprob, targets and loss must be non-null");
@@ -1398,5 +1346,54 @@ extern "C" flp_status flp_loss(const float* logprob, const int64_t* targets, int
     flp_loss_kernel<<<1, LOSS_THREADS, 0, s>>>(p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "flp_loss_kernel launch");
+    return FLP_OK;
+}
+
+extern "C" flp_status flp_policy_loss(const float* logprob, const int64_t* targets, int64_t M,
+                                      int64_t ignore_index, const int64_t* seq_offsets,
+                                      int64_t num_seqs, const float* old_logprob,
+                                      const float* advantage, const float* ref_logprob, float eps_low,
+                                      float eps_high, float beta, int is_level, int aggregation,
+                                      double normalizer, float* per_token_loss, float* grad_logprob,
+                                      float* loss, void* stream) {
+    if (M < 0) return fail(FLP_ERR_INVALID_ARG, "M >= 0 required");
+    if (is_level != FLP_IS_TOKEN && is_level != FLP_IS_SEQUENCE)
+        return fail(FLP_ERR_INVALID_ARG, "is_level must be FLP_IS_TOKEN or FLP_IS_SEQUENCE");
+    if (aggregation != FLP_AGG_TOKEN_MEAN && aggregation != FLP_AGG_SEQUENCE_MEAN &&
+        aggregation != FLP_AGG_SUM_OVER)
+        return fail(FLP_ERR_INVALID_ARG, "unknown aggregation");
+    if (!loss || (M > 0 && (!logprob || !targets || !old_logprob || !advantage)))
+        return fail(FLP_ERR_INVALID_ARG, "logprob, targets, old_logprob, advantage and loss must be non-null");
+    if (seq_offsets && num_seqs < 1)
+        return fail(FLP_ERR_INVALID_ARG, "num_seqs >= 1 required with seq_offsets");
+    if (!(eps_low >= 0.f && eps_low <= 1.f && eps_high >= 0.f && std::isfinite(eps_high) &&
+          std::isfinite(beta) && std::isfinite(normalizer)))
+        return fail(FLP_ERR_INVALID_ARG, "eps_low in [0, 1], eps_high >= 0, finite beta and normalizer required");
+    DevInfo* d;
+    flp_status st = device_info(&d, nullptr);
+    if (st != FLP_OK) return st;
+    PolicyLossParams p{};
+    p.lp = logprob;
+    p.y = reinterpret_cast<const long long*>(targets);
+    p.M = M;
+    p.ignore_index = ignore_index;
+    p.off = reinterpret_cast<const long long*>(seq_offsets);
+    p.B = seq_offsets ? num_seqs : 1;
+    p.old_lp = old_logprob;
+    p.adv = advantage;
+    p.ref_lp = ref_logprob;
+    p.eps_low = eps_low;
+    p.eps_high = eps_high;
+    p.beta = beta;
+    p.is_level = is_level;
+    p.aggregation = aggregation;
+    p.normalizer = normalizer;
+    p.per_row = per_token_loss;
+    p.grad = grad_logprob;
+    p.loss = loss;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    flp_policy_loss_kernel<<<1, LOSS_THREADS, 0, s>>>(p);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "flp_policy_loss_kernel launch");
     return FLP_OK;
 }

@@ -675,12 +675,23 @@ constexpr int MERGE_BATCH = 8;   // splits whose loads a warp has in flight at o
 // entropy (the "reduced" and "result" stages kept in buffers separate from the
 // raw partials).  Each warp reads a stripe of splits for 32 consecutive rows
 // (coalesced), the stripes are combined through shared memory.  Base-2 units
-// inside, natural log out.
+// inside, natural log out.  When the forward tile kernel gave up on a wait
+// (timeout bit in the error word) its partials are incomplete: every output
+// row is then NaN, so that no stale or partial value passes for a result.
 __global__ void __launch_bounds__(MERGE_ROWS * MERGE_WAYS) flp_merge_kernel(const MergeParams p) {
     __shared__ Stats part[MERGE_WAYS][MERGE_ROWS];
     const int lane = threadIdx.x & 31;
     const int w = threadIdx.x >> 5;
     const int i = blockIdx.x * MERGE_ROWS + lane;
+    if (*reinterpret_cast<volatile const int*>(p.err) & ERR_TIMEOUT) {
+        if (w == 0 && i < p.M) {
+            const float nan = __int_as_float(0x7fc00000);
+            p.lse[i] = nan;
+            p.logprob[i] = nan;
+            if (p.compute_entropy) p.entropy[i] = nan;
+        }
+        return;
+    }
     Stats acc{-INFINITY, 0.f, 0.f};
     if (i < p.M) {
         // splits w, w + 8, w + 16, ... in order; the loads of MERGE_BATCH of

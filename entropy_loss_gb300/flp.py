@@ -25,14 +25,21 @@ FLP_ERR_TIMEOUT = 6
 FLP_F32 = 0
 FLP_BF16 = 1
 
-EXPORTS = ("flp_workspace_query", "flp_forward", "flp_backward", "flp_get_error",
+EXPORTS = ("flp_workspace_query", "flp_workspace_query_ex", "flp_forward", "flp_backward", "flp_get_error",
            "flp_set_phase_events", "flp_status_string", "flp_last_error_message",
            "flp_forward_noalloc", "flp_selftest_wait_timeout", "flp_loss", "flp_backward_ex",
            "flp_backward_plan", "flp_backward_schedule", "flp_selftest_dependency_timeout",
-           "flp_selftest_dz_wait_timeout")
+           "flp_selftest_dz_wait_timeout", "flp_policy_loss")
 FLP_LOSS_NLL_MEAN = 1
 FLP_LOSS_CLIPPED_SURROGATE = 2
+FLP_LOSS_NLL_SUM = 3
+FLP_IS_TOKEN = 0
+FLP_IS_SEQUENCE = 1
+FLP_AGG_TOKEN_MEAN = 0
+FLP_AGG_SEQUENCE_MEAN = 1
+FLP_AGG_SUM_OVER = 2
 SELFTEST_WORKSPACE_BYTES = 1 << 20
+SELFTEST_OUTPUT_OFFSET = 768 << 10  # the forward self-test's logprob, lse, entropy (fp32 [256] each)
 STATIC_SCRATCH_BYTES = 16 << 20
 FLP_BWD_AUTO = 0
 FLP_BWD_SPLIT = 1
@@ -65,8 +72,10 @@ def load(path: str = LIB_PATH):
         raise FlpError(FLP_ERR_CUDA, f"{path} is missing: build it with entropy_loss_gb300.build.build()")
     lib = ctypes.CDLL(path)
     p, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
-    lib.flp_workspace_query.argtypes = [i64, i64, i64, i32, i64, ctypes.POINTER(ctypes.c_size_t),
+    lib.flp_workspace_query.argtypes = [i64, i64, i64, i32, ctypes.POINTER(ctypes.c_size_t),
                                         ctypes.POINTER(ctypes.c_size_t)]
+    lib.flp_workspace_query_ex.argtypes = [i64, i64, i64, i32, i64, ctypes.POINTER(ctypes.c_size_t),
+                                           ctypes.POINTER(ctypes.c_size_t)]
     lib.flp_forward.argtypes = [p, p, p, i64, i64, i64, i64, ctypes.c_float, i32, p, p, p, p,
                                 ctypes.c_size_t, p]
     lib.flp_backward.argtypes = [p, p, p, i64, i64, i64, i64, ctypes.c_float, i32, p, p, p, p, p,
@@ -94,6 +103,9 @@ def load(path: str = LIB_PATH):
     lib.flp_loss.argtypes = [p, p, i64, i64, i32, p, p, p, ctypes.c_float, ctypes.c_float,
                              ctypes.c_float, p, p, p, p]
     lib.flp_loss.restype = i32
+    lib.flp_policy_loss.argtypes = [p, p, i64, i64, p, i64, p, p, p, ctypes.c_float, ctypes.c_float,
+                                    ctypes.c_float, i32, i32, ctypes.c_double, p, p, p, p]
+    lib.flp_policy_loss.restype = i32
     lib.flp_get_error.argtypes = [p, p]
     lib.flp_set_phase_events.argtypes = [ctypes.POINTER(ctypes.c_void_p), i32]
     lib.flp_set_phase_events.restype = i32
@@ -101,7 +113,8 @@ def load(path: str = LIB_PATH):
     lib.flp_status_string.restype = ctypes.c_char_p
     lib.flp_last_error_message.argtypes = []
     lib.flp_last_error_message.restype = ctypes.c_char_p
-    for name in ("flp_workspace_query", "flp_forward", "flp_backward", "flp_get_error"):
+    for name in ("flp_workspace_query", "flp_workspace_query_ex", "flp_forward", "flp_backward",
+                 "flp_get_error"):
         getattr(lib, name).restype = i32
     _lib = lib
     return lib
@@ -126,11 +139,18 @@ def _stream(stream):
 
 
 def workspace_query(M: int, H: int, V: int, compute_entropy: bool = True, chunk_rows: int = 0):
-    """(forward bytes, backward bytes) on the current device."""
+    """(forward bytes, backward bytes) on the current device; chunk_rows > 0
+    sizes the backward for row waves of that many rows (flp_workspace_query_ex),
+    else for the default waves (flp_workspace_query)."""
     f = ctypes.c_size_t(0)
     b = ctypes.c_size_t(0)
-    _check(load().flp_workspace_query(M, H, V, int(compute_entropy), chunk_rows, ctypes.byref(f),
-                                      ctypes.byref(b)), "flp_workspace_query")
+    lib = load()
+    if chunk_rows > 0:
+        _check(lib.flp_workspace_query_ex(M, H, V, int(compute_entropy), chunk_rows, ctypes.byref(f),
+                                          ctypes.byref(b)), "flp_workspace_query_ex")
+    else:
+        _check(lib.flp_workspace_query(M, H, V, int(compute_entropy), ctypes.byref(f), ctypes.byref(b)),
+               "flp_workspace_query")
     return f.value, b.value
 
 
@@ -352,6 +372,37 @@ def loss(logprob, y, kind=FLP_LOSS_NLL_MEAN, *, ignore_index: int = -100, old_lo
                            _ptr(advantage), _ptr(ref_logprob), float(eps_low), float(eps_high),
                            float(beta), _ptr(per), _ptr(grad), _ptr(out), _stream(stream)),
            "flp_loss")
+    return out, grad, per
+
+
+def policy_loss(logprob, y, old_logprob, advantage, *, seq_offsets=None, ignore_index: int = -100,
+                ref_logprob=None, eps_low: float = 0.2, eps_high: float = 0.2, beta: float = 0.0,
+                is_level: int = FLP_IS_TOKEN, aggregation: int = FLP_AGG_TOKEN_MEAN,
+                normalizer: float = 0.0, per_token=True, stream=None):
+    """Clipped-surrogate loss over sequences (flp_policy_loss): (scalar loss
+    [1], grad_logprob [M], per-token terms [M] or None).  seq_offsets: int64
+    [B + 1] device tensor of the sequences' row offsets (None: one sequence).
+    aggregation FLP_AGG_SUM_OVER with normalizer = num_items_in_batch is dapo."""
+    M = logprob.shape[0]
+    _need(logprob, torch.float32, (M,), "logprob")
+    _need(y, torch.int64, (M,), "targets")
+    _need(old_logprob, torch.float32, (M,), "old_logprob")
+    _need(advantage, torch.float32, (M,), "advantage")
+    _need_opt(ref_logprob, torch.float32, (M,), "ref_logprob")
+    B = 0
+    if seq_offsets is not None:
+        B = seq_offsets.shape[0] - 1
+        _need(seq_offsets, torch.int64, (B + 1,), "seq_offsets")
+    dev = logprob.device
+    out = torch.empty(1, dtype=torch.float32, device=dev)
+    grad = torch.empty(M, dtype=torch.float32, device=dev)
+    per = torch.empty(M, dtype=torch.float32, device=dev) if per_token else None
+    _check(load().flp_policy_loss(_ptr(logprob), _ptr(y), M, ignore_index, _ptr(seq_offsets), B,
+                                  _ptr(old_logprob), _ptr(advantage), _ptr(ref_logprob),
+                                  float(eps_low), float(eps_high), float(beta), int(is_level),
+                                  int(aggregation), float(normalizer), _ptr(per), _ptr(grad),
+                                  _ptr(out), _stream(stream)),
+           "flp_policy_loss")
     return out, grad, per
 
 

@@ -75,24 +75,38 @@ typedef enum {
 typedef enum { FLP_F32 = 0, FLP_BF16 = 1 } flp_dtype;
 
 /*
- * Workspace sizes, in bytes, for the given problem on the current device.
+ * Workspace sizes, in bytes, for the given problem on the current device
+ * (the Liger-Kernel native commit's "Summary" lists reusable workspace
+ * configuration and query APIs).
  *   fwd_bytes : needed by flp_forward (per-split raw partials and the target
  *               logits; the SkyRL page "perf(megatron): autotune fused LM-head
  *               Triton kernels", section "Correctness", keeps raw and final
  *               results in separate buffers, and so does this library).
- *   bwd_bytes : needed by flp_backward when it processes the rows in waves of
- *               `chunk_rows` rows (chunk_rows <= 0 selects 8192); one wave's
- *               bf16 dZ, [chunk, ceil(V/256)*256], dominates, beside a few
- *               KiB of tile counters.  The Liger-Kernel native commit's
- *               "Memory" section reports the same kind of reusable workspace,
- *               and pull request 1294's "Kernel design notes" a reusable
- *               per-chunk grad_logits buffer.
+ *   bwd_bytes : needed by flp_backward with its default row waves of up to
+ *               8192 rows (all M rows when M <= 8192); one wave's bf16 dZ,
+ *               [wave rows, ceil(V/256)*256], dominates, beside a few KiB of
+ *               tile counters.  The native commit's "Memory" section reports
+ *               the same kind of reusable workspace, and pull request 1294's
+ *               "Kernel design notes" a reusable per-chunk grad_logits buffer.
  * Either output pointer may be NULL.  The same buffer may serve both calls.
  * Returns FLP_ERR_INVALID_ARG for negative sizes, FLP_ERR_CUDA if the device
- * cannot be queried.
+ * cannot be queried (FLP_ERR_UNSUPPORTED if it is not an sm_103 device).
  */
 flp_status flp_workspace_query(int64_t M, int64_t H, int64_t V, int compute_entropy,
-                               int64_t chunk_rows, size_t* fwd_bytes, size_t* bwd_bytes);
+                               size_t* fwd_bytes, size_t* bwd_bytes);
+
+/*
+ * flp_workspace_query with the backward's wave size chosen by the caller:
+ * bwd_bytes is what flp_backward needs to process the rows in waves of
+ * `chunk_rows` rows (rounded up to a multiple of 128, at most M;
+ * chunk_rows <= 0 selects the default of flp_workspace_query).  A smaller
+ * wave trades speed for a smaller workspace; below 2048-row waves
+ * flp_backward runs the vocabulary-split schedule instead when the same bytes
+ * also hold its fp32 dX scratch (see flp_backward_ex).  Errors as
+ * flp_workspace_query.
+ */
+flp_status flp_workspace_query_ex(int64_t M, int64_t H, int64_t V, int compute_entropy,
+                                  int64_t chunk_rows, size_t* fwd_bytes, size_t* bwd_bytes);
 
 /*
  * Forward: writes logprob[M], lse[M] and (when compute_entropy != 0)
@@ -101,7 +115,9 @@ flp_status flp_workspace_query(int64_t M, int64_t H, int64_t V, int compute_entr
  * compute_entropy gates the entropy buffers and kernel work).
  * Two kernels run on `stream`: the fused tcgen05 GEMM + online
  * max / sum-exp / target / entropy epilogue writing raw per-split partials to
- * the workspace, then the merge of those partials into the outputs.
+ * the workspace, then the merge of those partials into the outputs.  If a
+ * bounded wait of the first kernel runs out (FLP_ERR_TIMEOUT in the error
+ * word), the merge writes NaN to every output row.
  */
 flp_status flp_forward(const void* X, const void* W, const int64_t* targets, int64_t M,
                        int64_t H, int64_t V, int64_t ignore_index, float scale,
@@ -235,7 +251,9 @@ flp_status flp_backward_schedule(int64_t M, int64_t H, int64_t V, size_t workspa
  *    call's contents (each call clears its error word first): calls that
  *    overlap on the GPU race and corrupt each other's results.
  *  - Out-of-range targets still give logprob = NaN; the error word of this
- *    array is not readable through flp_get_error.
+ *    array is not readable through flp_get_error.  If a bounded wait of the
+ *    forward kernel ever runs out, the merge writes NaN to every output row,
+ *    so a failed call cannot pass stale values from the array for results.
  */
 #define FLP_STATIC_SCRATCH_BYTES (16u << 20)
 flp_status flp_forward_noalloc(const void* X, const void* W, const int64_t* targets, int64_t M,
@@ -248,6 +266,8 @@ flp_status flp_forward_noalloc(const void* X, const void* W, const int64_t* targ
  * "Chunked Triton GRPO loss": a loss on top of the lm_head's per-token
  * log-probs).  With N = the number of rows whose target is not ignore_index:
  *   FLP_LOSS_NLL_MEAN           loss = -(1/N) sum_i lp_i
+ *   FLP_LOSS_NLL_SUM            loss = -sum_i lp_i  (token-sum reduction;
+ *                               grad_logprob = -1 on every valid row)
  *   FLP_LOSS_CLIPPED_SURROGATE  r_i = exp(lp_i - old_i),
  *       loss = (1/N) sum_i [ -min(r_i A_i, clip(r_i, 1 - eps_low, 1 + eps_high) A_i)
  *                            + beta (exp(ref_i - lp_i) - (ref_i - lp_i) - 1) ]
@@ -260,11 +280,51 @@ flp_status flp_forward_noalloc(const void* X, const void* W, const int64_t* targ
  * fp32 on the device.  One block with fixed-order fp64 reductions:
  * deterministic.  N = 0 gives loss 0 and zero gradients.
  */
-typedef enum { FLP_LOSS_NLL_MEAN = 1, FLP_LOSS_CLIPPED_SURROGATE = 2 } flp_loss_kind;
+typedef enum { FLP_LOSS_NLL_MEAN = 1, FLP_LOSS_CLIPPED_SURROGATE = 2, FLP_LOSS_NLL_SUM = 3 } flp_loss_kind;
 flp_status flp_loss(const float* logprob, const int64_t* targets, int64_t M, int64_t ignore_index,
                     int kind, const float* old_logprob, const float* advantage,
                     const float* ref_logprob, float eps_low, float eps_high, float beta,
                     float* per_token_loss, float* grad_logprob, float* loss, void* stream);
+
+/*
+ * Clipped-surrogate policy loss over sequences (the chunked GRPO page: its
+ * "Setup" runs loss_type="dapo" with importance_sampling_level="sequence" and
+ * num_items_in_batch, its "Correctness" section covers the grpo / bnpo /
+ * dr_grpo / dapo aggregations with token- and sequence-level ratios).  The
+ * page names these options without defining them; this library reads them so:
+ *   seq_offsets : int64 [num_seqs + 1] device array; rows [off[b], off[b+1])
+ *                 form sequence b (ranges are clamped to [0, M); they must not
+ *                 overlap).  NULL: one sequence of all M rows.  A row is a
+ *                 token of the loss when its target is not ignore_index; n_b
+ *                 counts the tokens of sequence b, N all of them.
+ *   is_level    : FLP_IS_TOKEN     log r_t = lp_t - old_t
+ *                 FLP_IS_SEQUENCE  log r_t = (1/n_b) sum_{u in b} (lp_u - old_u),
+ *                                  shared by every token of b
+ *   term_t      = -min(r_t A_t, clip(r_t, 1 - eps_low, 1 + eps_high) A_t)
+ *                 + beta (exp(ref_t - lp_t) - (ref_t - lp_t) - 1)  (when ref_logprob != NULL)
+ *   aggregation : FLP_AGG_TOKEN_MEAN     loss = (1/N) sum_t term_t            (bnpo)
+ *                 FLP_AGG_SEQUENCE_MEAN  loss = (1/B) sum_b (1/max(n_b,1)) sum_{t in b} term_t (grpo)
+ *                 FLP_AGG_SUM_OVER       loss = (1/D) sum_t term_t, D = normalizer when > 0
+ *                                        (dapo: num_items_in_batch, the token count of the
+ *                                        whole global batch; dr_grpo: B x the longest
+ *                                        completion), else D = N
+ * Outputs as flp_loss: per_token_loss (term_t, 0 on rows that are not
+ * tokens) and grad_logprob (d loss / d lp_t, the upstream gradient for
+ * flp_backward; with a sequence-level ratio it includes every term of the
+ * sequence through log r_b) may be NULL; loss is one fp32 on the device.
+ * old_logprob and advantage (per row: broadcast a per-sequence advantage) are
+ * required.  One block, fp64 arithmetic, fixed-order reductions:
+ * deterministic.  FLP_LOSS_CLIPPED_SURROGATE of flp_loss is the token-level
+ * ratio with FLP_AGG_TOKEN_MEAN.
+ */
+typedef enum { FLP_IS_TOKEN = 0, FLP_IS_SEQUENCE = 1 } flp_is_level;
+typedef enum { FLP_AGG_TOKEN_MEAN = 0, FLP_AGG_SEQUENCE_MEAN = 1, FLP_AGG_SUM_OVER = 2 } flp_loss_aggregation;
+flp_status flp_policy_loss(const float* logprob, const int64_t* targets, int64_t M,
+                           int64_t ignore_index, const int64_t* seq_offsets, int64_t num_seqs,
+                           const float* old_logprob, const float* advantage,
+                           const float* ref_logprob, float eps_low, float eps_high, float beta,
+                           int is_level, int aggregation, double normalizer,
+                           float* per_token_loss, float* grad_logprob, float* loss, void* stream);
 
 /*
  * Synchronises `stream`, then reads and returns the workspace's error word
@@ -294,18 +354,24 @@ flp_status flp_set_phase_events(void* const* events, int count);
 
 /*
  * Self-test of the kernels' bounded waits (a diagnostic; the pages have no
- * counterpart).  Runs the forward tile kernel on a small internal problem
- * (M = 256, H = 256, V = 512, all-zero inputs) laid out in `workspace`
- * (caller-owned device memory of at least FLP_SELFTEST_WORKSPACE_BYTES).
- * With stall_after >= 0 the TMA producers stop after that many pipeline
- * stages, so the MMA issuer waits for data that never arrives: every wait
- * gives up after wait_limit_ns, the kernel records FLP_ERR_TIMEOUT in the
- * error word, lets its copies and MMAs in flight finish, frees its TMEM and
- * returns; nothing faults and the context stays usable.  With stall_after < 0
- * the same launch runs normally.  Synchronises `stream` and returns the error
- * word (FLP_ERR_TIMEOUT, or FLP_OK), or an argument / CUDA error.
+ * counterpart).  Runs the forward (tile kernel, then the split merge) on a
+ * small internal problem (M = 256, H = 256, V = 512, all-zero inputs, targets
+ * 0) laid out in `workspace` (caller-owned device memory of at least
+ * FLP_SELFTEST_WORKSPACE_BYTES).  With stall_after >= 0 the TMA producers
+ * stop after that many pipeline stages, so the MMA issuer waits for data that
+ * never arrives: every wait gives up after wait_limit_ns, the kernel records
+ * FLP_ERR_TIMEOUT in the error word, lets its copies and MMAs in flight
+ * finish, frees its TMEM and returns; nothing faults and the context stays
+ * usable.  The merge then finds the timeout bit and writes NaN to every
+ * output.  With stall_after < 0 the same launches run normally (every row:
+ * lse = entropy = log 512, logprob = -log 512).  The outputs, fp32 logprob,
+ * lse and entropy of the 256 rows one after the other, are left in the
+ * workspace at byte offset FLP_SELFTEST_OUTPUT_OFFSET.  Synchronises `stream`
+ * and returns the error word (FLP_ERR_TIMEOUT, or FLP_OK), or an argument /
+ * CUDA error.
  */
 #define FLP_SELFTEST_WORKSPACE_BYTES (1u << 20)
+#define FLP_SELFTEST_OUTPUT_OFFSET (768u << 10)
 flp_status flp_selftest_wait_timeout(void* workspace, size_t workspace_bytes, int stall_after,
                                      int64_t wait_limit_ns, void* stream);
 

@@ -158,3 +158,61 @@ def test_loss_argument_checks_need_no_device(lib):
     assert lib.flp_loss(b, b, 4, -100, 2, None, b, None, f(0.2), f(0.2), f(0), b, b, b, None) == flp.FLP_ERR_INVALID_ARG
     assert lib.flp_loss(b, b, 4, -100, 2, b, b, None, f(-0.1), f(0.2), f(0), b, b, b, None) == flp.FLP_ERR_INVALID_ARG
     assert lib.flp_loss(b, b, 4, -100, 1, None, None, None, f(0.2), f(0.2), f(0), b, b, None, None) == flp.FLP_ERR_INVALID_ARG
+
+
+def test_a_caller_of_the_contract_compiles_and_links(tmp_path):
+    """A C program written against include/flp.h, calling the six-argument
+    flp_workspace_query of the boundary contract and its wave-size variant,
+    compiles, links against the library and runs on a machine without a GPU:
+    negative sizes are rejected before any device is touched, and a valid
+    query reports that no sm_103 device can be queried."""
+    from entropy_loss_gb300 import build
+    build.build()
+    src = tmp_path / "caller.c"
+    src.write_text(r'''
+#include <stdio.h>
+#include "flp.h"
+int main(void) {
+    size_t f = 0, b = 0;
+    flp_status a = flp_workspace_query(-1, 64, 10, 1, &f, &b);
+    flp_status c = flp_workspace_query_ex(4, 64, 10, 1, -5, NULL, NULL);
+    flp_status d = flp_workspace_query(4, 64, 10, 0, &f, NULL);
+    printf("%d %d %d\n", (int)a, (int)c, (int)d);
+    return 0;
+}
+''')
+    exe = tmp_path / "caller"
+    libdir = os.path.dirname(build.LIB)
+    subprocess.run(["gcc", "-std=c11", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"),
+                    str(src), "-o", str(exe), f"-L{libdir}", "-l:libflp.so",
+                    f"-Wl,-rpath,{libdir}"], check=True)
+    out = subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split()
+    from entropy_loss_gb300 import flp
+    assert int(out[0]) == flp.FLP_ERR_INVALID_ARG
+    assert int(out[1]) in (flp.FLP_ERR_CUDA, flp.FLP_ERR_UNSUPPORTED, flp.FLP_OK)
+    assert int(out[2]) in (flp.FLP_ERR_CUDA, flp.FLP_ERR_UNSUPPORTED, flp.FLP_OK)
+
+
+def test_policy_loss_argument_checks_need_no_device(lib):
+    from entropy_loss_gb300 import flp
+    import ctypes as C
+    buf = C.create_string_buffer(64)
+    b = (C.addressof(buf) + 15) // 16 * 16
+    f, dd = C.c_float, C.c_double
+
+    def call(**o):
+        a = dict(lp=b, y=b, M=4, off=None, B=0, old=b, adv=b, ref=None, lo=0.2, hi=0.2, beta=0.0,
+                 lvl=0, agg=0, norm=0.0, per=b, grad=b, loss=b)
+        a.update(o)
+        return lib.flp_policy_loss(a["lp"], a["y"], a["M"], -100, a["off"], a["B"], a["old"], a["adv"],
+                                   a["ref"], f(a["lo"]), f(a["hi"]), f(a["beta"]), a["lvl"], a["agg"],
+                                   dd(a["norm"]), a["per"], a["grad"], a["loss"], None)
+    assert call(M=-1) == flp.FLP_ERR_INVALID_ARG
+    assert call(lvl=2) == flp.FLP_ERR_INVALID_ARG
+    assert call(agg=3) == flp.FLP_ERR_INVALID_ARG
+    assert call(old=None) == flp.FLP_ERR_INVALID_ARG
+    assert call(adv=None) == flp.FLP_ERR_INVALID_ARG
+    assert call(loss=None) == flp.FLP_ERR_INVALID_ARG
+    assert call(off=b, B=0) == flp.FLP_ERR_INVALID_ARG
+    assert call(lo=1.5) == flp.FLP_ERR_INVALID_ARG
+    assert call(norm=float("inf")) == flp.FLP_ERR_INVALID_ARG

@@ -441,6 +441,26 @@ def test_bad_target_sets_error_word(flp):
     assert flp.get_error(ws) == flp.FLP_OK
 
 
+def test_workspace_query_forms_agree(flp):
+    """The six-argument query of the boundary contract sizes the default row
+    waves (all M rows up to 8192) exactly as the wave-size variant with
+    chunk_rows <= 0; a wave size changes only the backward bytes."""
+    import ctypes
+    lib = flp.load()
+    for M, H, V, ent in ((4096, 4096, 131072, 1), (20001, 4096, 128257, 1), (300, 64, 999, 0)):
+        a = [ctypes.c_size_t(0) for _ in range(6)]
+        assert lib.flp_workspace_query(M, H, V, ent, ctypes.byref(a[0]), ctypes.byref(a[1])) == flp.FLP_OK
+        assert lib.flp_workspace_query_ex(M, H, V, ent, 0, ctypes.byref(a[2]),
+                                          ctypes.byref(a[3])) == flp.FLP_OK
+        assert lib.flp_workspace_query_ex(M, H, V, ent, 1024, ctypes.byref(a[4]),
+                                          ctypes.byref(a[5])) == flp.FLP_OK
+        assert (a[0].value, a[1].value) == (a[2].value, a[3].value)
+        assert a[4].value == a[0].value
+        Vp = -(-V // 256) * 256
+        assert a[1].value - a[5].value == (min(M + (-M % 128), 8192) - min(1024, M + (-M % 128))) * Vp * 2
+        assert flp.backward_plan(M, H, V, a[1].value, "split")[0] == min(M + (-M % 128), 8192)
+
+
 def test_argument_errors(flp):
     dev = torch.device("cuda")
     d = case(64, 64, 300, seed=13)

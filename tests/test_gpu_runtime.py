@@ -7,6 +7,7 @@ that the wait gives up after its limit with FLP_ERR_TIMEOUT in the error
 word, that the kernel returns on its own, and that the CUDA context keeps
 working afterwards.  Nothing faults, traps or hangs the GPU.
 """
+import math
 import time
 
 import numpy as np
@@ -31,13 +32,27 @@ def flp():
 
 def test_bounded_wait_times_out_and_context_survives(flp):
     limit_ns = 200_000_000  # 0.2 s per wait
-    assert flp.selftest_wait_timeout(-1, limit_ns) == flp.FLP_OK  # same launch, no stall
+    ws = torch.empty(flp.SELFTEST_WORKSPACE_BYTES, dtype=torch.uint8, device="cuda")
+
+    def outputs():
+        o = flp.SELFTEST_OUTPUT_OFFSET
+        return ws[o:o + 3 * 256 * 4].view(torch.float32).view(3, 256).cpu().double()
+
+    assert flp.selftest_wait_timeout(-1, limit_ns, workspace=ws) == flp.FLP_OK  # no stall
+    # all-zero logits over 512 classes: lse = entropy = log 512, logprob = -log 512
+    lp, lse, ent = outputs()
+    assert torch.allclose(lse, torch.full_like(lse, math.log(512)), atol=1e-5)
+    assert torch.allclose(ent, torch.full_like(ent, math.log(512)), atol=1e-5)
+    assert torch.allclose(lp, torch.full_like(lp, -math.log(512)), atol=1e-5)
     t0 = time.perf_counter()
-    st = flp.selftest_wait_timeout(1, limit_ns)
+    st = flp.selftest_wait_timeout(1, limit_ns, workspace=ws)
     elapsed = time.perf_counter() - t0
     assert st == flp.FLP_ERR_TIMEOUT
     assert elapsed < 5.0, f"timed-out kernel took {elapsed:.2f} s to return"
-    assert flp.selftest_wait_timeout(0, limit_ns) == flp.FLP_ERR_TIMEOUT  # stall before any data
+    # the merge saw the timeout bit: no row reports a stale or partial value
+    assert torch.isnan(outputs()).all()
+    assert flp.selftest_wait_timeout(0, limit_ns, workspace=ws) == flp.FLP_ERR_TIMEOUT  # before any data
+    assert torch.isnan(outputs()).all()
     # the context still runs the real path correctly
     d = inputs.make_inputs(inputs.custom("after", 200, 64, 1000, w_std=0.05, seed=41))
     dev = torch.device("cuda")
