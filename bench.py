@@ -39,11 +39,11 @@ PAGES_B300_TP1_FWD_BWD_TFLOPS = 1606.5  # Liger-Kernel native commit, "M=4096 fo
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
-def parse():
+def parse(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=inputs.HEADLINE, choices=sorted(inputs.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -56,7 +56,11 @@ def parse():
                          "persistent launch (fused); auto lets the library pick")
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="target CPU time of the oracle baseline sample")
-    return ap.parse_args()
+    ap.add_argument("--workloads", default="baseline", choices=["baseline", "none"],
+                    help="also time the other synthetic workloads (tiny, temperature 0.7, ragged, "
+                         "large) for a few steps each and report them under 'workloads'")
+    ap.add_argument("--workload-steps", type=int, default=5)
+    return ap.parse_args(argv)
 
 
 # ------------------------------------------------------------------ helpers
@@ -117,6 +121,51 @@ def profiled_traffic(kernel: str, workload: str):
                 and parts[3] == "sources-sha256"):
             return float(parts[2]) if parts[4] == digest else None
     return None
+
+
+def profiled_counters(workload: str):
+    """Per-kernel ncu counters (tensor-pipe activity, DRAM bytes and GB/s)
+    from the committed summary of `workload`, keyed by kernel, or None when
+    there is none or the kernel sources changed since the capture.  A line
+    reads: ncu-counters <kernel> key=value ... sources-sha256 <digest>."""
+    path = os.path.join(ROOT, "profiles", f"counters_{workload}.md")
+    try:
+        with open(path) as f:
+            lines = f.read().splitlines()
+    except OSError:
+        return None
+    digest = kernel_sources_digest()
+    out = {}
+    for ln in lines:
+        parts = ln.split()
+        if len(parts) < 4 or parts[0] != "ncu-counters" or parts[-2] != "sources-sha256":
+            continue
+        if parts[-1] != digest:
+            return None
+        vals = {}
+        for kv in parts[2:-2]:
+            k, _, v = kv.partition("=")
+            try:
+                vals[k] = float(v)
+            except ValueError:
+                vals[k] = v
+        out[parts[1]] = vals
+    return out or None
+
+
+def choose_peak(peaks, timed_s: float, clocks):
+    """The bf16 denominator for a kernel timed inside this run: the burst
+    figure when the timed region is short (under a second) or the sampled SM
+    clock stayed within 5 % of its maximum, else the sustained figure (a
+    seconds-long loop under the power cap)."""
+    burst = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    sustained = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+    sm, smax = (clocks or {}).get("sm_mhz"), (clocks or {}).get("sm_max_mhz")
+    near_max = bool(sm and smax and sm >= 0.95 * smax)
+    if timed_s < 1.0 or near_max:
+        why = "burst: timed region %.2f s%s" % (timed_s, ", SM clock within 5% of max" if near_max else "")
+        return "bf16_tflops", burst, why
+    return "bf16_tflops_sustained", sustained, "sustained: timed region %.2f s at SM clock %s MHz" % (timed_s, sm)
 
 
 def load_peaks():
@@ -189,6 +238,106 @@ class ClockSampler:
 
 # ------------------------------------------------------------- our path
 
+def _device_case(w, dev, chunk_rows, flp):
+    """Seeded inputs of workload `w` copied to the device, its workspace and
+    output buffers."""
+    d = inputs.make_inputs(w)
+    M, H, V = w.M, w.H, w.V
+    ent = d["compute_entropy"]
+    c = dict(d=d, M=M, H=H, V=V, ent=ent)
+    c["X"], c["W"], c["y"] = d["X"].to(dev), d["W"].to(dev), d["y"].to(dev)
+    c["g_lp"] = d["g_lp"].to(dev)
+    c["g_ent"] = d["g_ent"].to(dev) if d["g_ent"] is not None else None
+    c["ws"] = flp.alloc_workspace(M, H, V, ent, chunk_rows=chunk_rows, device=dev)
+    c["lp"] = torch.empty(M, dtype=torch.float32, device=dev)
+    c["lse"] = torch.empty(M, dtype=torch.float32, device=dev)
+    c["en"] = torch.empty(M, dtype=torch.float32, device=dev) if ent else None
+    c["dX"] = torch.empty(M, H, dtype=torch.bfloat16, device=dev)
+    c["dW"] = torch.empty(V, H, dtype=torch.float32, device=dev)
+    return c
+
+
+def _step_fn(c, flp, schedule):
+    d = c["d"]
+    kw = dict(ignore_index=d["ignore_index"], scale=d["scale"], compute_entropy=c["ent"], workspace=c["ws"])
+
+    def step():
+        flp.forward(c["X"], c["W"], c["y"], logprob=c["lp"], lse=c["lse"], entropy=c["en"], **kw)
+        flp.backward(c["X"], c["W"], c["y"], c["lse"], c["en"], c["g_lp"], c["g_ent"], dX=c["dX"],
+                     dW=c["dW"], schedule=schedule, **kw)
+    return step
+
+
+def _phase_names(sched):
+    # phases the library records (events 2k, 2k+1 around phase k); the split
+    # and vsplit schedules record their first wave's / chunk's launches
+    if sched == "fused":
+        return {"fwd": 0, "merge": 1, "bwd": 2}
+    return {"fwd": 0, "merge": 1, "bwd_dz": 2, "bwd_gemm": 3}
+
+
+def _first_launch_share(flp, c, sched, wave_rows):
+    """Rows x vocabulary share (in rows of the full vocabulary) covered by the
+    first wave's (or vocabulary chunk's) two backward launches."""
+    M, H, V = c["M"], c["H"], c["V"]
+    if sched != "vsplit":
+        return float(min(M, wave_rows))
+    units = flp.backward_schedule(M, H, V, c["ws"].numel(), "vsplit", 76)
+    Vt, Mt = -(-V // 256), -(-M // 256)
+    first = units[units[:, 0] == 0, 1]  # the first chunk's dZ launch (kind 4: two 256-column tiles)
+    return M * (int((first == 4).sum() * 2 + (first != 4).sum()) // Mt) / Vt
+
+
+def time_extra_workload(name, args, flp, dev, schedule):
+    """A few timed steps of another workload: per-step CUDA events, an L2 flush
+    between steps when its operands fit in L2, median and mean."""
+    w = inputs.WORKLOADS[name]
+    c = _device_case(w, dev, 0, flp)
+    step = _step_fn(c, flp, schedule)
+    stream = torch.cuda.current_stream(dev)
+    wave_rows, waves, sched = flp.backward_plan(c["M"], c["H"], c["V"], c["ws"].numel(), schedule)
+    operand_bytes = 2 * (c["M"] + c["V"]) * c["H"]
+    flush = operand_bytes < 256 * 2**20
+    scrub = torch.empty(512 * 2**20, dtype=torch.uint8, device=dev) if flush else None
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    if flp.get_error(c["ws"]) != flp.FLP_OK:
+        raise RuntimeError(f"error word set after the warm-up of {name}")
+    names = _phase_names(sched)
+    K = max(1, args.workload_steps)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2 * len(flp.PHASES) + 2)] for _ in range(K)]
+    for row in evs:
+        for e in row:
+            e.record(stream)  # materialise the handles (torch creates them on first record)
+    torch.cuda.synchronize()
+    for k in range(K):
+        if scrub is not None:
+            scrub.zero_()  # evict the operands from L2 (outside the timed events)
+        evs[k][-2].record(stream)
+        flp.set_phase_events(evs[k][:2 * len(flp.PHASES)])
+        step()
+        flp.set_phase_events(None)
+        evs[k][-1].record(stream)
+    torch.cuda.synchronize()
+    if flp.get_error(c["ws"]) != flp.FLP_OK:
+        raise RuntimeError(f"error word set after the timed steps of {name}")
+    per = [evs[k][-2].elapsed_time(evs[k][-1]) for k in range(K)]
+    phase = {n: statistics.median(evs[k][2 * i].elapsed_time(evs[k][2 * i + 1]) for k in range(K))
+             for n, i in names.items()}
+    med = statistics.median(per)
+    out = {"M": c["M"], "H": c["H"], "V": c["V"], "compute_entropy": c["ent"], "scale": c["d"]["scale"],
+           "steps": K, "ms_per_step_median": round(med, 4), "ms_per_step_mean": round(statistics.mean(per), 4),
+           "value": round(8.0 * c["M"] * c["H"] * c["V"] / (med * 1e-3) / 1e12, 1), "unit": UNIT,
+           "phase_ms_median": {k: round(v, 4) for k, v in phase.items()},
+           "bwd_schedule": sched, "wave_rows": wave_rows, "waves": waves,
+           "l2": ("operands fit in L2: 512 MiB written between timed steps" if flush else
+                  "operands larger than L2 (%.2f GiB), no flush" % (operand_bytes / 2**30))}
+    del c, scrub
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_ours(args, world, rank, local):
     from entropy_loss_gb300 import build as libbuild
     from entropy_loss_gb300 import flp
@@ -198,33 +347,14 @@ def run_ours(args, world, rank, local):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     w = inputs.WORKLOADS[args.workload]
-    d = inputs.make_inputs(w)
-    M, H, V = w.M, w.H, w.V
-    ent = d["compute_entropy"]
-    X, W, y = d["X"].to(dev), d["W"].to(dev), d["y"].to(dev)
-    g_lp = d["g_lp"].to(dev)
-    g_ent = d["g_ent"].to(dev) if d["g_ent"] is not None else None
-    ws = flp.alloc_workspace(M, H, V, ent, chunk_rows=args.chunk_rows, device=dev)
-    lp = torch.empty(M, dtype=torch.float32, device=dev)
-    lse = torch.empty(M, dtype=torch.float32, device=dev)
-    en = torch.empty(M, dtype=torch.float32, device=dev) if ent else None
-    dX = torch.empty(M, H, dtype=torch.bfloat16, device=dev)
-    dW = torch.empty(V, H, dtype=torch.float32, device=dev)
+    c = _device_case(w, dev, args.chunk_rows, flp)
+    d, ws = c["d"], c["ws"]
+    M, H, V, ent = c["M"], c["H"], c["V"], c["ent"]
+    X, W = c["X"], c["W"]
     stream = torch.cuda.current_stream(dev)
-    kw = dict(ignore_index=d["ignore_index"], scale=d["scale"], compute_entropy=ent, workspace=ws)
-    bkw = dict(kw, schedule=args.schedule)
     wave_rows, waves, sched = flp.backward_plan(M, H, V, ws.numel(), args.schedule)
-    # phases the library records (events 2k, 2k+1 around phase k)
-    if sched == "fused":
-        phase_names = {"fwd": 0, "merge": 1, "bwd": 2}
-    elif sched == "vsplit":
-        phase_names = {"fwd": 0, "merge": 1, "bwd_dz": 2, "bwd_gemm": 3}  # first vocabulary chunk
-    else:
-        phase_names = {"fwd": 0, "merge": 1, "bwd_dz": 2, "bwd_gemm": 3}
-
-    def step():
-        flp.forward(X, W, y, logprob=lp, lse=lse, entropy=en, **kw)
-        flp.backward(X, W, y, lse, en, g_lp, g_ent, dX=dX, dW=dW, **bkw)
+    phase_names = _phase_names(sched)
+    step = _step_fn(c, flp, args.schedule)
 
     for _ in range(max(args.warmup, 3)):
         step()
@@ -234,7 +364,8 @@ def run_ours(args, world, rank, local):
 
     K = args.steps
     nph = len(flp.PHASES)
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2 * nph)] for _ in range(K)]
+    # per step: the library's phase events, then one event at the step's start
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2 * nph + 1)] for _ in range(K)]
     for row in evs:
         for e in row:
             e.record(stream)  # materialise the handles
@@ -248,7 +379,8 @@ def run_ours(args, world, rank, local):
     torch.cuda.synchronize()
     t_start.record(stream)
     for k in range(K):
-        flp.set_phase_events(evs[k])
+        evs[k][-1].record(stream)
+        flp.set_phase_events(evs[k][:2 * nph])
         step()
     t_stop.record(stream)
     torch.cuda.synchronize()
@@ -258,10 +390,12 @@ def run_ours(args, world, rank, local):
     ms_total = t_start.elapsed_time(t_stop)
     ms_total = max_over_ranks(ms_total, world)
     ms_step = ms_total / K
-    phase_ms = {}
+    per_step = [evs[k][-1].elapsed_time(evs[k + 1][-1] if k + 1 < K else t_stop) for k in range(K)]
+    phase_ms, phase_med = {}, {}
     for name, i in phase_names.items():
         vals = [evs[k][2 * i].elapsed_time(evs[k][2 * i + 1]) for k in range(K)]
         phase_ms[name] = statistics.mean(vals)
+        phase_med[name] = statistics.median(vals)
     if flp.get_error(ws) != flp.FLP_OK:
         raise RuntimeError("error word set after the timed steps")
 
@@ -270,26 +404,24 @@ def run_ours(args, world, rank, local):
 
     # roofline of the dominant kernel launch (largest mean duration among the phases)
     peaks, peak_src = load_peaks()
-    first_wave = min(M, wave_rows)
-    share = first_wave * 1.0  # rows x vocabulary share covered by the first wave's (or chunk's) launches
-    if sched == "vsplit":
-        units = flp.backward_schedule(M, H, V, ws.numel(), "vsplit", 76)
-        Vt, Mt = -(-V // 256), -(-M // 256)
-        first = units[units[:, 0] == 0, 1]  # the first chunk's dZ launch (kind 4: two 256-column tiles)
-        share = M * (int((first == 4).sum() * 2 + (first != 4).sum()) // Mt) / Vt
+    share = _first_launch_share(flp, c, sched, wave_rows)
     phase_flops = {"fwd": 2.0 * M * H * V, "merge": 0.0,
                    "bwd": 6.0 * M * H * V,                       # fused: every wave in one launch
                    "bwd_dz": 2.0 * share * H * V,                # split / vsplit: the first wave's / chunk's launches
                    "bwd_gemm": 4.0 * share * H * V}
     dom = max(phase_ms, key=lambda n: phase_ms[n])
     achieved = phase_flops[dom] / (phase_ms[dom] * 1e-3) / 1e12
-    peak = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+    peak_key, peak, why = choose_peak(peaks, ms_total * 1e-3, clocks)
+    burst = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    sustained = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
     kname = {"fwd": "flp_fwd_kernel", "bwd": "flp_bwd_kernel", "bwd_dz": "flp_dz_kernel",
              "bwd_gemm": "flp_bwd_kernel/dx_dw"}[dom]
     roofline = {"bound": "tensor", "kernel": kname, "achieved": round(achieved, 1),
                 "peak": peak, "unit": UNIT, "frac": round(achieved / peak, 4),
                 "traffic": profiled_traffic(kname, w.name),
-                "peak_source": f"bf16_tflops_sustained of {peak_src}"}
+                "peak_source": f"{peak_key} of {peak_src} ({why})",
+                "frac_burst": round(achieved / burst, 4), "frac_sustained": round(achieved / sustained, 4),
+                "sm_mhz_median": (clocks or {}).get("sm_mhz")}
 
     # our kernels per step: forward, merge, and the backward's launches (from the
     # library's own plan; host arithmetic)
@@ -311,12 +443,17 @@ def run_ours(args, world, rank, local):
                    "wave_rows": wave_rows, "waves": waves, "bwd_schedule": sched,
                    "workspace_bytes": int(ws.numel()),
                    "fwd_bwd_flop_per_step": flops_step},
-        "pct_of_bf16_peak": {"measured_burst": round(value / world / float(peaks.get("bf16_tflops", 1900.0)), 4),
-                             "measured_sustained": round(value / world / peak, 4),
-                             "nominal_2250": round(value / world / 2250.0, 4)},
+        "ms_per_step_median": round(statistics.median(per_step), 4),
+        "value_median": round(world * flops_step / (statistics.median(per_step) * 1e-3) / 1e12, 1),
+        "pct_of_bf16_peak": {"measured_burst": round(value / world / burst, 4),
+                             "measured_sustained": round(value / world / sustained, 4),
+                             "nominal_2250": round(value / world / 2250.0, 4),
+                             "sm_mhz_median": (clocks or {}).get("sm_mhz")},
         "phase_ms": {k: round(v, 4) for k, v in phase_ms.items()},
+        "phase_ms_median": {k: round(v, 4) for k, v in phase_med.items()},
         "fwd_tflops": round(2.0 * M * H * V / ((phase_ms["fwd"] + phase_ms["merge"]) * 1e-3) / 1e12, 1),
         "roofline": roofline,
+        "ncu": profiled_counters(w.name),
         "gpu_launches": launches,
         "clocks": clocks,
     }
@@ -324,6 +461,11 @@ def run_ours(args, world, rank, local):
     if not args.no_e2e:
         result["e2e"] = run_e2e(args, d, X.device, W, ws, world, M, H, V, ent, stream, flp,
                                 args.schedule)
+    del c, X, W, ws
+    torch.cuda.empty_cache()
+    if args.workloads == "baseline" and w.name == inputs.HEADLINE:
+        result["workloads"] = {n: time_extra_workload(n, args, flp, dev, args.schedule)
+                               for n in inputs.BASELINE_OTHERS}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(d, w, args.cpu_seconds)
     if rank == 0:

@@ -35,3 +35,29 @@ def test_reference_arm_prints_its_json_line():
     assert d["impl"] == "reference" and d["value"] > 0 and d["steps"] == 2 and d["warmup"] == 3
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["config"]["workload"] == "tiny"
+
+
+def test_peak_follows_the_timed_region_and_the_clock():
+    peaks = {"bf16_tflops": 1878.3, "bf16_tflops_sustained": 1704.2}
+    key, peak, _ = bench.choose_peak(peaks, 0.3, {"sm_mhz": 1500.0, "sm_max_mhz": 2070.0})
+    assert (key, peak) == ("bf16_tflops", 1878.3)          # short region: burst
+    key, peak, _ = bench.choose_peak(peaks, 5.0, {"sm_mhz": 2040.0, "sm_max_mhz": 2070.0})
+    assert (key, peak) == ("bf16_tflops", 1878.3)          # clock near its maximum: burst
+    key, peak, _ = bench.choose_peak(peaks, 5.0, {"sm_mhz": 1455.0, "sm_max_mhz": 2070.0})
+    assert (key, peak) == ("bf16_tflops_sustained", 1704.2)
+    key, _, _ = bench.choose_peak(peaks, 5.0, None)
+    assert key == "bf16_tflops_sustained"
+
+
+def test_profiled_counters_follow_the_kernel_sources(tmp_path, monkeypatch):
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    (tmp_path / "profiles").mkdir()
+    monkeypatch.setattr(bench, "kernel_sources_digest", lambda: "ab" * 32)
+    (tmp_path / "profiles" / "counters_w.md").write_text(
+        "# text\nncu-counters flp_fwd_kernel tensor_pipe_pct=88.5 dram_gb=1.2 case=q sources-sha256 "
+        + "ab" * 32 + "\n")
+    got = bench.profiled_counters("w")
+    assert got == {"flp_fwd_kernel": {"tensor_pipe_pct": 88.5, "dram_gb": 1.2, "case": "q"}}
+    monkeypatch.setattr(bench, "kernel_sources_digest", lambda: "cd" * 32)
+    assert bench.profiled_counters("w") is None
+    assert bench.profiled_counters("missing") is None
