@@ -425,3 +425,22 @@ def test_backward_dw_cols_equals_the_full_backward_rows(rnd):
     _, dw_b = oracle.backward(oracle.bf16_bits_to_f64(Xb), oracle.bf16_bits_to_f64(Wb), y, g_lp,
                               None, compute_entropy=False)
     np.testing.assert_allclose(got_b, dw_b[cols], rtol=1e-13, atol=1e-15)
+
+
+def test_backward_dw_cols_forward_outputs_equal_the_forward():
+    """The per-row forward outputs the dW-columns entry returns are those of
+    the pinned forward, bit for bit (same definitions, same logit rows)."""
+    M, H, V = 11, 6, 29
+    X, W, y = rand_case(43, M, H, V)
+    y[4] = -100
+    g = rng(44).normal(size=M)
+    for ent in (True, False):
+        _, lp, lse, en = oracle.backward_dw_cols(X, W, y, g, g, [1, 2], scale=1.7,
+                                                 compute_entropy=ent, with_forward=True)
+        f_lp, f_lse, f_en = oracle.forward(X, W, y, scale=1.7, compute_entropy=ent)
+        np.testing.assert_array_equal(lp, f_lp)
+        np.testing.assert_array_equal(lse, f_lse)
+        if ent:
+            np.testing.assert_array_equal(en, f_en)
+        else:
+            assert en is None
