@@ -404,7 +404,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         tma_prefetch_desc(&tmDx);
         tma_prefetch_desc(&tmDw);
     }
+    if (threadIdx.x == 0) griddep_launch_dependents();  // the next launch may be scheduled early
     const uint32_t tmem_base = pair_prologue(sm, warp);
+    griddep_wait();  // the previous launch's results (dZ, the error word) are complete from here on
     const uint64_t limit = p.wait_limit_ns;
     volatile int* abort_flag = sm.abort_flag;
 
@@ -821,7 +823,9 @@ __global__ void __launch_bounds__(WIDE_THREADS, 1)
         tma_prefetch_desc(&tmWk);
         tma_prefetch_desc(&tmDz);
     }
+    if (threadIdx.x == 0) griddep_launch_dependents();  // the next launch may be scheduled early
     const uint32_t tmem_base = pair_prologue(sm, warp);
+    griddep_wait();  // the previous launch's results (dZ, the error word) are complete from here on
     const uint64_t limit = p.wait_limit_ns;
     volatile int* abort_flag = sm.abort_flag;
 

@@ -385,22 +385,28 @@ flp_status check_on_current_device(const void* p, const char* what) {
 }
 
 // Launches `kernel` on `grid` CTAs grouped in clusters of two (the CTA pairs
-// that share each tcgen05.mma.cta_group::2 tile).
+// that share each tcgen05.mma.cta_group::2 tile).  With `after_kernel` the
+// launch follows another of this library's kernels on the stream and uses
+// programmatic dependent launch: its CTAs may be scheduled on the SMs the
+// previous grid frees while that grid's last tiles finish, run their set-up,
+// and wait in griddepcontrol.wait for its results.
 template <typename... KArgs, typename... Args>
 flp_status launch_pairs_n(void (*kernel)(KArgs...), int grid, int threads, cudaStream_t s, const char* what,
-                          Args&&... args) {
+                          bool after_kernel, Args&&... args) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid));
     cfg.blockDim = dim3(static_cast<unsigned>(threads));
     cfg.dynamicSmemBytes = SMEM_ALLOC;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = after_kernel ? 2 : 1;
     cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
     if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, what);
@@ -408,15 +414,15 @@ flp_status launch_pairs_n(void (*kernel)(KArgs...), int grid, int threads, cudaS
 }
 
 template <typename... KArgs, typename... Args>
-flp_status launch_pairs(void (*kernel)(KArgs...), int grid, cudaStream_t s, const char* what,
+flp_status launch_pairs(void (*kernel)(KArgs...), int grid, cudaStream_t s, const char* what, bool after_kernel,
                         Args&&... args) {
-    return launch_pairs_n(kernel, grid, NUM_THREADS, s, what, std::forward<Args>(args)...);
+    return launch_pairs_n(kernel, grid, NUM_THREADS, s, what, after_kernel, std::forward<Args>(args)...);
 }
 
 template <bool kEnt>
 flp_status launch_fwd(int grid, const CUtensorMap& a, const CUtensorMap& b, const FwdParams& p,
                       cudaStream_t s) {
-    return launch_pairs_n(flp_fwd_kernel<kEnt>, grid, WIDE_THREADS, s, "flp_fwd_kernel launch", a, b, p);
+    return launch_pairs_n(flp_fwd_kernel<kEnt>, grid, WIDE_THREADS, s, "flp_fwd_kernel launch", false, a, b, p);
 }
 
 flp_status common_checks(const void* X, const void* W, const int64_t* targets, int64_t M,
@@ -493,9 +499,22 @@ flp_status launch_forward(const void* X, const void* W, const int64_t* targets, 
     mp.entropy = entropy;
     mp.err = err;
     mark(2, s);
-    flp_merge_kernel<<<static_cast<unsigned>(cdiv(M, MERGE_ROWS)), MERGE_ROWS * MERGE_WAYS, 0, s>>>(mp);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return cuda_fail(e, "flp_merge_kernel launch");
+    {
+        // programmatic dependent launch on the tile kernel (unless an event
+        // recorded in between separates them)
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(static_cast<unsigned>(cdiv(M, MERGE_ROWS)));
+        cfg.blockDim = dim3(MERGE_ROWS * MERGE_WAYS);
+        cfg.stream = s;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        cudaError_t e = cudaLaunchKernelEx(&cfg, flp_merge_kernel, mp);
+        if (e == cudaSuccess) e = cudaGetLastError();
+        if (e != cudaSuccess) return cuda_fail(e, "flp_merge_kernel launch");
+    }
     mark(3, s);
     return FLP_OK;
 }
@@ -848,8 +867,10 @@ int launch_kinds(const BwdParams& p) {
     return k;
 }
 
+// after_kernel: the launch directly follows another of this library's kernels
+// on the stream (programmatic dependent launch, see launch_pairs_n).
 flp_status launch_bwd(int pairs, const BwdMaps& m, const BwdParams& p, unsigned long long* ticket_base,
-                      cudaStream_t s) {
+                      cudaStream_t s, bool after_kernel = false) {
     const int np = std::min(p.total, pairs);
     // a ticketed launch draws every unit plus one past the end per CTA pair;
     // a static round-robin draws none
@@ -857,14 +878,14 @@ flp_status launch_bwd(int pairs, const BwdMaps& m, const BwdParams& p, unsigned 
     const char* what = "flp_bwd_kernel launch";
     switch (launch_kinds(p)) {
         case kHasDzWide:
-            return launch_pairs_n(flp_dz_kernel, 2 * np, WIDE_THREADS, s, "flp_dz_kernel launch", m.Xk, m.Wk,
-                                  m.DzSt, p);
+            return launch_pairs_n(flp_dz_kernel, 2 * np, WIDE_THREADS, s, "flp_dz_kernel launch", after_kernel,
+                                  m.Xk, m.Wk, m.DzSt, p);
         case kHasDx | kHasDw:
-            return launch_pairs(flp_bwd_kernel<kHasDx | kHasDw>, 2 * np, s, what, m.Xk, m.Wk, m.Dz, m.Wmn,
-                                m.DzMn, m.Xmn, m.Dx, m.Dw, p);
-        default:
-            return launch_pairs(flp_bwd_kernel<kHasDz | kHasDx | kHasDw>, 2 * np, s, what, m.Xk, m.Wk, m.Dz,
+            return launch_pairs(flp_bwd_kernel<kHasDx | kHasDw>, 2 * np, s, what, after_kernel, m.Xk, m.Wk, m.Dz,
                                 m.Wmn, m.DzMn, m.Xmn, m.Dx, m.Dw, p);
+        default:
+            return launch_pairs(flp_bwd_kernel<kHasDz | kHasDx | kHasDw>, 2 * np, s, what, after_kernel, m.Xk,
+                                m.Wk, m.Dz, m.Wmn, m.DzMn, m.Xmn, m.Dx, m.Dw, p);
     }
 }
 
@@ -987,6 +1008,7 @@ flp_status flp_backward_ex(const void* X, const void* W, const int64_t* targets,
     if (ch.schedule == FLP_BWD_FUSED) FLP_CUDA(cudaMemsetAsync(ws + L.off_cnt, 0, L.cnt_bytes, s));
 
     int64_t mapped_r0 = -1, mapped_rows = -1;
+    bool after_kernel = false;  // the first launch follows the header memset
     for (LaunchSpec& spec : plan) {
         NvtxRange launch_range("flp_backward_launch");
         if (spec.r0 != mapped_r0 || spec.rows != mapped_rows) {
@@ -1018,8 +1040,9 @@ flp_status flp_backward_ex(const void* X, const void* W, const int64_t* targets,
         p.err = base.err;
         p.wait_limit_ns = base.wait_limit_ns;
         if (spec.mark_begin >= 0) mark(spec.mark_begin, s);
-        if ((st = launch_bwd(pairs, m, p, &ticket_base, s)) != FLP_OK) return st;
+        if ((st = launch_bwd(pairs, m, p, &ticket_base, s, after_kernel)) != FLP_OK) return st;
         if (spec.mark_end >= 0) mark(spec.mark_end, s);
+        after_kernel = true;
     }
     if (dx_scratch) {
         const int64_t n = M * H;

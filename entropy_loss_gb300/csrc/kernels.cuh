@@ -413,7 +413,9 @@ __global__ void __launch_bounds__(WIDE_THREADS, 1)
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
     }
+    if (threadIdx.x == 0) griddep_launch_dependents();  // the next launch may be scheduled early
     const uint32_t tmem_base = pair_prologue(sm, warp);
+    griddep_wait();  // the previous launch's results (dZ, the error word) are complete from here on
     const uint64_t limit = p.wait_limit_ns;
     volatile int* abort_flag = sm.abort_flag;
 
@@ -683,6 +685,7 @@ __global__ void __launch_bounds__(MERGE_ROWS * MERGE_WAYS) flp_merge_kernel(cons
     const int lane = threadIdx.x & 31;
     const int w = threadIdx.x >> 5;
     const int i = blockIdx.x * MERGE_ROWS + lane;
+    griddep_wait();  // the forward tile kernel's partials and error word are complete
     if (*reinterpret_cast<volatile const int*>(p.err) & ERR_TIMEOUT) {
         if (w == 0 && i < p.M) {
             const float nan = __int_as_float(0x7fc00000);

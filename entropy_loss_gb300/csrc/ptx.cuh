@@ -17,6 +17,19 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
     return t;
 }
 
+// ---------------------------------------------- programmatic dependent launch
+
+// Lets the grid launched after this one on the stream (with programmatic
+// stream serialization) be scheduled once every CTA of this grid has issued
+// it or exited; its CTAs still wait in griddep_wait for this grid's results.
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Waits until the grids this one depends on have completed and their memory
+// operations are visible (returns at once for a launch without the attribute).
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ------------------------------------------------------------------ mbarrier
 
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
