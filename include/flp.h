@@ -175,12 +175,14 @@ flp_status flp_backward(const void* X, const void* W, const int64_t* targets, in
  *   FLP_BWD_AUTO  : the faster one on GB300: FLP_BWD_SPLIT when its waves
  *                   hold all rows or at least 2048 rows, else FLP_BWD_VSPLIT
  *                   when the workspace allows it (else FLP_BWD_SPLIT).  The
- *                   fused launch ran 0.6-2% slower than the split schedule at
- *                   every shape measured: the chip runs at its power cap, and
- *                   mixing dZ tiles (exp-heavy epilogue) with dX / dW tiles
- *                   lowers the clock while the cycles per tile stay the same.
- * Both schedules compute every output tile with the same instructions in the
- * same order: their results are bit-identical.
+ *                   fused launch keeps 256 x 256 dZ and dW tiles (its
+ *                   dependency counters count 256-column tiles) where the
+ *                   split schedule runs 256 x 512 ones, and measured ~7%
+ *                   slower per headline step; with the same tile shapes in
+ *                   both schedules it was 0.6-2% slower at every shape
+ *                   measured.
+ * The split and fused schedules compute every output tile with the same
+ * instructions in the same order: their results are bit-identical.
  */
 typedef enum { FLP_BWD_AUTO = 0, FLP_BWD_SPLIT = 1, FLP_BWD_FUSED = 2, FLP_BWD_VSPLIT = 3 } flp_bwd_schedule;
 
