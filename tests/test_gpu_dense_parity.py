@@ -19,6 +19,8 @@ Per tensor: relative L2 within 1e-2, cosine > 0.999 and norm ratio within 2%
 L2 within 1e-2 as well, so one broken tile cannot hide in a global norm.
 Ignored rows of dX are exactly zero.
 """
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -156,6 +158,69 @@ def test_dense_backward_every_element_ragged_m777_h4096_v50257(flp):
     assert rep["split, two waves"][0][:2] == (512, 2)
 
 
+def _sampled_dense(flp, w, schedules, n_rows=256, n_cols=256, seed=1014):
+    """Every row live at the workload's full size: the forward on all rows,
+    dX on a row sample (first, last and tile-boundary rows included), dW on a
+    vocabulary sample plus the 256-column tile boundaries at both ends, every
+    row-wave boundary's neighbourhood and every vocabulary-split chunk
+    boundary, each dW row summed over all M rows; for each (label, chunk_rows,
+    schedule)."""
+    dev = torch.device("cuda")
+    d = inputs.make_inputs(w)
+    X, W, y, g1, g2 = _device_inputs(d, dev)
+    ent = d["compute_entropy"]
+    Xb, Wb, yn = inputs.bf16_bits(d["X"]), inputs.bf16_bits(d["W"]), d["y"].numpy()
+    M, H, V = w.M, w.H, w.V
+    wss = {label: flp.alloc_workspace(M, H, V, ent, chunk_rows=cr, device=dev)
+           for label, cr, _ in schedules}
+    bounds = {0, V - 1}
+    for label, _, sched in schedules:
+        if flp.backward_plan(M, H, V, wss[label].numel(), sched)[2] != "vsplit":
+            continue
+        units = flp.backward_schedule(M, H, V, wss[label].numel(), "vsplit", 76)
+        for li in range(0, int(units[:, 0].max()) + 1, 2):
+            t = int(units[(units[:, 0] == li) & np.isin(units[:, 1], (0, 4)), 4].min())
+            bounds |= {t * 256 - 1, t * 256, t * 256 + 255}
+    for t in (1, (V - 1) // 256):
+        bounds |= {t * 256 - 1, t * 256, t * 256 + 255}
+    g = np.random.default_rng(seed)
+    cols = np.unique(np.concatenate([g.choice(V, n_cols, replace=False),
+                                     np.array(sorted(c for c in bounds if 0 <= c < V))]))
+    rows = inputs.sample_rows(M, n_rows, seed=seed + 1).numpy()
+    wave_edges = [r for k in range(8192, M, 8192) for r in (k - 1, k)]  # default row-wave boundaries
+    rows = np.unique(np.concatenate([rows, np.array(wave_edges, dtype=rows.dtype)]))
+    g_lp = d["g_lp"].double().numpy()
+    g_ent = d["g_ent"].double().numpy() if ent else None
+    o_dw, o_lp, o_lse, o_en = oracle.backward_dw_cols(
+        Xb, Wb, yn, g_lp, g_ent, cols, ignore_index=d["ignore_index"], scale=d["scale"],
+        compute_entropy=ent, with_forward=True)
+    o_dx, _ = oracle.backward(Xb, Wb, yn, g_lp, g_ent, ignore_index=d["ignore_index"],
+                              scale=d["scale"], compute_entropy=ent, rows=rows, want_dw=False)
+    want_dw = torch.from_numpy(o_dw).to(dev)
+    want_dx = torch.from_numpy(o_dx).to(dev)
+    ridx = torch.as_tensor(rows, device=dev)
+    cidx = torch.as_tensor(cols, device=dev)
+    ignored = np.flatnonzero(yn[rows] == d["ignore_index"])
+    first = schedules[0][0]
+    lp, lse, en = flp.forward(X, W, y, ignore_index=d["ignore_index"], scale=d["scale"],
+                              compute_entropy=ent, workspace=wss[first])
+    torch.cuda.synchronize()
+    assert flp.get_error(wss[first]) == flp.FLP_OK
+    check_fwd(lp, o_lp, "logprob (all rows)")
+    check_fwd(lse, o_lse, "lse (all rows)")
+    if ent:
+        check_fwd(en, o_en, "entropy (all rows)")
+    for label, _, sched in schedules:
+        plan = flp.backward_plan(M, H, V, wss[label].numel(), sched)
+        dX, dW = _run_backward(flp, X, W, y, lse, en, g1, g2, d, wss[label], sched)
+        rx = check_dense(dX[ridx], want_dx, f"{label} dX rows", zero_rows=ignored)
+        rw = check_dense(dW[cidx], want_dw, f"{label} dW vocabulary rows")
+        print(f"{w.name} {label}: plan {plan}; dX rows rel L2 {rx[0]:.2e} (worst {rx[1]:.2e}); dW "
+              f"vocabulary rows rel L2 {rw[0]:.2e} (worst {rw[1]:.2e}); {len(rows)} rows, "
+              f"{len(cols)} vocabulary rows")
+        del dX, dW
+
+
 def test_dense_backward_headline_sampled(flp):
     """The headline workload (M = 4096, H = 4096, V = 131072, every row live,
     5% ignored) in the bench's launch configuration, and with the fused and
@@ -164,53 +229,29 @@ def test_dense_backward_headline_sampled(flp):
     sampled vocabulary rows plus every 256-column tile boundary row around
     the ends and the boundaries of the vocabulary-split chunks, each dW row a
     sum over all 4096 rows."""
-    dev = torch.device("cuda")
-    w = inputs.WORKLOADS["m4096_h4096_v131072"]
-    d = inputs.make_inputs(w)
-    X, W, y, g1, g2 = _device_inputs(d, dev)
-    Xb, Wb, yn = inputs.bf16_bits(d["X"]), inputs.bf16_bits(d["W"]), d["y"].numpy()
-    M, H, V = w.M, w.H, w.V
-    ws = flp.alloc_workspace(M, H, V, True, device=dev)
-    small = flp.alloc_workspace(M, H, V, True, chunk_rows=1024, device=dev)
-    vrows, vchunks, vs = flp.backward_plan(M, H, V, small.numel(), "vsplit")
-    assert vs == "vsplit" and vchunks > 1
-    units = flp.backward_schedule(M, H, V, small.numel(), "vsplit", 76)
-    # first vocabulary tile of each vsplit chunk (dZ tiles of the chunk's first launch)
-    chunk_first = sorted({int(units[(units[:, 0] == li) & np.isin(units[:, 1], (0, 4)), 4].min())
-                          for li in range(0, int(units[:, 0].max()) + 1, 2)})
-    bounds = set()
-    for t in chunk_first + [1, V // 256 - 1]:
-        for c in (t * 256 - 1, t * 256, t * 256 + 255):
-            if 0 <= c < V:
-                bounds.add(c)
-    g = np.random.default_rng(1014)
-    cols = np.unique(np.concatenate([g.choice(V, 256, replace=False),
-                                     np.array(sorted(bounds | {0, V - 1}))]))
-    rows = inputs.sample_rows(M, 256, seed=1015).numpy()
+    _sampled_dense(flp, inputs.WORKLOADS["m4096_h4096_v131072"],
+                   [("split (the bench's)", 0, "auto"), ("fused", 0, "fused"),
+                    ("vocabulary split", 1024, "vsplit")])
 
-    o_dw, o_lp, o_lse, o_en = oracle.backward_dw_cols(
-        Xb, Wb, yn, d["g_lp"].double().numpy(), d["g_ent"].double().numpy(), cols,
-        ignore_index=d["ignore_index"], scale=d["scale"], with_forward=True)
-    o_dx, _ = oracle.backward(Xb, Wb, yn, d["g_lp"].double().numpy(), d["g_ent"].double().numpy(),
-                              ignore_index=d["ignore_index"], scale=d["scale"], rows=rows,
-                              want_dw=False)
-    want_dw = torch.from_numpy(o_dw).to(dev)
-    want_dx = torch.from_numpy(o_dx).to(dev)
-    ridx = torch.as_tensor(rows, device=dev)
-    cidx = torch.as_tensor(cols, device=dev)
-    ignored = np.flatnonzero(yn[rows] == d["ignore_index"])
 
-    lp, lse, en = flp.forward(X, W, y, workspace=ws)
-    torch.cuda.synchronize()
-    assert flp.get_error(ws) == flp.FLP_OK
-    check_fwd(lp, o_lp, "logprob (all rows)")
-    check_fwd(lse, o_lse, "lse (all rows)")
-    check_fwd(en, o_en, "entropy (all rows)")
-    for label, wsp, sched in (("split (the bench's)", ws, "auto"), ("fused", ws, "fused"),
-                              ("vocabulary split", small, "vsplit")):
-        dX, dW = _run_backward(flp, X, W, y, lse, en, g1, g2, d, wsp, sched)
-        rx = check_dense(dX[ridx], want_dx, f"{label} dX rows", zero_rows=ignored)
-        rw = check_dense(dW[cidx], want_dw, f"{label} dW vocabulary rows")
-        print(f"headline {label}: dX rows rel L2 {rx[0]:.2e} (worst {rx[1]:.2e}); dW vocabulary rows "
-              f"rel L2 {rw[0]:.2e} (worst {rw[1]:.2e}); {len(rows)} rows, {len(cols)} vocabulary rows")
-        del dX, dW
+@pytest.mark.skipif(not os.environ.get("FLP_SLOW_PARITY"),
+                    reason="the oracle's forward of every row takes 5-16 min here: set FLP_SLOW_PARITY=1")
+@pytest.mark.parametrize("name", ["ragged_m20001_h4096_v128257", "m8192_h8192_v131072",
+                                  "large_m32768_h5120_v152064"])
+def test_dense_backward_large_workloads_sampled(flp, name):
+    """The three largest workloads at full size in the bench's launch
+    configuration (row waves of 8192: three for the ragged one, four for the
+    large one; dW added across waves in fp32) with every row live: the
+    forward on all rows, dX on ~256 rows, dW on ~270 vocabulary rows, each a
+    sum over all rows (including the ragged vocabulary's tail tile)."""
+    _sampled_dense(flp, inputs.WORKLOADS[name], [("split (the bench's)", 0, "auto")])
+
+
+@pytest.mark.skipif(not os.environ.get("FLP_SLOW_PARITY"),
+                    reason="the oracle's full backward at the headline shape takes ~6 min here: set FLP_SLOW_PARITY=1")
+def test_dense_backward_every_element_headline(flp):
+    """The headline workload exactly as the bench times it (M = 4096, H = 4096,
+    V = 131072, every row live, one wave, the split schedule): every element
+    of dX and dW against the oracle's full fp64 backward."""
+    _full_dense(flp, inputs.WORKLOADS["m4096_h4096_v131072"],
+                [("split (the bench's)", 0, "auto", torch.bfloat16, torch.float32)])
