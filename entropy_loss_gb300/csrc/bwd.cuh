@@ -345,6 +345,33 @@ __device__ __forceinline__ void gemm_tile_epilogue(StoreRing& ring, uint8_t* sme
     }
 }
 
+// The same through one group's two narrow boxes: 32 bf16 columns per box, or
+// 16 fp32 columns per box (two boxes per TMEM load of 32 columns).
+__device__ __forceinline__ void gemm_tile_epilogue_narrow(StoreRing& ring, uint8_t* box0, uint32_t bar_id,
+                                                          int et, int r, uint32_t tbase, bool bf16_out,
+                                                          bool add, const CUtensorMap* out, int col0, int row0,
+                                                          uint32_t tempty) {
+#pragma unroll 1
+    for (int b = 0; b < BN / 32; ++b) {
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(tbase + b * 32, v);
+        tmem_wait_ld();
+        if (b == BN / 32 - 1) {
+            tc_fence_before();
+            mbar_arrive_cluster(tempty);
+        }
+        if (bf16_out) {
+            uint32_t w[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) w[j] = pack_bf16x2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
+            narrow_box_store(ring, box0, bar_id, et, r, w, out, col0 + b * 32, row0, false);
+        } else {
+            narrow_box_store(ring, box0, bar_id, et, r, v, out, col0 + b * 32, row0, add);
+            narrow_box_store(ring, box0, bar_id, et, r, v + 16, out, col0 + b * 32 + 16, row0, add);
+        }
+    }
+}
+
 // The kernel is instantiated per set of tile kinds a launch holds, so a
 // launch of dZ tiles alone (or of dX and dW tiles alone) carries no code for
 // the others.
@@ -372,16 +399,24 @@ __device__ __forceinline__ int unit_kblocks(const BwdParams& p, const UnitClass&
 
 // ------------------------------------------------------------------ kernel
 
+// A launch of dX and dW tiles alone (the split and vocabulary-split
+// schedules) runs two epilogue groups of four warps (320 threads): group g
+// drains every use of accumulator g, so the two halves of a wide tile drain in
+// parallel, each through the group's own narrow boxes.  The fused launch keeps
+// one group of four warps (192 threads) and 128-byte boxes.
 template <int kKinds>
-__global__ void __launch_bounds__(NUM_THREADS, 1)
+__host__ __device__ constexpr bool two_groups() { return kKinds == (kHasDx | kHasDw); }
+
+template <int kKinds>
+__global__ void __launch_bounds__(WIDE_THREADS, 1)
     flp_bwd_kernel(const __grid_constant__ CUtensorMap tmXk,    // X, K-major A of dZ tiles (64 x 128 boxes)
                    const __grid_constant__ CUtensorMap tmWk,    // W, K-major B of dZ tiles (64 x 128)
                    const __grid_constant__ CUtensorMap tmDz,    // dZ buffer: dZ store boxes and K-major A of dX (64 x 128)
                    const __grid_constant__ CUtensorMap tmWmn,   // W, MN-major B of dX (64 x 64)
                    const __grid_constant__ CUtensorMap tmDzMn,  // dZ buffer, MN-major A of dW (64 x 64)
                    const __grid_constant__ CUtensorMap tmXmn,   // X, MN-major B of dW (64 x 64)
-                   const __grid_constant__ CUtensorMap tmDx,    // dX store boxes
-                   const __grid_constant__ CUtensorMap tmDw,    // dW store / add boxes
+                   const __grid_constant__ CUtensorMap tmDx,    // dX store boxes (narrow with two groups)
+                   const __grid_constant__ CUtensorMap tmDw,    // dW store / add boxes (narrow with two groups)
                    const __grid_constant__ BwdParams p) {
     extern __shared__ uint8_t smem_raw[];
     const Smem sm = smem_layout(smem_raw);
@@ -405,7 +440,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         tma_prefetch_desc(&tmDw);
     }
     if (threadIdx.x == 0) griddep_launch_dependents();  // the next launch may be scheduled early
-    const uint32_t tmem_base = pair_prologue(sm, warp);
+    constexpr bool kTwo = two_groups<kKinds>();
+    const uint32_t tmem_base = pair_prologue(sm, warp, 2 + (kTwo ? 4 : 2) * EPI_THREADS);
     griddep_wait();  // the previous launch's results (dZ, the error word) are complete from here on
     const uint64_t limit = p.wait_limit_ns;
     volatile int* abort_flag = sm.abort_flag;
@@ -685,12 +721,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
     } else {
         // --------------------------------------------------------- epilogue
-        const int et = threadIdx.x - 64;  // 0..127; thread 0 issues the bulk stores
+        const int g = kTwo ? (warp - 2) >> 2 : 0;  // epilogue group (drains accumulator g when kTwo)
+        const int et = threadIdx.x - 64 - g * EPI_THREADS;  // 0..127; thread 0 issues the bulk stores
         const int q = warp & 3;           // TMEM lane quadrant of this warp
         const int r = q * 32 + lane;      // accumulator row == TMEM lane
         const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
         const uint32_t tempty_leader0 = mapa_shared(smem_addr(&sm.tempty[0]), 0);
         const uint32_t tempty_leader1 = mapa_shared(smem_addr(&sm.tempty[1]), 0);
+        const uint32_t bar_box = kTwo ? 1 + 2 * g : 1, bar_vote = kTwo ? 2 + 2 * g : 2;
+        uint8_t* nbox0 = smem + SMEM_STG + g * (2 * NBOX_BYTES);  // this group's narrow boxes
         int acc = 0;        // next accumulator (a wide dX tile drains acc, then acc ^ 1)
         uint32_t tpar = 0;  // bit a: parity of the uses of accumulator a so far
         bool ok = true;
@@ -741,12 +780,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 nacc = c.wide ? 2 : 1;
                 for (int h = 0; h < nacc && ready; ++h) {
                     const int a = acc ^ h;
+                    if (kTwo && a != g) continue;  // the other group drains it
                     ready = mbar_wait(&sm.tfull[a], (tpar >> a) & 1u, limit, abort_flag);
                 }
             }
-            // every epilogue thread takes the same branch (the store barriers
-            // below need all of them)
-            if (!named_bar_all(2, EPI_THREADS, ready)) {
+            // every epilogue thread of the group takes the same branch (the
+            // store barriers below need all of them)
+            if (!named_bar_all(bar_vote, EPI_THREADS, ready)) {
                 ok = false;
                 break;
             }
@@ -756,7 +796,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 const int a = acc ^ h;
                 const uint32_t tbase = tmem_base + static_cast<uint32_t>(a * BN) + lane_off;
                 const uint32_t tempty = a ? tempty_leader1 : tempty_leader0;
-                if (c.dz) {
+                if constexpr (kTwo) {
+                    if (a == g) {
+                        if (c.dx)
+                            gemm_tile_epilogue_narrow(ring, nbox0, bar_box, et, r, tbase, !p.dx_f32,
+                                                      p.dx_add != 0, &tmDx, (t.nt * nacc + h) * BN,
+                                                      wi.r0 + t.mt * PM + rofs, tempty);
+                        else
+                            gemm_tile_epilogue_narrow(ring, nbox0, bar_box, et, r, tbase, p.dw_bf16 != 0,
+                                                      t.wave > 0 || p.dw_add0, &tmDw, (t.nt * nacc + h) * BN,
+                                                      t.mt * PM + rofs, tempty);
+                    }
+                } else if (c.dz) {
                     dz_tile_epilogue(ring, smem, et, r, tbase, t.nt * BN, (t.nt - p.vt0) * BN, p.V,
                                      p.scale2, d, &tmDz, t.mt * PM + rofs, tempty);
                 } else if (c.dx) {

@@ -869,8 +869,10 @@ int launch_kinds(const BwdParams& p) {
 
 // after_kernel: the launch directly follows another of this library's kernels
 // on the stream (programmatic dependent launch, see launch_pairs_n).
+// narrow: the dX / dW store maps have narrow (64-byte) boxes, which only the
+// two-group dX + dW instantiation writes.
 flp_status launch_bwd(int pairs, const BwdMaps& m, const BwdParams& p, unsigned long long* ticket_base,
-                      cudaStream_t s, bool after_kernel = false) {
+                      cudaStream_t s, bool after_kernel = false, bool narrow = false) {
     const int np = std::min(p.total, pairs);
     // a ticketed launch draws every unit plus one past the end per CTA pair;
     // a static round-robin draws none
@@ -881,9 +883,11 @@ flp_status launch_bwd(int pairs, const BwdMaps& m, const BwdParams& p, unsigned 
             return launch_pairs_n(flp_dz_kernel, 2 * np, WIDE_THREADS, s, "flp_dz_kernel launch", after_kernel,
                                   m.Xk, m.Wk, m.DzSt, p);
         case kHasDx | kHasDw:
-            return launch_pairs(flp_bwd_kernel<kHasDx | kHasDw>, 2 * np, s, what, after_kernel, m.Xk, m.Wk, m.Dz,
-                                m.Wmn, m.DzMn, m.Xmn, m.Dx, m.Dw, p);
+            if (!narrow) return fail(FLP_ERR_UNSUPPORTED, "dX + dW launch without narrow store maps");
+            return launch_pairs_n(flp_bwd_kernel<kHasDx | kHasDw>, 2 * np, WIDE_THREADS, s, what, after_kernel,
+                                  m.Xk, m.Wk, m.Dz, m.Wmn, m.DzMn, m.Xmn, m.Dx, m.Dw, p);
         default:
+            if (narrow) return fail(FLP_ERR_UNSUPPORTED, "backward launch of this kind with narrow store maps");
             return launch_pairs(flp_bwd_kernel<kHasDz | kHasDx | kHasDw>, 2 * np, s, what, after_kernel, m.Xk,
                                 m.Wk, m.Dz, m.Wmn, m.DzMn, m.Xmn, m.Dx, m.Dw, p);
     }
@@ -954,12 +958,17 @@ flp_status flp_backward_ex(const void* X, const void* W, const int64_t* targets,
     float* scr = dx_scratch ? reinterpret_cast<float*>(ws + ch.off_scr) : nullptr;
 
     BwdMaps m{};
+    // the split and vocabulary-split schedules' dX + dW launches store through
+    // narrow boxes (two epilogue groups); the fused launch through 128-byte ones
+    const bool narrow = ch.schedule != FLP_BWD_FUSED;
+    const CUtensorMapSwizzle out_swz = narrow ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B;
+    const uint32_t box_bf16 = narrow ? 32 : 64, box_f32 = narrow ? 16 : 32;  // columns per store box
     if ((st = tmap_2d(&m.Wk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, W, H, V, H * 2, BK, BNH)) != FLP_OK) return st;
     if ((st = tmap_2d(&m.Wmn, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, W, H, V, H * 2, 64, 64)) != FLP_OK) return st;
     if (dW_dtype == FLP_BF16)
-        st = tmap_2d(&m.Dw, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dW, H, V, H * 2, 64, BM);
+        st = tmap_2d(&m.Dw, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dW, H, V, H * 2, box_bf16, BM, out_swz);
     else
-        st = tmap_2d(&m.Dw, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, dW, H, V, H * 4, 32, BM);
+        st = tmap_2d(&m.Dw, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, dW, H, V, H * 4, box_f32, BM, out_swz);
     if (st != FLP_OK) return st;
 
     // Row tensor maps (X, dX, dZ buffer) over `rows` rows starting at global
@@ -977,11 +986,12 @@ flp_status flp_backward_ex(const void* X, const void* W, const int64_t* targets,
                          CU_TENSOR_MAP_SWIZZLE_64B)) != FLP_OK)
             return e;
         if (dx_scratch)
-            return tmap_2d(&m.Dx, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, scr + r0 * H, H, rows, H * 4, 32, BM);
+            return tmap_2d(&m.Dx, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, scr + r0 * H, H, rows, H * 4, box_f32, BM,
+                           out_swz);
         uint8_t* dXc = static_cast<uint8_t*>(dX) + r0 * H * dx_es;
         if (dX_dtype == FLP_F32)
-            return tmap_2d(&m.Dx, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, dXc, H, rows, H * 4, 32, BM);
-        return tmap_2d(&m.Dx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dXc, H, rows, H * 2, 64, BM);
+            return tmap_2d(&m.Dx, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, dXc, H, rows, H * 4, box_f32, BM, out_swz);
+        return tmap_2d(&m.Dx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dXc, H, rows, H * 2, box_bf16, BM, out_swz);
     };
 
     std::vector<LaunchSpec> plan;
@@ -1040,7 +1050,7 @@ flp_status flp_backward_ex(const void* X, const void* W, const int64_t* targets,
         p.err = base.err;
         p.wait_limit_ns = base.wait_limit_ns;
         if (spec.mark_begin >= 0) mark(spec.mark_begin, s);
-        if ((st = launch_bwd(pairs, m, p, &ticket_base, s, after_kernel)) != FLP_OK) return st;
+        if ((st = launch_bwd(pairs, m, p, &ticket_base, s, after_kernel, narrow)) != FLP_OK) return st;
         if (spec.mark_end >= 0) mark(spec.mark_end, s);
         after_kernel = true;
     }

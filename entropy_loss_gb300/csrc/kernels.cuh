@@ -143,7 +143,10 @@ __device__ __forceinline__ void raise_abort(const Smem& sm, int* err) {
 
 // Barrier set-up, TMEM allocation on both CTAs, and the cluster handshake that
 // makes the peer's barriers visible before any remote arrive or TMA signal.
-__device__ __forceinline__ uint32_t pair_prologue(const Smem& sm, int warp) {
+// sched_arrivals: arrivals that free a slot of the unit hand-off ring (the
+// peer's producer, the MMA issuer and every epilogue thread of both CTAs).
+__device__ __forceinline__ uint32_t pair_prologue(const Smem& sm, int warp,
+                                                  uint32_t sched_arrivals = 2 + 2 * EPI_THREADS) {
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&sm.full[s], 1);
@@ -156,7 +159,7 @@ __device__ __forceinline__ uint32_t pair_prologue(const Smem& sm, int warp) {
         mbar_init(sm.drain, 1);
         for (int s = 0; s < SCHED_SLOTS; ++s) {
             mbar_init(&sm.sched_full[s], 1);
-            mbar_init(&sm.sched_empty[s], 2 + 2 * EPI_THREADS);
+            mbar_init(&sm.sched_empty[s], sched_arrivals);
         }
         *sm.abort_flag = 0;
         fence_mbarrier_init();
@@ -250,6 +253,40 @@ __device__ __forceinline__ void store_box_release(StoreRing& ring, uint8_t* smem
             tma_reduce_add_2d(tmOut, src, x, y);
         else
             tma_store_2d(tmOut, src, x, y);
+        bulk_commit_group();
+    }
+    ring.n++;
+}
+
+// Narrow store boxes: 128 rows x 64 bytes (32 bf16 or 16 fp32 columns,
+// 64-byte swizzle), two per epilogue group, so that two groups fit the store
+// region.  One box of this thread's row (16 words) is staged and stored (or
+// added) in its group's ring; before a box is rewritten, the bulk store that
+// last read it must have finished reading (thread 0 of the group waits, the
+// group's named barrier hands that on).
+constexpr uint32_t NBOX_BYTES = BM * 64;
+static_assert(2 * 2 * NBOX_BYTES <= NUM_STG * STG_BYTES, "two narrow boxes per epilogue group");
+
+__device__ __forceinline__ void narrow_box_store(StoreRing& ring, uint8_t* box0, uint32_t bar_id, int et, int r,
+                                                 const uint32_t* w, const CUtensorMap* out, int x, int y,
+                                                 bool add) {
+    const uint32_t buf = ring.n & 1u;
+    if (ring.n >= 2) {
+        if (et == 0) bulk_wait_group_read<1>();
+        named_bar_sync(bar_id, EPI_THREADS);
+    }
+    uint8_t* box = box0 + buf * NBOX_BYTES;
+    const uint32_t row_addr = smem_addr(box) + r * 64;
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+        st_shared_v4(row_addr + ((c ^ ((r >> 1) & 3)) << 4), w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+    fence_proxy_async_smem();
+    named_bar_sync(bar_id, EPI_THREADS);
+    if (et == 0) {
+        if (add)
+            tma_reduce_add_2d(out, box, x, y);
+        else
+            tma_store_2d(out, box, x, y);
         bulk_commit_group();
     }
     ring.n++;
