@@ -94,14 +94,41 @@ def max_over_ranks(x: float, world: int) -> float:
     return float(t.item())
 
 
+def strip_comments(src: str) -> str:
+    """C/C++ source without its comments, trailing blanks and empty lines
+    (string and character literals are kept as they are)."""
+    out, i, n = [], 0, len(src)
+    while i < n:
+        c = src[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and src[j] != c:
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        elif src.startswith("//", i):
+            j = src.find("\n", i)
+            i = n if j < 0 else j
+        elif src.startswith("/*", i):
+            j = src.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        else:
+            out.append(c)
+            i += 1
+    lines = (ln.rstrip() for ln in "".join(out).splitlines())
+    return "\n".join(ln for ln in lines if ln)
+
+
 def kernel_sources_digest() -> str:
-    """sha256 over the CUDA sources' names and contents (sorted by name)."""
+    """sha256 over the CUDA sources' names and code (sorted by name), comments
+    left out: a profile stays valid while only the comments change."""
     import glob
     import hashlib
     h = hashlib.sha256()
     for f in sorted(glob.glob(os.path.join(ROOT, "entropy_loss_gb300", "csrc", "*"))):
-        with open(f, "rb") as fh:
-            h.update(os.path.basename(f).encode() + b"\0" + fh.read() + b"\0")
+        with open(f, encoding="utf-8") as fh:
+            code = strip_comments(fh.read())
+        h.update(os.path.basename(f).encode() + b"\0" + code.encode() + b"\0")
     return h.hexdigest()
 
 

@@ -28,13 +28,13 @@
 // accumulator on the leader's `tempty` barrier.  Two 256-column accumulators
 // (512 TMEM columns) let a tile's epilogue overlap the next tile's MMAs.
 //
-// The forward runs wide tiles instead: 256 rows x 512 columns, one per pair,
-// both accumulators (half h of the columns in accumulator h), so each SM loads
-// 16 KiB of A and 32 KiB of B per K step for twice the MACs (25 % fewer
-// operand bytes per MAC).  It has two epilogue groups of four warps (warps
-// 2..5 drain half 0, warps 6..9 half 1; 320 threads), and the MMA issuer
-// staggers the halves at both ends of a tile so that one half's epilogue runs
-// under the other half's MMAs.
+// The forward, the dZ kernel and the backward's dX + dW launch run wide tiles
+// instead: 256 rows x 512 columns, one per pair, both accumulators (half h of
+// the columns in accumulator h), so each SM loads 16 KiB of A and 32 KiB of B
+// per K step for twice the MACs (25 % fewer operand bytes per MAC).  They have
+// two epilogue groups of four warps (warps 2..5 drain half 0, warps 6..9 half
+// 1; 320 threads), and the MMA issuer staggers the halves at both ends of a
+// tile so that one half's epilogue runs under the other half's MMAs.
 //
 // Every mbarrier wait is bounded (globaltimer); on expiry the kernel raises the
 // timeout bit in the error word, stops issuing work, lets its copies and MMAs
@@ -55,7 +55,7 @@ constexpr int UMMA_K = 16;        // K per tcgen05.mma (bf16)
 constexpr int STAGES = 6;
 constexpr int NUM_THREADS = 192;
 constexpr int EPI_THREADS = 128;
-constexpr int WIDE_THREADS = 64 + 2 * EPI_THREADS;  // wide-tile kernels (forward, dZ): two epilogue groups of four warps
+constexpr int WIDE_THREADS = 64 + 2 * EPI_THREADS;  // wide-tile kernels (forward, dZ, dX + dW): two epilogue groups of four warps
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint16_t PAIR_MASK = 0x3;
 

@@ -61,3 +61,28 @@ def test_profiled_counters_follow_the_kernel_sources(tmp_path, monkeypatch):
     monkeypatch.setattr(bench, "kernel_sources_digest", lambda: "cd" * 32)
     assert bench.profiled_counters("w") is None
     assert bench.profiled_counters("missing") is None
+
+
+def test_strip_comments_keeps_code_and_literals():
+    src = ('int a = 1; // tail\n'
+           '/* block\n   over lines */ int b = 2;\n'
+           'const char* s = "not // a comment /* nor this */";\n'
+           "char c = '/'; char d = '\\''; /**/ int e;\n"
+           '   \n')
+    assert bench.strip_comments(src) == (
+        'int a = 1;\n'
+        ' int b = 2;\n'
+        'const char* s = "not // a comment /* nor this */";\n'
+        "char c = '/'; char d = '\\'';  int e;")
+
+
+def test_kernel_sources_digest_ignores_comments_only(tmp_path, monkeypatch):
+    csrc = tmp_path / "entropy_loss_gb300" / "csrc"
+    csrc.mkdir(parents=True)
+    (csrc / "k.cuh").write_text("// header\nint f() { return 1; }  // one\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    d0 = bench.kernel_sources_digest()
+    (csrc / "k.cuh").write_text("/* another header */\n\nint f() { return 1; }\n")
+    assert bench.kernel_sources_digest() == d0
+    (csrc / "k.cuh").write_text("int f() { return 2; }\n")
+    assert bench.kernel_sources_digest() != d0
