@@ -159,6 +159,8 @@ def test_waves_and_ragged_tail(flp, schedule):
     (257, 136, 513, 256),    # two waves, the second a single row
     (2600, 72, 5000, 1024),  # fused: dZ tiles of a wave wait on the previous wave's dX / dW tiles
     (1300, 512, 16500, 512), # wide (256 x 512) dX tiles in three waves
+    (900, 640, 3001, 512),   # three 256-column tiles of H (the last half-filled): 256 x 256 dX and
+                             # dW tiles, several per row tile, alternating accumulators, two waves
 ])
 def test_schedules_match_oracle(flp, schedule, M, H, V, chunk):
     run_case(flp, case(M, H, V, seed=22), chunk_rows=chunk, schedule=schedule)
@@ -174,6 +176,8 @@ def test_schedules_match_oracle(flp, schedule, M, H, V, chunk):
     (1300, 512, 16500, 512, True, True, False, True),   # wide dX tiles, three waves, slot layouts switching
     (1200, 264, 16500, 0, True, False, False, False),   # wide dX tiles whose second half is mostly beyond H
     (1000, 1024, 3000, 512, False, False, False, False),
+    (900, 640, 3001, 512, True, True, False, True),      # three 256-column tiles of H: 256 x 256 dX / dW tiles
+    (900, 640, 3001, 0, False, False, True, False),      # the same, one wave, bf16 dW
 ])
 def test_fused_and_split_bit_identical(flp, M, H, V, chunk, ent, dx_f32, dw_bf16, acc):
     """Both schedules run every output tile with the same instructions in the
