@@ -261,9 +261,10 @@ __device__ __forceinline__ void store_box_release(StoreRing& ring, uint8_t* smem
 // Narrow store boxes: 128 rows x 64 bytes (32 bf16 or 16 fp32 columns,
 // 64-byte swizzle), two per epilogue group, so that two groups fit the store
 // region.  One box of this thread's row (16 words) is staged and stored (or
-// added) in its group's ring; before a box is rewritten, the bulk store that
-// last read it must have finished reading (thread 0 of the group waits, the
-// group's named barrier hands that on).
+// added) in its group's ring, with one named barrier per box: before it,
+// thread 0 of the group waits until every earlier bulk store has finished
+// reading, so after it the other box (read by the previous store) may be
+// rewritten by the next call while this box's store runs.
 constexpr uint32_t NBOX_BYTES = BM * 64;
 static_assert(2 * 2 * NBOX_BYTES <= NUM_STG * STG_BYTES, "two narrow boxes per epilogue group");
 
@@ -271,16 +272,15 @@ __device__ __forceinline__ void narrow_box_store(StoreRing& ring, uint8_t* box0,
                                                  const uint32_t* w, const CUtensorMap* out, int x, int y,
                                                  bool add) {
     const uint32_t buf = ring.n & 1u;
-    if (ring.n >= 2) {
-        if (et == 0) bulk_wait_group_read<1>();
-        named_bar_sync(bar_id, EPI_THREADS);
-    }
+    // box buf was last read by the store two boxes back, which thread 0
+    // waited for before the previous call's barrier
     uint8_t* box = box0 + buf * NBOX_BYTES;
     const uint32_t row_addr = smem_addr(box) + r * 64;
 #pragma unroll
     for (int c = 0; c < 4; ++c)
         st_shared_v4(row_addr + ((c ^ ((r >> 1) & 3)) << 4), w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
     fence_proxy_async_smem();
+    if (et == 0) bulk_wait_group_read<0>();  // the other box is free again after the barrier
     named_bar_sync(bar_id, EPI_THREADS);
     if (et == 0) {
         if (add)
