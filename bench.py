@@ -500,7 +500,7 @@ def run_ours(args, world, rank, local):
     torch.cuda.empty_cache()
     if args.workloads == "baseline" and w.name == inputs.HEADLINE:
         result["workloads"] = {n: time_extra_workload(n, args, flp, dev, args.schedule)
-                               for n in inputs.BASELINE_OTHERS}
+                               for n in inputs.REPORTED_WORKLOADS}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(d, w, args.cpu_seconds)
     if rank == 0:
