@@ -87,7 +87,7 @@ WORKLOADS = {
 HEADLINE = "m4096_h4096_v131072"
 # the other synthetic workloads timed beside the headline (tiny, temperature 0.7, ragged, large)
 REPORTED_WORKLOADS = ("tiny", "m8192_h8192_v131072", "ragged_m20001_h4096_v128257",
-                   "large_m32768_h5120_v152064")
+                      "large_m32768_h5120_v152064")
 
 
 def custom(name: str, M: int, H: int, V: int, **kw) -> Workload:
